@@ -1,0 +1,98 @@
+"""Pins of the planner oracle (CPU): brute-force coverage checks and invariants."""
+import numpy as np
+import torch
+
+from oracle import planner as PL
+from paged_kv_block_gb300 import workloads as W
+from tests import bruteforce as BF
+
+
+def _check_order(recs, natural_key):
+    cost = recs[:, 5] - recs[:, 4]
+    assert np.all(np.diff(cost) <= 0)
+    for c in np.unique(cost):
+        sub = recs[cost == c]
+        keys = [natural_key(r) for r in sub]
+        assert keys == sorted(keys)
+
+
+def test_bsr_tiles_cover_every_row_once():
+    B, Sq, Hq, Hkv, qbs = 2, 50, 8, 2, 12
+    p = W.make_bsr_problem(1, B=B, Sq=Sq, Hq=Hq, Hkv=Hkv, D=8, seq_lens=[70, 55], page_size=4,
+                           qbs=qbs, kvbs=4, policy="random", p=0.4)
+    tt = 5
+    recs = PL.plan_bsr_tiles(B, Sq, Hq, Hkv, qbs, p["block_indptr"], tt)
+    assert len(recs) == PL.bsr_tile_capacity(B, Sq, Hkv, qbs, tt)
+    seen = np.zeros((B, Hkv, Sq), int)
+    bptr = p["block_indptr"].numpy()
+    for b, g, tok0, ntok, kb, ke, qrow, z in recs:
+        assert 1 <= ntok <= tt and z == 0 and qrow == b * Sq + tok0
+        r = tok0 // qbs
+        assert (tok0 + ntok - 1) // qbs == r                      # never crosses a q-block
+        assert (kb, ke) == (bptr[b, g, r], bptr[b, g, r + 1])
+        seen[b, g, tok0:tok0 + ntok] += 1
+    assert np.all(seen == 1)
+    _check_order(recs, lambda r: (r[0], r[1], r[2]))
+
+
+def test_prefill_tiles_hold_exactly_the_visible_key_span():
+    for mask, w in (("causal", -1), ("causal", 37), ("dense", -1), ("causal", 0)):
+        p = W.make_prefill_problem(2, q_lens=[130, 7, 300], prefix_lens=[0, 250, 90], Hq=4,
+                                   Hkv=2, D=8, page_size=16, mask_type=mask, window_left=w)
+        tt = 32
+        recs = PL.plan_prefill_tiles(2, p["qo_indptr"], p["seq_lens_kv"], tt, mask, w)
+        qo = p["qo_indptr"].numpy()
+        seen = {}
+        for b, g, tok0, ntok, kb, ke, qrow, _ in recs:
+            assert qrow == qo[b] + tok0
+            vis = set()
+            for i in range(tok0, tok0 + ntok):
+                vis.update(BF.prefill_visible(p, b, i))
+                seen[(b, g, i)] = seen.get((b, g, i), 0) + 1
+            if not vis:
+                assert kb == ke == 0
+                continue
+            assert kb == min(vis) // 128 and ke == max(vis) // 128 + 1
+        assert all(v == 1 for v in seen.values())
+        assert len(seen) == 2 * int(qo[-1])
+        _check_order(recs, lambda r: (r[0], r[1], r[2]))
+
+
+def test_decode_splits_partition_the_visible_keys():
+    lens = [1, 127, 128, 129, 1000, 5]
+    for w in (-1, 0, 200):
+        for chunk in (128, 256, 1024):
+            off, items = PL.plan_decode(lens, 3, chunk, w)
+            assert off[0] == 0 and np.all(np.diff(off) >= 1)
+            assert len(items) == 3 * off[-1]
+            for b, L in enumerate(lens):
+                n = off[b + 1] - off[b]
+                lo = max(0, L - 1 - w) if w >= 0 else 0
+                for g in range(3):
+                    rows = items[3 * off[b] + g * n: 3 * off[b] + (g + 1) * n]
+                    assert np.all(rows[:, 0] == b) and np.all(rows[:, 1] == g)
+                    assert rows[0, 2] == lo and rows[-1, 3] == L
+                    assert np.all(rows[1:, 2] == rows[:-1, 3])
+                    assert np.all(rows[:, 3] - rows[:, 2] <= chunk)
+                    assert np.all(rows[1:, 2] % chunk == 0)
+
+
+def test_decode_chunk_formula():
+    assert PL.decode_split_chunk(64, 8, 8192, 152) == 512
+    assert PL.decode_split_chunk(1, 1, 100, 152) == 128
+    assert PL.decode_split_chunk(4096, 8, 1000, 148) == 128 * 8
+    assert PL.decode_split_chunk(4096, 8, 1 << 20, 148) % 128 == 0
+
+
+def test_bitmap_csr_matches_bruteforce():
+    p = W.make_qsa_problem(3, [16, 24, 8], Hq=2, Hkv=1, D=8, block_size=4, n_near=2,
+                           n_random=3)
+    p["lo"] = p["lo"] + torch.tensor([(t % 3) for t in range(48)], dtype=torch.int32)
+    indptr, indices = PL.plan_bitmap(p["sel_blocks"], p["lo"], p["hi"], p["block_first"],
+                                     p["block_last"])
+    first = p["block_first"].numpy()
+    for t in range(48):
+        got = indices[indptr[t]:indptr[t + 1]].tolist()
+        js = BF.qsa_visible(p, t)
+        blocks = sorted(set(int(np.searchsorted(first, j, side="right") - 1) for j in js))
+        assert got == blocks
