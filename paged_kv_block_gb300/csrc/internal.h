@@ -1,0 +1,118 @@
+// Declarations shared by the translation units of libpagedattn (not part of the ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+// Tile record written by the planner and read by the prefill / block-sparse kernel:
+// b, g, tok0, ntok, kv_begin, kv_end, q_row0, 0.
+struct TileRec {
+  int b, g, tok0, ntok, kv_begin, kv_end, q_row0, pad;
+};
+
+// Split-KV work item of the decode kernel.
+struct SplitItem {
+  int b, g, kv_begin, kv_end;
+};
+
+constexpr int kSortChunk = 1024;     // records per counting-sort chunk
+constexpr int kMaxSortCost = 4095;   // costs are capped at this value for ordering
+constexpr int kKvTile = 128;         // keys per KV tile of the prefill kernel
+constexpr int kMTileRows = 128;      // rows per Q sub-tile (one TMEM lane per row)
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+inline long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
+
+// Tokens per Q sub-tile: floor(128 / G); a CTA holds two sub-tiles.
+inline int sub_tile_tokens(int G) { return kMTileRows / G; }
+inline int cta_tile_tokens(int G) { return 2 * sub_tile_tokens(G); }
+
+// ---- planner launchers (planner.cu) ----------------------------------------------------
+// All write the status word on capacity problems; none synchronises the host.
+void launch_bsr_tiles(const int* block_indptr, int B, int Hkv, int Sq, int qbs, int tile_tokens,
+                      TileRec* tmp, cudaStream_t st);
+void launch_prefill_tiles(const int* qo_indptr, const int* seq_lens, int B, int Hkv,
+                          int tile_tokens, int causal, int window_left, int capacity,
+                          int* tile_offsets, int* n_tiles, TileRec* tmp, uint32_t* status,
+                          cudaStream_t st);
+// Stable sort of n records (n_dev: device count, or nullptr to use n_static) by
+// min(kv_end - kv_begin, max_cost) descending.
+void launch_tile_sort(const TileRec* in, TileRec* out, const int* n_dev, int n_static,
+                      int capacity, int max_cost, int* hist, int* offs, cudaStream_t st);
+size_t tile_sort_scratch_ints(int capacity, int max_cost);
+
+void launch_bitmap_plan(const uint8_t* sel, const int* lo, const int* hi, const int* bfirst,
+                        const int* blast, int T, int NB, long long capacity, int* indptr,
+                        int* indices, uint32_t* status, cudaStream_t st);
+
+void launch_decode_plan(const int* seq_lens, int B, int Hkv, int chunk, int window_left,
+                        int max_splits, int* split_offset, SplitItem* items, cudaStream_t st);
+
+// Keys per sub-chunk of a 128-key KV tile: the largest of 128, 64 or kv_block_size that
+// divides kv_block_size (dense tiles use 128).
+inline int attn_sub_chunk(int kv_block_size, bool block_sparse) {
+  if (!block_sparse) return kKvTile;
+  if (kv_block_size % kKvTile == 0) return kKvTile;
+  if (kv_block_size % 64 == 0) return 64;
+  return kv_block_size;
+}
+
+// ---- kernels launchers ------------------------------------------------------------------
+struct DecodeLaunch {
+  const CUtensorMap* kmap;   // host copies, passed by value to the kernel
+  const CUtensorMap* vmap;
+  const __nv_bfloat16* q;    // [B, Hq, D]
+  const int* kv_indptr;
+  const int* kv_indices;
+  const int* seq_lens;
+  const int* split_offset;
+  const SplitItem* items;
+  float* part_o;             // [items, G, D]
+  float* part_lse;           // [items, G]
+  __nv_bfloat16* out;        // [B, Hq, D]
+  float* lse;                // [B, Hq] or nullptr
+  uint32_t* status;
+  int B, Hq, Hkv, D, page_size, page_rows, k_head_off, v_head_off, num_pages;
+  int capacity;              // launched work items
+  float scale_log2, out_scale;
+  int window_left;
+};
+int launch_decode(const DecodeLaunch& a, cudaStream_t st);
+
+struct AttnLaunch {
+  CUtensorMap qmap, kmap, vmap;
+  const TileRec* tiles;
+  const int* n_tiles;        // device count (nullptr: all `capacity` tiles are live)
+  int capacity;
+  // page table: CSR (pt_indptr != nullptr) or row-strided (pt_stride)
+  const int* pt;
+  const int* pt_indptr;
+  int pt_stride;
+  const int* seq_lens;
+  const int* qo_indptr;      // packed-Q form: nq of request b; nullptr -> fixed q_len
+  int q_len;
+  const uint32_t* valid_bits;
+  int valid_words;
+  const int* block_indices;  // BSR form; nullptr -> dense KV tiles
+  int kv_block_size;
+  __nv_bfloat16* out;
+  float* lse;
+  uint32_t* status;
+  int Hq, Hkv, G, D, page_size, page_rows, k_head_off, v_head_off, num_pages;
+  int causal, window_left;
+  float scale_log2, out_scale;
+};
+int launch_attn(const AttnLaunch& a, cudaStream_t st);
+
+// ---- tensor maps (api.cu) -----------------------------------------------------------------
+bool encode_rows_map(CUtensorMap* map, const void* base, long long rows, int D, int box_rows);
+bool encode_q_map(CUtensorMap* map, const void* base, long long rows, int Hq, int D,
+                  int box_heads, int box_tokens);
+
+}  // namespace pa

@@ -1,0 +1,408 @@
+// Device-side work planner: expands BSR rows, packed-Q prefill requests, per-query block
+// bitmaps and decode requests into the work lists the attention kernels consume.  All
+// outputs are integers with one correct value each (deterministic ordering, no atomics
+// whose order matters), so they can be compared bit for bit with a reference planner.
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pa {
+namespace {
+
+// Exclusive scan of one int per thread over a CTA of blockDim.x (a multiple of 32, <=1024)
+// threads.  `total` receives the sum over the CTA.
+__device__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int s = lane < nw ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_sums[lane] = s;
+  }
+  __syncthreads();
+  const int before = w > 0 ? warp_sums[w - 1] : 0;
+  total = warp_sums[nw - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+// ---- block-sparse tiles ----------------------------------------------------------------
+// One thread per BSR row (b, g, r).  Tile (b, g, r, m) goes to natural index
+// (b * Hkv + g) * tiles_per_bg + r * ceil(qbs / tt) + m.
+__global__ void bsr_tiles_kernel(const int* __restrict__ block_indptr, int B, int Hkv, int Sq,
+                                 int qbs, int tt, TileRec* __restrict__ tmp) {
+  const int nqb = (Sq + qbs - 1) / qbs;
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= B * Hkv * nqb) return;
+  const int r = row % nqb, bg = row / nqb, g = bg % Hkv, b = bg / Hkv;
+  const int full_tiles = (qbs + tt - 1) / tt;
+  const int last_n = Sq - (nqb - 1) * qbs;
+  const int tiles_per_bg = (nqb - 1) * full_tiles + (last_n + tt - 1) / tt;
+  const int n_r = min(qbs, Sq - r * qbs);
+  const int base = bg * tiles_per_bg + r * full_tiles;
+  const int kb = block_indptr[bg * (nqb + 1) + r];
+  const int ke = block_indptr[bg * (nqb + 1) + r + 1];
+  for (int m = 0; m * tt < n_r; ++m) {
+    TileRec t;
+    t.b = b;
+    t.g = g;
+    t.tok0 = r * qbs + m * tt;
+    t.ntok = min(tt, n_r - m * tt);
+    t.kv_begin = kb;
+    t.kv_end = ke;
+    t.q_row0 = b * Sq + t.tok0;
+    t.pad = 0;
+    tmp[base + m] = t;
+  }
+}
+
+// ---- packed-Q prefill tiles --------------------------------------------------------------
+__global__ void prefill_count_kernel(const int* __restrict__ qo, int B, int Hkv, int tt,
+                                     int capacity, int* __restrict__ off, int* n_tiles,
+                                     uint32_t* status) {
+  __shared__ int warp_sums[32];
+  int carry = 0;
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    int c = 0;
+    if (b < B) {
+      const int nq = qo[b + 1] - qo[b];
+      c = nq > 0 ? (nq + tt - 1) / tt : 0;
+    }
+    int total;
+    const int ex = block_exclusive_scan(c, warp_sums, total);
+    if (b < B) off[b] = carry + ex;
+    carry += total;
+  }
+  if (threadIdx.x == 0) {
+    off[B] = carry;
+    long long n = static_cast<long long>(Hkv) * carry;
+    if (n > capacity) {
+      report_error(status, kErrCapacity);
+      n = capacity;
+    }
+    *n_tiles = static_cast<int>(n);
+  }
+}
+
+__global__ void prefill_fill_kernel(const int* __restrict__ qo, const int* __restrict__ lens,
+                                    int Hkv, int tt, int causal, int window_left, int capacity,
+                                    const int* __restrict__ off, TileRec* __restrict__ tmp) {
+  const int b = blockIdx.x;
+  const int nq = qo[b + 1] - qo[b];
+  const int L = lens[b];
+  const int nt = off[b + 1] - off[b];
+  for (int idx = threadIdx.x; idx < Hkv * nt; idx += blockDim.x) {
+    const int g = idx / nt, m = idx % nt;
+    const long long pos = static_cast<long long>(Hkv) * off[b] + idx;
+    if (pos >= capacity) continue;
+    const int tok0 = m * tt;
+    const int ntok = min(tt, nq - tok0);
+    const long long p0 = static_cast<long long>(L) - nq + tok0;
+    const long long p1 = p0 + ntok - 1;
+    const long long hi = causal ? min(static_cast<long long>(L), p1 + 1) : L;
+    const long long lo = (causal && window_left >= 0) ? max(0LL, p0 - window_left) : 0LL;
+    TileRec t;
+    t.b = b;
+    t.g = g;
+    t.tok0 = tok0;
+    t.ntok = ntok;
+    if (hi <= lo) {
+      t.kv_begin = t.kv_end = 0;
+    } else {
+      t.kv_begin = static_cast<int>(lo / kKvTile);
+      t.kv_end = static_cast<int>((hi + kKvTile - 1) / kKvTile);
+    }
+    t.q_row0 = qo[b] + tok0;
+    t.pad = 0;
+    tmp[pos] = t;
+  }
+}
+
+// ---- stable counting sort of tiles by capped cost, descending ------------------------------
+__device__ __forceinline__ int rec_cost(const TileRec& r, int maxc) {
+  const int c = r.kv_end - r.kv_begin;
+  return c < 0 ? 0 : (c > maxc ? maxc : c);
+}
+
+__global__ void sort_hist_kernel(const TileRec* __restrict__ in, const int* n_dev, int n_static,
+                                 int maxc, int* __restrict__ hist) {
+  extern __shared__ int h[];
+  const int n = n_dev ? *n_dev : n_static;
+  for (int k = threadIdx.x; k <= maxc; k += blockDim.x) h[k] = 0;
+  __syncthreads();
+  const int i = blockIdx.x * kSortChunk + threadIdx.x;
+  if (i < n) atomicAdd(&h[rec_cost(in[i], maxc)], 1);
+  __syncthreads();
+  for (int k = threadIdx.x; k <= maxc; k += blockDim.x)
+    hist[static_cast<long long>(blockIdx.x) * (maxc + 1) + k] = h[k];
+}
+
+__global__ void sort_offsets_kernel(int nchunks, int maxc, const int* __restrict__ hist,
+                                    int* __restrict__ offs) {
+  extern __shared__ int tot[];
+  __shared__ int warp_sums[32];
+  const long long W = maxc + 1;
+  for (int k = threadIdx.x; k <= maxc; k += blockDim.x) {
+    int run = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = hist[c * W + k];
+      offs[c * W + k] = run;
+      run += v;
+    }
+    tot[k] = run;
+  }
+  __syncthreads();
+  // base[k] = number of records with a larger cost: scan the bins from the top.
+  int carry = 0;
+  for (int d0 = 0; d0 <= maxc; d0 += blockDim.x) {
+    const int d = d0 + threadIdx.x;
+    const int v = d <= maxc ? tot[maxc - d] : 0;
+    int total;
+    const int ex = block_exclusive_scan(v, warp_sums, total);
+    if (d <= maxc) tot[maxc - d] = carry + ex;
+    carry += total;
+  }
+  __syncthreads();
+  for (int k = threadIdx.x; k <= maxc; k += blockDim.x)
+    for (int c = 0; c < nchunks; ++c) offs[c * W + k] += tot[k];
+}
+
+__global__ void sort_scatter_kernel(const TileRec* __restrict__ in, TileRec* __restrict__ out,
+                                    const int* n_dev, int n_static, int maxc,
+                                    const int* __restrict__ offs) {
+  extern __shared__ int cnt[];
+  const int n = n_dev ? *n_dev : n_static;
+  for (int k = threadIdx.x; k <= maxc; k += blockDim.x) cnt[k] = 0;
+  __syncthreads();
+  const int i = blockIdx.x * kSortChunk + threadIdx.x;
+  const bool live = i < n;
+  const int k = live ? rec_cost(in[i], maxc) : -1;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const unsigned peers = __match_any_sync(0xffffffffu, k);
+  const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
+  const int leader = __ffs(peers) - 1;
+  int my_base = 0;
+  // Warps take their turn in index order, so equal costs keep their input order.
+  for (int step = 0; step < (kSortChunk >> 5); ++step) {
+    if (w == step) {
+      if (live) my_base = cnt[k];
+      __syncwarp();
+      if (live && lane == leader) cnt[k] = my_base + __popc(peers);
+    }
+    __syncthreads();
+  }
+  if (live) {
+    const long long pos =
+        offs[static_cast<long long>(blockIdx.x) * (maxc + 1) + k] + my_base + rank_in_warp;
+    out[pos] = in[i];
+  }
+}
+
+// ---- bitmap planner ------------------------------------------------------------------------
+__device__ __forceinline__ int first_block_ending_at_or_after(const int* __restrict__ blast,
+                                                              int NB, int lo) {
+  int a = 0, b = NB;
+  while (a < b) {
+    const int m = (a + b) >> 1;
+    if (blast[m] < lo) a = m + 1;
+    else b = m;
+  }
+  return a;
+}
+
+// One warp per query token; lane l looks at blocks base + 4l .. base + 4l + 3.
+template <bool kFill>
+__global__ void bitmap_scan_kernel(const uint8_t* __restrict__ sel, const int* __restrict__ lo,
+                                   const int* __restrict__ hi, const int* __restrict__ bfirst,
+                                   const int* __restrict__ blast, int T, int NB,
+                                   int* __restrict__ counts, const int* __restrict__ indptr,
+                                   int* __restrict__ indices, long long capacity) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int l = lo[t], h = hi[t];
+  long long written = kFill ? indptr[t] : 0;
+  int cnt = 0;
+  if (h >= l) {
+    const int g0 = first_block_ending_at_or_after(blast, NB, l);
+    const long long rowbase = static_cast<long long>(t) * NB;
+    for (int base = g0; base < NB; base += 128) {
+      bool stop = false;
+      int mine[4];
+      int c = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int g = base + lane * 4 + e;
+        if (g < NB) {
+          const int f = bfirst[g];
+          if (f > h) {
+            stop = true;
+          } else if (sel[rowbase + g] != 0 && max(f, l) <= min(blast[g], h)) {
+            mine[c++] = g;
+          }
+        }
+      }
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      if (kFill) {
+        const long long at = written + incl - c;
+        for (int e = 0; e < c; ++e)
+          if (at + e < capacity) indices[at + e] = mine[e];
+      }
+      written += total;
+      cnt += total;
+      if (__any_sync(0xffffffffu, stop)) break;
+    }
+  }
+  if (!kFill && lane == 0) counts[t] = cnt;
+}
+
+__global__ void counts_to_indptr_kernel(const int* __restrict__ counts, int T, long long capacity,
+                                        int* __restrict__ indptr, uint32_t* status) {
+  __shared__ int warp_sums[32];
+  long long carry = 0;
+  for (int base = 0; base < T; base += blockDim.x) {
+    const int t = base + threadIdx.x;
+    const int c = t < T ? counts[t] : 0;
+    int total;
+    const int ex = block_exclusive_scan(c, warp_sums, total);
+    if (t < T) indptr[t] = static_cast<int>(carry + ex);
+    carry += total;
+  }
+  if (threadIdx.x == 0) {
+    indptr[T] = static_cast<int>(carry);
+    if (carry > capacity) report_error(status, kErrCapacity);
+  }
+}
+
+// ---- decode split planner -----------------------------------------------------------------
+__device__ __forceinline__ void decode_split_range(int L, int chunk, int window_left, int& lo,
+                                                   int& s0, int& n) {
+  if (L < 0) L = 0;
+  lo = window_left >= 0 ? max(0, L - 1 - window_left) : 0;
+  s0 = lo / chunk;
+  const int s1 = max((L + chunk - 1) / chunk, s0 + 1);
+  n = s1 - s0;
+}
+
+__global__ void decode_plan_kernel(const int* __restrict__ lens, int B, int chunk,
+                                   int window_left, int max_splits, int* __restrict__ off) {
+  __shared__ int warp_sums[32];
+  int carry = 0;
+  for (int base = 0; base < B; base += blockDim.x) {
+    const int b = base + threadIdx.x;
+    int n = 0;
+    if (b < B) {
+      int lo, s0;
+      decode_split_range(lens[b], chunk, window_left, lo, s0, n);
+      n = min(n, max_splits);
+    }
+    int total;
+    const int ex = block_exclusive_scan(n, warp_sums, total);
+    if (b < B) off[b] = carry + ex;
+    carry += total;
+  }
+  if (threadIdx.x == 0) off[B] = carry;
+}
+
+__global__ void decode_items_kernel(const int* __restrict__ lens, int Hkv, int chunk,
+                                    int window_left, const int* __restrict__ off,
+                                    SplitItem* __restrict__ items) {
+  const int b = blockIdx.x;
+  int L = lens[b];
+  int lo, s0, n_all;
+  decode_split_range(L, chunk, window_left, lo, s0, n_all);
+  if (L < 0) L = 0;
+  const int n = off[b + 1] - off[b];
+  for (int idx = threadIdx.x; idx < Hkv * n; idx += blockDim.x) {
+    const int g = idx / n, k = idx % n;
+    const long long s = static_cast<long long>(s0) + k;
+    SplitItem it;
+    it.b = b;
+    it.g = g;
+    it.kv_begin = static_cast<int>(max(s * chunk, static_cast<long long>(lo)));
+    it.kv_end = static_cast<int>(min((s + 1) * chunk, static_cast<long long>(L)));
+    items[static_cast<long long>(Hkv) * off[b] + idx] = it;
+  }
+}
+
+}  // namespace
+
+// ---- launchers ---------------------------------------------------------------------------
+void launch_bsr_tiles(const int* block_indptr, int B, int Hkv, int Sq, int qbs, int tile_tokens,
+                      TileRec* tmp, cudaStream_t st) {
+  const int rows = B * Hkv * ceil_div(Sq, qbs);
+  if (rows <= 0) return;
+  bsr_tiles_kernel<<<ceil_div(rows, 256), 256, 0, st>>>(block_indptr, B, Hkv, Sq, qbs,
+                                                        tile_tokens, tmp);
+}
+
+void launch_prefill_tiles(const int* qo_indptr, const int* seq_lens, int B, int Hkv,
+                          int tile_tokens, int causal, int window_left, int capacity,
+                          int* tile_offsets, int* n_tiles, TileRec* tmp, uint32_t* status,
+                          cudaStream_t st) {
+  prefill_count_kernel<<<1, 1024, 0, st>>>(qo_indptr, B, Hkv, tile_tokens, capacity,
+                                           tile_offsets, n_tiles, status);
+  if (B > 0)
+    prefill_fill_kernel<<<B, 256, 0, st>>>(qo_indptr, seq_lens, Hkv, tile_tokens, causal,
+                                           window_left, capacity, tile_offsets, tmp);
+}
+
+size_t tile_sort_scratch_ints(int capacity, int max_cost) {
+  const size_t nchunks = static_cast<size_t>(ceil_div(capacity > 0 ? capacity : 1, kSortChunk));
+  return nchunks * static_cast<size_t>(max_cost + 1);
+}
+
+void launch_tile_sort(const TileRec* in, TileRec* out, const int* n_dev, int n_static,
+                      int capacity, int max_cost, int* hist, int* offs, cudaStream_t st) {
+  if (capacity <= 0) return;
+  const int nchunks = ceil_div(capacity, kSortChunk);
+  const size_t sm = static_cast<size_t>(max_cost + 1) * sizeof(int);
+  sort_hist_kernel<<<nchunks, kSortChunk, sm, st>>>(in, n_dev, n_static, max_cost, hist);
+  sort_offsets_kernel<<<1, 1024, sm, st>>>(nchunks, max_cost, hist, offs);
+  sort_scatter_kernel<<<nchunks, kSortChunk, sm, st>>>(in, out, n_dev, n_static, max_cost,
+                                                       offs);
+}
+
+void launch_bitmap_plan(const uint8_t* sel, const int* lo, const int* hi, const int* bfirst,
+                        const int* blast, int T, int NB, long long capacity, int* indptr,
+                        int* indices, uint32_t* status, cudaStream_t st) {
+  if (T <= 0) return;
+  const int warps_per_cta = 8;
+  const int grid = ceil_div(T, warps_per_cta);
+  // counts are staged in indices' tail-free scratch: indptr[1..T] first holds the counts
+  bitmap_scan_kernel<false><<<grid, 32 * warps_per_cta, 0, st>>>(
+      sel, lo, hi, bfirst, blast, T, NB, indptr + 1, nullptr, nullptr, capacity);
+  counts_to_indptr_kernel<<<1, 1024, 0, st>>>(indptr + 1, T, capacity, indptr, status);
+  bitmap_scan_kernel<true><<<grid, 32 * warps_per_cta, 0, st>>>(
+      sel, lo, hi, bfirst, blast, T, NB, nullptr, indptr, indices, capacity);
+}
+
+void launch_decode_plan(const int* seq_lens, int B, int Hkv, int chunk, int window_left,
+                        int max_splits, int* split_offset, SplitItem* items, cudaStream_t st) {
+  decode_plan_kernel<<<1, 1024, 0, st>>>(seq_lens, B, chunk, window_left, max_splits,
+                                         split_offset);
+  if (B > 0)
+    decode_items_kernel<<<B, 256, 0, st>>>(seq_lens, Hkv, chunk, window_left, split_offset,
+                                           items);
+}
+
+}  // namespace pa
