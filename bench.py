@@ -1,0 +1,576 @@
+#!/usr/bin/env python
+"""Benchmark of the paged-KV attention forward library on one GB300.
+
+Headline (one JSON line): the paged decode workload (B=64, Hq=32, Hkv=8, D=128, lens
+U[512, 8192], combined cache, page 16, split-KV), as KV GB/s over the live K/V bytes.  A step
+is one call of paged_decode_run: device planner, split-KV partial kernel and merge.  The
+other named workloads (block-sparse, packed prefill, bitmap) are measured in the same run and
+reported under "per_config" as tensor TFLOPS over visible (selected, unmasked, valid) pairs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--no-extra] [--skip-cpu]
+
+Under torchrun each rank runs the same workload on its own GPU (replicas: the path has no
+exchange step), the timed region is bracketed by a barrier and synchronisation on both
+sides, and the slowest rank's time is reported.  --impl reference times the float64 CPU
+oracle on a bounded sample of the workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import paged_kv_block_gb300 as pkb  # noqa: E402
+from paged_kv_block_gb300 import workloads as W  # noqa: E402
+
+METRIC = "sparse/prefill attn TFLOPS & decode KV GB/s; % of tensor/HBM roofline, 1 GB300"
+HEADLINE = "decode_b64"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------------------
+# environment
+# ----------------------------------------------------------------------------------------
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            self.path = f"/tmp/pkb_clocks_{os.getpid()}.csv"
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "decode_split_kernel": ["paged_kv_block_gb300/csrc/decode.cu",
+                            "paged_kv_block_gb300/csrc/common.cuh"],
+    "attn_tc_kernel": ["paged_kv_block_gb300/csrc/attn_tc.cu",
+                       "paged_kv_block_gb300/csrc/common.cuh"],
+}
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, or None when the kernel's
+    source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(kernel, {}).get(workload)
+    if not e or e.get("source_hash") != source_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------------------
+# work accounting (independent of the checker package)
+# ----------------------------------------------------------------------------------------
+
+def decode_kv_bytes(p):
+    Hkv = p["kv_cache"].shape[2]
+    D = p["kv_cache"].shape[-1]
+    return int(p["seq_lens"].to(torch.int64).sum()) * Hkv * D * 2 * 2
+
+
+def bsr_pairs(p):
+    q = p["q"]
+    B, Sq, Hq, _ = q.shape
+    Hkv = (p["k_cache"] if "k_cache" in p else p["kv_cache"][:, 0]).shape[1]
+    G = Hq // Hkv
+    qbs, kvbs = p["q_block_size"], p["kv_block_size"]
+    nqb = -(-Sq // qbs)
+    bptr = p["block_indptr"].numpy().astype(np.int64)
+    bidx = p["block_indices"].numpy().astype(np.int64)
+    lens = p["seq_lens_kv"].numpy().astype(np.int64)
+    words = p["kv_valid_bits"].numpy().view(np.uint32) if p["kv_valid_bits"] is not None else None
+    total = 0
+    for b in range(B):
+        L = int(lens[b])
+        live = np.ones(L, bool)
+        if words is not None:
+            j = np.arange(L)
+            live = ((words[b][j >> 5] >> (j & 31).astype(np.uint32)) & 1).astype(bool)
+        for g in range(Hkv):
+            for r in range(nqb):
+                blocks = bidx[bptr[b, g, r]:bptr[b, g, r + 1]]
+                keys = (blocks[:, None] * kvbs + np.arange(kvbs)[None, :]).ravel()
+                keys = keys[keys < L]
+                keys = np.sort(keys[live[keys]])
+                rows = np.arange(r * qbs, min((r + 1) * qbs, Sq))
+                if p["mask_type"] == "causal":
+                    total += int(np.searchsorted(keys, L - Sq + rows, side="right").sum())
+                else:
+                    total += keys.size * rows.size
+    return total * G
+
+
+def prefill_pairs(p):
+    qo = p["qo_indptr"].numpy().astype(np.int64)
+    lens = p["seq_lens_kv"].numpy().astype(np.int64)
+    Hq = p["q"].shape[1]
+    w = p["window_left"]
+    total = 0
+    for b in range(lens.size):
+        nq, L = int(qo[b + 1] - qo[b]), int(lens[b])
+        if p["mask_type"] != "causal":
+            total += nq * L
+            continue
+        pos = L - nq + np.arange(nq)
+        hi = np.minimum(pos + 1, L)
+        lo = np.maximum(pos - w, 0) if w >= 0 else np.zeros_like(pos)
+        total += int(np.maximum(hi - lo, 0).sum())
+    return total * Hq
+
+
+def qsa_pairs(p):
+    sel = p["sel_blocks"].numpy()
+    t, g = np.nonzero(sel)
+    lo, hi = p["lo"].numpy()[t].astype(np.int64), p["hi"].numpy()[t].astype(np.int64)
+    first = p["block_first"].numpy()[g].astype(np.int64)
+    last = p["block_last"].numpy()[g].astype(np.int64)
+    return int(np.maximum(np.minimum(last, hi) - np.maximum(first, lo) + 1, 0).sum()) * \
+        p["q"].shape[1]
+
+
+# ----------------------------------------------------------------------------------------
+# one workload on the GPU
+# ----------------------------------------------------------------------------------------
+
+def make_workload(name):
+    if name == "decode_b64":
+        return W.decode_b64()
+    if name == "tiny_bsr":
+        return W.tiny_bsr()
+    if name == "prefill_b16":
+        return W.prefill_b16(window_left=-1)
+    if name == "prefill_b16_w1023":
+        return W.prefill_b16(window_left=1023)
+    if name == "long_bsr":
+        return W.long_bsr()
+    if name == "qsa_t32k":
+        return W.qsa_t32k()
+    raise ValueError(name)
+
+
+def describe(name, p):
+    if p["form"] == "decode":
+        return {"workload": name, "batch": int(p["q"].shape[0]), "num_qo_heads": int(p["q"].shape[1]),
+                "num_kv_heads": int(p["kv_cache"].shape[2]), "head_dim": int(p["q"].shape[2]),
+                "page_size": int(p["page_size"]), "seq_lens": "U[512,8192]",
+                "total_kv_tokens": int(p["seq_lens"].sum()), "cache": "combined [P,2,Hkv,ps,D]",
+                "mask": p["mask_type"], "split_kv": True}
+    if p["form"] == "bsr":
+        return {"workload": name, "batch": int(p["q"].shape[0]), "q_len": int(p["q"].shape[1]),
+                "num_qo_heads": int(p["q"].shape[2]), "page_size": int(p["page_size"]),
+                "q_block_size": p["q_block_size"], "kv_block_size": p["kv_block_size"],
+                "selected_blocks": int(p["block_indices"].numel()), "mask": p["mask_type"],
+                "kv_valid_bits": p["kv_valid_bits"] is not None}
+    if p["form"] == "prefill":
+        return {"workload": name, "batch": int(p["seq_lens_kv"].numel()),
+                "total_q": int(p["q"].shape[0]), "num_qo_heads": int(p["q"].shape[1]),
+                "page_size": int(p["page_size"]), "mask": p["mask_type"],
+                "window_left": p["window_left"]}
+    return {"workload": name, "tokens": int(p["q"].shape[0]), "num_qo_heads": int(p["q"].shape[1]),
+            "head_dim": int(p["q"].shape[2]), "num_blocks": int(p["sel_blocks"].shape[1])}
+
+
+class Runner:
+    """Owns the device copies of one workload and runs one step through the C ABI."""
+
+    def __init__(self, p, dev):
+        self.p = p
+        self.dev = dev
+        self.d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+        d = self.d
+        self.form = p["form"]
+        if self.form == "decode":
+            self.params = pkb.decode_params(d["q"], d["kv_cache"], p["max_seq_len"],
+                                            bmm1_scale=p["sm_scale"], bmm2_scale=p["bmm2_scale"],
+                                            mask_type=p["mask_type"],
+                                            window_left=p["window_left"])
+            self.ws = torch.empty(pkb.paged_decode_workspace_size(self.params), dtype=torch.uint8,
+                                  device=dev)
+            self.out = torch.empty_like(d["q"])
+            self.lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
+        elif self.form == "bsr":
+            cache = d["kv_cache"] if "kv_cache" in d else (d["k_cache"], d["v_cache"])
+            self.k, self.v = (cache, None) if not isinstance(cache, tuple) else cache
+            self.params = pkb.bsr_params(d["q"], cache, p["q_block_size"], p["kv_block_size"],
+                                         p["max_seq_len_kv"],
+                                         has_valid_bits=p["kv_valid_bits"] is not None,
+                                         mask_type=p["mask_type"], sm_scale=p["sm_scale"])
+            self.meta = pkb.bsr_meta(d["kv_indptr"], d["kv_indices"], d["block_indptr"],
+                                     d["block_indices"], d["seq_lens_kv"], d["kv_valid_bits"])
+            self.ws = torch.empty(pkb.paged_attn_workspace_size(self.params), dtype=torch.uint8,
+                                  device=dev)
+            self.out = torch.empty_like(d["q"])
+            self.lse = torch.empty(d["q"].shape[:3], dtype=torch.float32, device=dev)
+        elif self.form == "prefill":
+            self.params = pkb.prefill_params(d["q"], d["k_cache"], d["block_tables"],
+                                             d["seq_lens_kv"].numel(), mask_type=p["mask_type"],
+                                             window_left=p["window_left"],
+                                             sm_scale=p["sm_scale"],
+                                             output_scale=p["output_scale"])
+            self.ws = torch.empty(pkb.paged_prefill_workspace_size(self.params),
+                                  dtype=torch.uint8, device=dev)
+            self.out = torch.empty_like(d["q"])
+            self.lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
+        else:
+            self.params = pkb.qsa_params(d["q"], d["k"], d["sel_blocks"].shape[1],
+                                         scale=p["scale"])
+            self.meta = pkb.qsa_meta(d["sel_blocks"], d["lo"], d["hi"], d["blk_base"],
+                                     d["tok_base"], d["block_first"], d["block_last"])
+            self.ws = torch.empty(pkb.paged_attn_workspace_size(self.params), dtype=torch.uint8,
+                                  device=dev)
+            self.out = torch.empty_like(d["q"])
+            self.out32 = torch.empty(d["q"].shape, dtype=torch.float32, device=dev)
+            self.lse = torch.empty(d["q"].shape[1], d["q"].shape[0], dtype=torch.float32,
+                                   device=dev)
+
+    def inputs(self):
+        """The step's input tensors (device), in a fixed order."""
+        names = {"decode": ["q", "kv_cache", "kv_indptr", "kv_indices", "seq_lens"],
+                 "bsr": ["q", "k_cache", "v_cache", "kv_cache", "kv_indptr", "kv_indices",
+                         "block_indptr", "block_indices", "seq_lens_kv", "kv_valid_bits"],
+                 "prefill": ["q", "k_cache", "v_cache", "qo_indptr", "block_tables",
+                             "seq_lens_kv"],
+                 "qsa": ["q", "k", "v", "sel_blocks", "lo", "hi", "blk_base", "tok_base",
+                         "block_first", "block_last"]}[self.form]
+        return [(n, self.d[n]) for n in names if isinstance(self.d.get(n), torch.Tensor)]
+
+    def step(self):
+        d = self.d
+        if self.form == "decode":
+            pkb.paged_decode_run(self.params, d["q"], d["kv_cache"], None, d["kv_indptr"],
+                                 d["kv_indices"], d["seq_lens"], self.out, self.lse, self.ws)
+        elif self.form == "bsr":
+            pkb.paged_attn_plan(self.params, self.meta, self.ws)
+            pkb.paged_attn_run(self.params, self.meta, d["q"], self.k, self.v, self.out, None,
+                               self.lse, self.ws)
+        elif self.form == "prefill":
+            pkb.paged_prefill_run(self.params, d["q"], d["k_cache"], d["v_cache"],
+                                  d["qo_indptr"], d["block_tables"], d["seq_lens_kv"], self.out,
+                                  self.lse, self.ws)
+        else:
+            pkb.paged_attn_plan(self.params, self.meta, self.ws)
+            pkb.paged_attn_run(self.params, self.meta, d["q"], d["k"], d["v"], self.out,
+                               self.out32, self.lse, self.ws)
+
+    def status(self):
+        return pkb.paged_attn_workspace_status(self.ws)
+
+
+def barrier(dist_on):
+    if dist_on:
+        torch.distributed.barrier()
+
+
+def time_steps(r, steps, warmup, dist_on):
+    """(region ms, main-kernel ms per launch, kernel launches of this library in the region)."""
+    for _ in range(warmup):
+        r.step()
+    torch.cuda.synchronize()
+    barrier(dist_on)
+    torch.cuda.synchronize()
+    pkb.paged_attn_kernel_timer(True)
+    n0 = pkb.paged_attn_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        r.step()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(dist_on)
+    torch.cuda.synchronize()
+    n1 = pkb.paged_attn_launch_count()
+    pkb.paged_attn_kernel_timer(False)
+    kms, kn = pkb.paged_attn_kernel_timer_read()
+    return e0.elapsed_time(e1), kms / max(kn, 1), n1 - n0
+
+
+def time_e2e(r, steps):
+    """Each step copies its inputs from pinned host memory, runs, and reads the output back."""
+    host = [(n, t.cpu().pin_memory()) for n, t in r.inputs()]
+    out_host = torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for _, t in host)
+    d2h = out_host.numel() * out_host.element_size()
+    for _ in range(2):
+        for n, t in host:
+            r.d[n].copy_(t, non_blocking=True)
+        r.step()
+        out_host.copy_(r.out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        for n, t in host:
+            r.d[n].copy_(t, non_blocking=True)
+        r.step()
+        out_host.copy_(r.out, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
+
+
+# ----------------------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ----------------------------------------------------------------------------------------
+
+def decode_subbatch(p, reqs):
+    """The requests `reqs` of a decode workload with their pages copied to a compact pool."""
+    indptr = p["kv_indptr"].numpy()
+    idx = p["kv_indices"].numpy()
+    pages, new_ptr = [], [0]
+    for b in reqs:
+        pg = idx[indptr[b]:indptr[b + 1]]
+        pages.append(pg)
+        new_ptr.append(new_ptr[-1] + pg.size)
+    allp = np.concatenate(pages)
+    return dict(p, q=p["q"][list(reqs)], kv_cache=p["kv_cache"][torch.from_numpy(allp).long()],
+                kv_indptr=torch.tensor(new_ptr, dtype=torch.int32),
+                kv_indices=torch.arange(allp.size, dtype=torch.int32),
+                seq_lens=p["seq_lens"][list(reqs)])
+
+
+def oracle_decode_seconds(p):
+    from oracle import attention as A
+    t0 = time.perf_counter()
+    A.batch_decode(p["q"], p["kv_indptr"], p["kv_indices"], p["seq_lens"],
+                   kv_cache=p["kv_cache"], bmm1_scale=p["sm_scale"], bmm2_scale=p["bmm2_scale"],
+                   mask_type=p["mask_type"], window_left=p["window_left"])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_decode(p, budget_s=12.0):
+    """Oracle over consecutive 8-request sub-batches until about budget_s seconds."""
+    B = p["q"].shape[0]
+    done_bytes, secs, reqs_done = 0, 0.0, 0
+    for s in range(0, B, 8):
+        sub = decode_subbatch(p, range(s, min(B, s + 8)))
+        secs += oracle_decode_seconds(sub)
+        done_bytes += decode_kv_bytes(sub)
+        reqs_done += sub["q"].shape[0]
+        if secs >= budget_s:
+            break
+    return {"value": done_bytes / secs / 1e9, "unit": "GB/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"float64 oracle on requests 0..{reqs_done - 1} of {B} "
+                      f"({done_bytes / 1e9:.3f} GB of live K/V, {secs:.1f} s; BLAS threads = "
+                      "all host cores, page gathers single-threaded)"}
+
+
+# ----------------------------------------------------------------------------------------
+# main
+# ----------------------------------------------------------------------------------------
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return 0
+    p = make_workload(args.workload)
+    if p["form"] != "decode":
+        print(json.dumps({"impl": "reference", "unavailable":
+                          "the reference arm is defined on the decode workload"}))
+        return 0
+    sub = decode_subbatch(p, range(0, 8))
+    nbytes = decode_kv_bytes(sub)
+    for _ in range(args.warmup):
+        oracle_decode_seconds(sub)
+    secs = [oracle_decode_seconds(sub) for _ in range(args.steps)]
+    tot = sum(secs)
+    v = nbytes * args.steps / tot / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": describe(args.workload, p),
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": "float64 oracle on requests 0..7 of the 64-request "
+                                       f"decode batch per step ({nbytes / 1e9:.3f} GB K/V)"},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--no-extra", action="store_true", help="skip the per_config workloads")
+    ap.add_argument("--skip-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+
+    dist_on = world > 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if dist_on:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    pk, pk_src = peaks()
+
+    p = make_workload(args.workload)
+    r = Runner(p, dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    region_ms, kernel_ms, launches = time_steps(r, args.steps, args.warmup, dist_on)
+    clocks = sampler.stop()
+    rc, raw = r.status()
+    if rc != pkb.OK:
+        raise RuntimeError(f"device status {raw:#x}")
+    t = torch.tensor([region_ms], dtype=torch.float64, device=dev)
+    if dist_on:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    region_ms = float(t.item())
+    ms_step = region_ms / args.steps
+
+    if p["form"] == "decode":
+        units = decode_kv_bytes(p)
+        unit, scale = "GB/s", 1e9
+        kernel, bound, peak = "decode_split_kernel", "hbm", pk["hbm_gbs"]
+    else:
+        nbytes = None
+        units = {"bsr": bsr_pairs, "prefill": prefill_pairs, "qsa": qsa_pairs}[p["form"]](p)
+        units *= 4 * p["q"].shape[-1]
+        unit, scale = "TFLOP/s", 1e12
+        kernel, bound, peak = "attn_tc_kernel", "tensor", pk["bf16_tflops"]
+    value = units * world / (ms_step * 1e-3) / scale
+    achieved = units / (kernel_ms * 1e-3) / scale
+    traffic = recorded_traffic(kernel, args.workload)
+    e2e_ms, h2d, d2h = time_e2e(r, max(3, min(args.steps, 10)))
+    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16; see workloads.py)",
+            "config": dict(describe(args.workload, p),
+                           l2="inputs larger than L2" if p["form"] == "decode" else
+                           "L2 not flushed between steps",
+                           parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+            "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
+                         "unit": unit, "frac": achieved / peak, "traffic": traffic,
+                         "kernel": kernel, "kernel_ms": kernel_ms,
+                         "peak_source": f"{pk_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})"},
+            "e2e": {"value": units * world / (e2e_ms * 1e-3) / scale, "unit": unit,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": launches,
+            "clocks": clocks}
+    del r
+    torch.cuda.empty_cache()
+
+    if rank == 0 and world == 1 and not args.skip_cpu and p["form"] == "decode":
+        line["cpu_baseline"] = cpu_baseline_decode(p)
+    if not args.no_extra and rank == 0:
+        extra = {}
+        for name in ("tiny_bsr", "prefill_b16", "prefill_b16_w1023", "long_bsr", "qsa_t32k"):
+            if name == args.workload:
+                continue
+            try:
+                q = make_workload(name)
+                rr = Runner(q, dev)
+                reg, kms, _ = time_steps(rr, max(3, min(args.steps, 20)), 3, False)
+                rc, raw = rr.status()
+                if rc != pkb.OK:
+                    raise RuntimeError(f"device status {raw:#x}")
+                n = {"bsr": bsr_pairs, "prefill": prefill_pairs, "qsa": qsa_pairs}[q["form"]](q)
+                flops = 4 * q["q"].shape[-1] * n
+                steps = max(3, min(args.steps, 20))
+                extra[name] = {"tflops_step": flops / (reg / steps * 1e-3) / 1e12,
+                               "tflops_kernel": flops / (kms * 1e-3) / 1e12,
+                               "frac_bf16_peak": flops / (kms * 1e-3) / 1e12 / pk["bf16_tflops"],
+                               "ms_step": reg / steps, "ms_kernel": kms,
+                               "visible_pairs": n, "flops": flops}
+                del rr
+                torch.cuda.empty_cache()
+            except pkb.PagedAttnError as e:
+                extra[name] = {"unavailable": str(e)}
+        line["per_config"] = extra
+    if rank == 0:
+        print(json.dumps(line))
+    if dist_on:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

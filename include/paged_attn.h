@@ -247,6 +247,21 @@ int paged_attn_plan_layout_of(const paged_attn_params* params, paged_attn_plan_l
 int paged_prefill_plan_layout_of(const paged_prefill_params* params, paged_attn_plan_layout* out);
 int paged_decode_plan_layout_of(const paged_decode_params* params, paged_attn_plan_layout* out);
 
+/* ---- benchmark hooks ------------------------------------------------------------------ */
+
+/* Kernel timer.  While enabled, every run brackets its main attention kernel (the
+ * block-sparse / prefill tensor-core kernel, the bitmap kernel, or the split-KV decode
+ * kernel) with a pair of CUDA events recorded on the launch stream.  enable = 1 clears the
+ * record and starts collecting; 0 stops.  Not for use inside CUDA graph capture. */
+int paged_attn_kernel_timer(int enable);
+
+/* Sum of the bracketed kernel times in milliseconds and the number of bracketed launches
+ * since the timer was last enabled; waits for the recorded events. */
+int paged_attn_kernel_timer_read(double* total_ms, int64_t* launches);
+
+/* Number of kernels this library has enqueued since it was loaded. */
+int64_t paged_attn_launch_count(void);
+
 /* ---- status -------------------------------------------------------------------------- */
 
 /* Synchronise `stream`, read the workspace status word and map it to a status code:

@@ -99,6 +99,9 @@ _EXPORTS = {
     "paged_decode_plan_layout_of": (C.c_int, [C.POINTER(DecodeParams), C.POINTER(PlanLayout)]),
     "paged_attn_workspace_status": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(C.c_uint32)]),
     "paged_attn_strerror": (C.c_char_p, [C.c_int]),
+    "paged_attn_kernel_timer": (C.c_int, [C.c_int]),
+    "paged_attn_kernel_timer_read": (C.c_int, [C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
+    "paged_attn_launch_count": (C.c_int64, []),
 }
 
 
@@ -243,6 +246,22 @@ def paged_attn_workspace_status(workspace, stream=None):
     rc = lib().paged_attn_workspace_status(_dev(workspace, "workspace"), _stream(stream),
                                            C.byref(raw))
     return rc, raw.value
+
+
+def paged_attn_kernel_timer(enable: bool) -> None:
+    _check(lib().paged_attn_kernel_timer(int(bool(enable))), "paged_attn_kernel_timer")
+
+
+def paged_attn_kernel_timer_read():
+    """(total milliseconds, launches) of the main kernels bracketed since enabling."""
+    ms, n = C.c_double(0.0), C.c_int64(0)
+    _check(lib().paged_attn_kernel_timer_read(C.byref(ms), C.byref(n)),
+           "paged_attn_kernel_timer_read")
+    return ms.value, n.value
+
+
+def paged_attn_launch_count() -> int:
+    return int(lib().paged_attn_launch_count())
 
 
 def _workspace(nbytes, device):

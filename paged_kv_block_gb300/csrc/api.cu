@@ -1,8 +1,11 @@
 // C ABI of libpagedattn: argument checks, workspace layouts, tensor-map encoding and the
 // launch sequence of each entry point (include/paged_attn.h documents the contract).
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
+#include <utility>
 #include <vector>
 
 #include <cudaTypedefs.h>
@@ -248,6 +251,38 @@ bool encode_q_map(CUtensorMap* map, const void* base, long long rows, int Hq, in
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// ---- kernel timer and launch counter -------------------------------------------------------
+namespace {
+std::atomic<long long> g_launches{0};
+struct Timer {
+  std::mutex mu;
+  bool on = false;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pairs;
+  size_t used = 0;
+} g_timer;
+}  // namespace
+
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+void timer_begin(cudaStream_t st, void** token) {
+  *token = nullptr;
+  std::lock_guard<std::mutex> lk(g_timer.mu);
+  if (!g_timer.on) return;
+  if (g_timer.used == g_timer.pairs.size()) {
+    cudaEvent_t a, b;
+    if (cudaEventCreate(&a) != cudaSuccess) return;
+    if (cudaEventCreate(&b) != cudaSuccess) { cudaEventDestroy(a); return; }
+    g_timer.pairs.emplace_back(a, b);
+  }
+  auto& pr = g_timer.pairs[g_timer.used++];
+  cudaEventRecord(pr.first, st);
+  *token = pr.second;
+}
+
+void timer_end(cudaStream_t st, void* token) {
+  if (token) cudaEventRecord(static_cast<cudaEvent_t>(token), st);
+}
+
 int launch_qsa(const paged_attn_params* p, const paged_attn_meta* m, const void* q,
                const void* k, const void* v, void* out, float* out_fp32, float* lse,
                const int* indptr, const int* indices, uint32_t* status, cudaStream_t st);
@@ -370,7 +405,7 @@ int paged_attn_run(const paged_attn_params* p, const paged_attn_meta* m, const v
                               at<int>(ws, s.indices), status, st);
     return rc;
   }
-  if (!m->kv_indptr_dev || !m->kv_indices_dev || !m->block_indices_dev || !m->seq_lens_kv_dev)
+  if (!m->kv_indptr_dev || !m->block_indptr_dev || !m->seq_lens_kv_dev)
     return PAGED_ATTN_ERR_INVALID_ARGUMENT;
   if (!p->combined_cache && !v) return PAGED_ATTN_ERR_INVALID_ARGUMENT;
   if (p->has_valid_bits && !m->kv_valid_bits_dev) return PAGED_ATTN_ERR_INVALID_ARGUMENT;
@@ -399,6 +434,7 @@ int paged_attn_run(const paged_attn_params* p, const paged_attn_meta* m, const v
   a.q_len = p->q_len;
   a.valid_bits = p->has_valid_bits ? m->kv_valid_bits_dev : nullptr;
   a.valid_words = ceil_div(p->max_seq_len_kv > 0 ? p->max_seq_len_kv : 1, 32);
+  a.block_sparse = 1;
   a.block_indices = m->block_indices_dev;
   a.kv_block_size = p->kv_block_size;
   a.out = static_cast<__nv_bfloat16*>(out);
@@ -417,7 +453,10 @@ int paged_attn_run(const paged_attn_params* p, const paged_attn_meta* m, const v
   a.window_left = -1;
   a.scale_log2 = scale * kLog2e;
   a.out_scale = 1.0f;
+  void* tok;
+  timer_begin(st, &tok);
   const int rc = launch_attn(a, st);
+  timer_end(st, tok);
   if (rc == -2) return PAGED_ATTN_ERR_UNSUPPORTED;
   return rc == 0 ? PAGED_ATTN_OK : PAGED_ATTN_ERR_CUDA;
 }
@@ -470,6 +509,7 @@ int paged_prefill_run(const paged_prefill_params* p, const void* q, const void* 
   a.q_len = 0;
   a.valid_bits = nullptr;
   a.valid_words = 0;
+  a.block_sparse = 0;
   a.block_indices = nullptr;
   a.kv_block_size = kKvTile;
   a.out = static_cast<__nv_bfloat16*>(out);
@@ -488,7 +528,10 @@ int paged_prefill_run(const paged_prefill_params* p, const void* q, const void* 
   a.window_left = p->window_left;
   a.scale_log2 = scale * kLog2e;
   a.out_scale = p->output_scale;
+  void* tok;
+  timer_begin(st, &tok);
   const int rc = launch_attn(a, st);
+  timer_end(st, tok);
   if (rc == -2) return PAGED_ATTN_ERR_UNSUPPORTED;
   return rc == 0 ? PAGED_ATTN_OK : PAGED_ATTN_ERR_CUDA;
 }
@@ -559,6 +602,7 @@ int paged_decode_run(const paged_decode_params* p, const void* query, const void
   a.scale_log2 = scale * kLog2e;
   a.out_scale = p->bmm2_scale;
   a.window_left = p->window_left;
+  a.timer_token = nullptr;
   return launch_decode(a, st) == 0 ? PAGED_ATTN_OK : PAGED_ATTN_ERR_CUDA;
 }
 
@@ -602,6 +646,30 @@ int paged_decode_plan_layout_of(const paged_decode_params* p, paged_attn_plan_la
   o->split_chunk = s.chunk;
   return PAGED_ATTN_OK;
 }
+
+int paged_attn_kernel_timer(int enable) {
+  std::lock_guard<std::mutex> lk(g_timer.mu);
+  g_timer.on = enable != 0;
+  if (enable) g_timer.used = 0;
+  return PAGED_ATTN_OK;
+}
+
+int paged_attn_kernel_timer_read(double* total_ms, int64_t* launches) {
+  std::lock_guard<std::mutex> lk(g_timer.mu);
+  double tot = 0.0;
+  for (size_t i = 0; i < g_timer.used; ++i) {
+    auto& pr = g_timer.pairs[i];
+    if (cudaEventSynchronize(pr.second) != cudaSuccess) return PAGED_ATTN_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, pr.first, pr.second) != cudaSuccess) return PAGED_ATTN_ERR_CUDA;
+    tot += ms;
+  }
+  if (total_ms) *total_ms = tot;
+  if (launches) *launches = static_cast<int64_t>(g_timer.used);
+  return PAGED_ATTN_OK;
+}
+
+int64_t paged_attn_launch_count(void) { return g_launches.load(); }
 
 int paged_attn_workspace_status(const void* ws, void* stream, uint32_t* raw) {
   if (!ws) return PAGED_ATTN_ERR_INVALID_ARGUMENT;

@@ -98,10 +98,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                              : a.q_len;
 
   KvWalk<CK> walk;
-  walk.dense = a.block_indices == nullptr;
+  walk.dense = !a.block_sparse;
   walk.kv_begin = tile.kv_begin;
   walk.kv_end = tile.kv_end;
-  walk.blocks = a.block_indices ? a.block_indices + tile.kv_begin : nullptr;
+  walk.blocks = a.block_sparse ? a.block_indices + tile.kv_begin : nullptr;
   walk.kvbs = a.kv_block_size;
   walk.spb = a.kv_block_size / CK;
   walk.total_sub = walk.dense ? 0 : (tile.kv_end - tile.kv_begin) * walk.spb;
@@ -452,6 +452,7 @@ int launch_ck(const AttnLaunch& a, cudaStream_t st) {
     attr_set = true;
   }
   attn_tc_kernel<CK><<<a.capacity, kThreads, kSmemBytes, st>>>(a.qmap, a.kmap, a.vmap, a);
+  count_launches(1);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
@@ -459,7 +460,7 @@ int launch_ck(const AttnLaunch& a, cudaStream_t st) {
 
 int launch_attn(const AttnLaunch& a, cudaStream_t st) {
   if (a.capacity <= 0) return 0;
-  switch (attn_sub_chunk(a.kv_block_size, a.block_indices != nullptr)) {
+  switch (attn_sub_chunk(a.kv_block_size, a.block_sparse != 0)) {
     case 8: return launch_ck<8>(a, st);
     case 16: return launch_ck<16>(a, st);
     case 32: return launch_ck<32>(a, st);

@@ -324,9 +324,17 @@ int launch_decode(const DecodeLaunch& a, cudaStream_t st) {
       return -1;
     attr_set = true;
   }
-  if (a.capacity > 0)
+  if (a.capacity > 0) {
+    void* tok;
+    timer_begin(st, &tok);
     decode_split_kernel<<<a.capacity, kThreads, kSmemBytes, st>>>(*a.kmap, *a.vmap, a);
-  if (a.B > 0) decode_merge_kernel<<<a.B * a.Hq, kD, 0, st>>>(a);
+    timer_end(st, tok);
+    count_launches(1);
+  }
+  if (a.B > 0) {
+    decode_merge_kernel<<<a.B * a.Hq, kD, 0, st>>>(a);
+    count_launches(1);
+  }
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -82,8 +82,14 @@ struct DecodeLaunch {
   int capacity;              // launched work items
   float scale_log2, out_scale;
   int window_left;
+  void* timer_token;
 };
 int launch_decode(const DecodeLaunch& a, cudaStream_t st);
+
+// Benchmark hooks (api.cu): count kernel launches; bracket the main kernel with events.
+void count_launches(int n);
+void timer_begin(cudaStream_t st, void** token);
+void timer_end(cudaStream_t st, void* token);
 
 struct AttnLaunch {
   CUtensorMap qmap, kmap, vmap;
@@ -99,7 +105,8 @@ struct AttnLaunch {
   int q_len;
   const uint32_t* valid_bits;
   int valid_words;
-  const int* block_indices;  // BSR form; nullptr -> dense KV tiles
+  int block_sparse;          // 1: KV tiles walk block_indices; 0: dense KV tile ranges
+  const int* block_indices;  // BSR form (may be null when no row lists a block)
   int kv_block_size;
   __nv_bfloat16* out;
   float* lse;

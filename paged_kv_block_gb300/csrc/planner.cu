@@ -353,6 +353,7 @@ void launch_bsr_tiles(const int* block_indptr, int B, int Hkv, int Sq, int qbs, 
   if (rows <= 0) return;
   bsr_tiles_kernel<<<ceil_div(rows, 256), 256, 0, st>>>(block_indptr, B, Hkv, Sq, qbs,
                                                         tile_tokens, tmp);
+  count_launches(1);
 }
 
 void launch_prefill_tiles(const int* qo_indptr, const int* seq_lens, int B, int Hkv,
@@ -361,9 +362,12 @@ void launch_prefill_tiles(const int* qo_indptr, const int* seq_lens, int B, int 
                           cudaStream_t st) {
   prefill_count_kernel<<<1, 1024, 0, st>>>(qo_indptr, B, Hkv, tile_tokens, capacity,
                                            tile_offsets, n_tiles, status);
-  if (B > 0)
+  count_launches(1);
+  if (B > 0) {
     prefill_fill_kernel<<<B, 256, 0, st>>>(qo_indptr, seq_lens, Hkv, tile_tokens, causal,
                                            window_left, capacity, tile_offsets, tmp);
+    count_launches(1);
+  }
 }
 
 size_t tile_sort_scratch_ints(int capacity, int max_cost) {
@@ -380,6 +384,7 @@ void launch_tile_sort(const TileRec* in, TileRec* out, const int* n_dev, int n_s
   sort_offsets_kernel<<<1, 1024, sm, st>>>(nchunks, max_cost, hist, offs);
   sort_scatter_kernel<<<nchunks, kSortChunk, sm, st>>>(in, out, n_dev, n_static, max_cost,
                                                        offs);
+  count_launches(3);
 }
 
 void launch_bitmap_plan(const uint8_t* sel, const int* lo, const int* hi, const int* bfirst,
@@ -394,15 +399,19 @@ void launch_bitmap_plan(const uint8_t* sel, const int* lo, const int* hi, const 
   counts_to_indptr_kernel<<<1, 1024, 0, st>>>(indptr + 1, T, capacity, indptr, status);
   bitmap_scan_kernel<true><<<grid, 32 * warps_per_cta, 0, st>>>(
       sel, lo, hi, bfirst, blast, T, NB, nullptr, indptr, indices, capacity);
+  count_launches(3);
 }
 
 void launch_decode_plan(const int* seq_lens, int B, int Hkv, int chunk, int window_left,
                         int max_splits, int* split_offset, SplitItem* items, cudaStream_t st) {
   decode_plan_kernel<<<1, 1024, 0, st>>>(seq_lens, B, chunk, window_left, max_splits,
                                          split_offset);
-  if (B > 0)
+  count_launches(1);
+  if (B > 0) {
     decode_items_kernel<<<B, 256, 0, st>>>(seq_lens, Hkv, chunk, window_left, split_offset,
                                            items);
+    count_launches(1);
+  }
 }
 
 }  // namespace pa
