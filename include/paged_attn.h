@@ -219,6 +219,27 @@ int paged_decode_run(const paged_decode_params* params, const void* query_dev,
                      void* out_dev, float* lse_dev, void* workspace_dev,
                      size_t workspace_bytes, void* stream);
 
+/* Decode without a workspace argument.  The pages describe no counterpart of this entry
+ * point; it exists for callers that cannot allocate device memory at call time (code inside
+ * an allocator or out-of-memory handler, plugins whose host owns every device allocation,
+ * runtimes that forbid allocations after start-up).  Same arguments and results as
+ * paged_decode_run, minus the workspace: the scratch lives in a fixed array inside the
+ * library of PAGED_DECODE_STATIC_SCRATCH_BYTES bytes, reserved on every GPU that loads the
+ * library until the process exits.  No cudaMalloc, cudaFree or other allocating call is
+ * made.
+ *   - Returns PAGED_ATTN_ERR_WORKSPACE without enqueuing anything when the problem needs
+ *     more scratch than that (paged_decode_workspace_size tells how much it needs).
+ *   - The first call on a device looks up the array's address on that device (the device
+ *     current at the call); make that first call before any stream capture.
+ *   - Every call on a device uses the same array, so calls whose work may overlap on the
+ *     GPU (other streams, other threads) race and must be serialised by the caller.
+ *   - The device status word lives inside the array and is not readable by the caller. */
+#define PAGED_DECODE_STATIC_SCRATCH_BYTES (32u << 20)
+int paged_decode_run_static(const paged_decode_params* params, const void* query_dev,
+                            const void* k_dev, const void* v_dev, const int32_t* kv_indptr_dev,
+                            const int32_t* kv_indices_dev, const int32_t* seq_lens_dev,
+                            void* out_dev, float* lse_dev, void* stream);
+
 /* ---- plan inspection -------------------------------------------------------------------- */
 
 /* Where a plan lives inside the workspace (byte offsets from its start), so that callers

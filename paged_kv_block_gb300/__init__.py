@@ -97,6 +97,7 @@ _EXPORTS = {
     "paged_attn_plan_layout_of": (C.c_int, [C.POINTER(AttnParams), C.POINTER(PlanLayout)]),
     "paged_prefill_plan_layout_of": (C.c_int, [C.POINTER(PrefillParams), C.POINTER(PlanLayout)]),
     "paged_decode_plan_layout_of": (C.c_int, [C.POINTER(DecodeParams), C.POINTER(PlanLayout)]),
+    "paged_decode_run_static": (C.c_int, [C.POINTER(DecodeParams)] + [C.c_void_p] * 9),
     "paged_attn_workspace_status": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(C.c_uint32)]),
     "paged_attn_strerror": (C.c_char_p, [C.c_int]),
     "paged_attn_kernel_timer": (C.c_int, [C.c_int]),
@@ -238,6 +239,18 @@ def plan_layout(params) -> PlanLayout:
           DecodeParams: lib().paged_decode_plan_layout_of}[type(params)]
     _check(fn(C.byref(params), C.byref(o)), "plan_layout")
     return o
+
+
+def paged_decode_run_static(params: DecodeParams, query, k, v, kv_indptr, kv_indices, seq_lens,
+                            out, lse, stream=None) -> None:
+    """paged_decode_run for callers that cannot allocate: the scratch is a fixed array
+    inside the library (see the C header for its size and the sharing rules)."""
+    _check(lib().paged_decode_run_static(C.byref(params), _dev(query, "query"), _dev(k, "k"),
+                                         _dev(v, "v"), _dev(kv_indptr, "kv_indptr"),
+                                         _dev(kv_indices, "kv_indices"),
+                                         _dev(seq_lens, "seq_lens"), _dev(out, "out"),
+                                         _dev(lse, "lse"), _stream(stream)),
+           "paged_decode_run_static")
 
 
 def paged_attn_workspace_status(workspace, stream=None):
