@@ -115,6 +115,7 @@ def source_hash(files):
 KERNEL_SOURCES = {
     "decode_split_kernel": ["paged_kv_block_gb300/csrc/decode.cu",
                             "paged_kv_block_gb300/csrc/common.cuh"],
+    "qsa_kernel": ["paged_kv_block_gb300/csrc/qsa.cu", "paged_kv_block_gb300/csrc/common.cuh"],
     "attn_tc_kernel": ["paged_kv_block_gb300/csrc/attn_tc.cu",
                        "paged_kv_block_gb300/csrc/common.cuh"],
 }
@@ -513,7 +514,8 @@ def main():
         units = {"bsr": bsr_pairs, "prefill": prefill_pairs, "qsa": qsa_pairs}[p["form"]](p)
         units *= 4 * p["q"].shape[-1]
         unit, scale = "TFLOP/s", 1e12
-        kernel, bound, peak = "attn_tc_kernel", "tensor", pk["bf16_tflops"]
+        kernel = "qsa_kernel" if p["form"] == "qsa" else "attn_tc_kernel"
+        bound, peak = "tensor", pk["bf16_tflops"]
     value = units * world / (ms_step * 1e-3) / scale
     achieved = units / (kernel_ms * 1e-3) / scale
     traffic = recorded_traffic(kernel, args.workload)

@@ -4,15 +4,17 @@
 // listed per (request, KV head, query block) in BSR form) and the dense packed-Q form of
 // batch_prefill_with_paged_kv_cache (every KV tile that meets the causal / window span).
 //
-// One CTA owns one planner tile: up to two Q sub-tiles of 128 rows, a row being a (token,
-// head-in-group) pair, so the G query heads that share a KV head share every K/V tile.
-// Roles (320 threads):
-//   warps 0-3  softmax of sub-tile 0 (thread t <-> TMEM lane t <-> row t)
-//   warps 4-7  softmax of sub-tile 1
-//   warp  8    TMA producer: Q once, then K and V of each 128-key tile, one box per page
-//              piece (a page, or the part of a page inside a selected block) and 64-column
-//              half, into a 2-stage ring
+// Persistent: one CTA per SM walks the planner's tile list (sorted by cost, largest first)
+// with a stride of the grid size.  A tile holds up to two Q sub-tiles of 128 rows, a row
+// being a (token, head-in-group) pair, so the G query heads that share a KV head share
+// every K/V tile.  Roles (384 threads):
+//   warps 0-3  softmax + epilogue of sub-tile 0 (thread t <-> TMEM lane t <-> row t)
+//   warps 4-7  softmax + epilogue of sub-tile 1
+//   warp  8    TMA producer of Q (once per tile) and K (3-stage ring)
 //   warp  9    TMEM owner and MMA issuer (one thread): S_w = Q_w K^T and O_w += P_w V
+//   warp 10    TMA producer of V (2-stage ring)
+// K and V of a 128-key tile are gathered one TMA box per page piece (a page, or the part of
+// a page inside a selected block) and 64-column half.
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512); P_w is
 // written as packed bf16 over the first 64 columns of S_w and read from TMEM by the PV MMA.
 // The online softmax runs in the log2 domain with exp2; the running maximum is only moved
@@ -28,30 +30,34 @@ namespace pa {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kQHalf = 128 * 128;              // bytes of a 128-row x 64-col bf16 half
 constexpr int kQBytes = 2 * kQHalf;            // one Q sub-tile
 constexpr int kKvHalf = kKvTile * 128;         // 128 keys x 64 cols
 constexpr int kKvBytes = 2 * kKvHalf;          // one K (or V) tile
-constexpr int kStages = 2;
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
+// Register split after set-up (launch: 384 threads x 168): the producer / MMA warpgroup
+// gives registers to the two softmax warpgroups; 2 x 128 x 200 + 128 x 104 = 384 x 168.
+constexpr int kSoftmaxRegs = 200;
+constexpr int kControlRegs = 104;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register split");
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct Ctrl {
-  uint64_t q_full;
-  uint64_t k_full[kStages];
-  uint64_t v_full[kStages];
-  uint64_t kv_empty[kStages];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_final[2];
+  uint64_t q_full, q_empty;
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t s_full[2], p_full[2], o_final[2], o_empty[2];
   uint32_t tmem_base;
   int abort_flag;
 };
 
-constexpr int kSmemBytes = 2 * kQBytes + kStages * 2 * kKvBytes + 1024 + 256;
+constexpr int kSmemBytes =
+    2 * kQBytes + (kKStages + kVStages) * kKvBytes + static_cast<int>(sizeof(Ctrl)) + 1024;
 
-// Geometry of the KV tile sequence of one CTA.
+// Geometry of the KV tile sequence of one planner tile.
 template <int CK>
 struct KvWalk {
   int dense;            // 1: tile n covers keys [(kv_begin + n) * 128, +128)
@@ -74,6 +80,66 @@ struct KvWalk {
 };
 
 template <int CK>
+struct TileInfo {
+  TileRec rec;
+  int ntok0, ntok1, nsub, L, nq, N;
+  KvWalk<CK> walk;
+};
+
+template <int CK>
+__device__ __forceinline__ TileInfo<CK> load_tile(const AttnLaunch& a, int idx) {
+  TileInfo<CK> t;
+  t.rec = a.tiles[idx];
+  const int TM = kMTileRows / a.G;
+  t.ntok0 = min(t.rec.ntok, TM);
+  t.ntok1 = t.rec.ntok - t.ntok0;
+  t.nsub = t.ntok1 > 0 ? 2 : 1;
+  t.L = __ldg(a.seq_lens + t.rec.b);
+  t.nq = a.qo_indptr ? (__ldg(a.qo_indptr + t.rec.b + 1) - __ldg(a.qo_indptr + t.rec.b))
+                     : a.q_len;
+  t.walk.dense = !a.block_sparse;
+  t.walk.kv_begin = t.rec.kv_begin;
+  t.walk.kv_end = t.rec.kv_end;
+  t.walk.blocks = a.block_sparse ? a.block_indices + t.rec.kv_begin : nullptr;
+  t.walk.kvbs = a.kv_block_size;
+  t.walk.spb = a.kv_block_size / CK;
+  t.walk.total_sub = t.walk.dense ? 0 : (t.rec.kv_end - t.rec.kv_begin) * t.walk.spb;
+  t.N = t.walk.num_tiles();
+  return t;
+}
+
+// Pool rows of the page pieces of KV tile n (R rows each, R = min(CK, page size)); returns a
+// bit mask of the pieces that hold live keys.  Pieces past the length are not loaded.
+template <int CK>
+__device__ __forceinline__ uint32_t gather_rows(const AttnLaunch& a, const TileInfo<CK>& t,
+                                                const int* pt, int n, int (&rows)[kKvTile / 8]) {
+  const int ps = a.page_size;
+  const int R = CK < ps ? CK : ps;
+  const int max_page_idx = (t.L + ps - 1) / ps;
+  uint32_t live = 0;
+  int idx = 0;
+#pragma unroll 1
+  for (int c = 0; c < kKvTile / CK; ++c) {
+    const int k0 = t.walk.key0(n, c);
+#pragma unroll 1
+    for (int p = 0; p < CK / R; ++p, ++idx) {
+      const int key = k0 + p * R;
+      if (k0 < 0 || key >= t.L) continue;
+      const int pidx = key / ps;
+      if (pidx >= max_page_idx) continue;
+      const int page = __ldg(pt + pidx);
+      if (page < 0 || page >= a.num_pages) {
+        report_error(a.status, kErrMetadata);
+        continue;
+      }
+      rows[idx] = page * a.page_rows + t.rec.g * ps + key % ps;
+      live |= 1u << idx;
+    }
+  }
+  return live;
+}
+
+template <int CK>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, AttnLaunch a) {
@@ -82,43 +148,32 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* q_s = base;                                   // 2 sub-tiles
-  uint8_t* kv_s = base + 2 * kQBytes;                    // stages: K then V
-  Ctrl* ctl = reinterpret_cast<Ctrl*>(kv_s + kStages * 2 * kKvBytes);
+  uint8_t* k_s = q_s + 2 * kQBytes;                      // K ring
+  uint8_t* v_s = k_s + kKStages * kKvBytes;              // V ring
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(v_s + kVStages * kKvBytes);
 
   const int n_live = a.n_tiles ? *a.n_tiles : a.capacity;
   if (static_cast<int>(blockIdx.x) >= n_live || launch_aborted(a.status)) return;
-  const TileRec tile = a.tiles[blockIdx.x];
   const int G = a.G;
   const int TM = kMTileRows / G;                         // tokens per sub-tile
-  const int ntok0 = min(tile.ntok, TM);
-  const int ntok1 = tile.ntok - ntok0;
-  const int n_sub_tiles = ntok1 > 0 ? 2 : 1;
-  const int L = __ldg(a.seq_lens + tile.b);
-  const int nq = a.qo_indptr ? (__ldg(a.qo_indptr + tile.b + 1) - __ldg(a.qo_indptr + tile.b))
-                             : a.q_len;
-
-  KvWalk<CK> walk;
-  walk.dense = !a.block_sparse;
-  walk.kv_begin = tile.kv_begin;
-  walk.kv_end = tile.kv_end;
-  walk.blocks = a.block_sparse ? a.block_indices + tile.kv_begin : nullptr;
-  walk.kvbs = a.kv_block_size;
-  walk.spb = a.kv_block_size / CK;
-  walk.total_sub = walk.dense ? 0 : (tile.kv_end - tile.kv_begin) * walk.spb;
-  const int N = walk.num_tiles();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(&ctl->q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    mbar_init(&ctl->q_empty, 1);
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&ctl->k_full[s], 1);
+      mbar_init(&ctl->k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&ctl->v_full[s], 1);
-      mbar_init(&ctl->kv_empty[s], 1);
+      mbar_init(&ctl->v_empty[s], 1);
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&ctl->s_full[w], 1);
       mbar_init(&ctl->p_full[w], 128);
       mbar_init(&ctl->o_final[w], 1);
+      mbar_init(&ctl->o_empty[w], 128);
     }
     ctl->abort_flag = 0;
     fence_mbar_init();
@@ -132,146 +187,197 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   volatile int* abort_flag = &ctl->abort_flag;
-
-  if (warp == 8) {
-    // =============================== producer ==========================================
+  if (warp >= 8) {
+  regs_decrease<kControlRegs>();
+  if (warp == 8 || warp == 10) {
+    // =============================== producers =========================================
     if (lane == 0) {
-      tma_prefetch_desc(&qmap);
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-      const uint32_t qbox = 128u * G * TM;
-      mbar_arrive_expect_tx(&ctl->q_full, qbox * 2 * n_sub_tiles);
-      for (int w = 0; w < n_sub_tiles; ++w)
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(q_s + w * kQBytes + h * kQHalf, &qmap, &ctl->q_full, h * 64, tile.g * G,
-                      tile.q_row0 + w * TM);
+      const bool is_k = warp == 8;
+      if (is_k) {
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&kmap);
+      } else {
+        tma_prefetch_desc(&vmap);
+      }
       const int ps = a.page_size;
-      const int R = CK < ps ? CK : ps;                  // rows per box
-      const int* pt = a.pt_indptr ? a.pt + __ldg(a.pt_indptr + tile.b)
-                                  : a.pt + static_cast<long long>(tile.b) * a.pt_stride;
-      const int max_page_idx = (L + ps - 1) / ps;
-      for (int n = 0; n < N; ++n) {
-        const int st = n % kStages;
-        if (n >= kStages &&
-            !mbar_wait(&ctl->kv_empty[st], ((n / kStages) - 1) & 1, a.status, abort_flag))
-          break;
-        uint8_t* kt = kv_s + st * 2 * kKvBytes;
-        uint8_t* vt = kt + kKvBytes;
-        int rows[kKvTile / 8];
-        uint32_t live = 0;
-        int npieces = 0;
-#pragma unroll 1
-        for (int c = 0; c < NSUB; ++c) {
-          const int k0 = walk.key0(n, c);
-#pragma unroll 1
-          for (int p = 0; p < CK / R; ++p) {
-            const int idx = npieces++;
-            const int key = k0 + p * R;
-            if (k0 < 0 || key >= L) continue;
-            const int pidx = key / ps;
-            if (pidx >= max_page_idx) continue;
-            const int page = __ldg(pt + pidx);
-            if (page < 0 || page >= a.num_pages) {
-              report_error(a.status, kErrMetadata);
-              continue;
-            }
-            rows[idx] = page * a.page_rows + tile.g * ps + key % ps;
-            live |= 1u << idx;
+      const int R = CK < ps ? CK : ps;
+      const int stages = is_k ? kKStages : kVStages;
+      uint8_t* ring = is_k ? k_s : v_s;
+      uint64_t* full = is_k ? ctl->k_full : ctl->v_full;
+      uint64_t* empty = is_k ? ctl->k_empty : ctl->v_empty;
+      const CUtensorMap* map = is_k ? &kmap : &vmap;
+      const int head_off = is_k ? a.k_head_off : a.v_head_off;
+      int kv_it = 0, qcount = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
+        const TileInfo<CK> t = load_tile<CK>(a, idx);
+        if (t.N == 0) continue;
+        if (is_k) {
+          if (qcount > 0 && !mbar_wait(&ctl->q_empty, (qcount - 1) & 1, a.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t qbox = 128u * G * TM;
+          mbar_arrive_expect_tx(&ctl->q_full, qbox * 2 * t.nsub);
+          for (int w = 0; w < t.nsub; ++w)
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(q_s + w * kQBytes + h * kQHalf, &qmap, &ctl->q_full, h * 64,
+                          t.rec.g * G, t.rec.q_row0 + w * TM);
+          ++qcount;
+        }
+        const int* pt = a.pt_indptr ? a.pt + __ldg(a.pt_indptr + t.rec.b)
+                                    : a.pt + static_cast<long long>(t.rec.b) * a.pt_stride;
+        for (int n = 0; n < t.N; ++n) {
+          const int it = kv_it + n, slot = it % stages;
+          if (it >= stages &&
+              !mbar_wait(&empty[slot], ((it / stages) - 1) & 1, a.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          int rows[kKvTile / 8];
+          const uint32_t live = gather_rows<CK>(a, t, pt, n, rows);
+          const uint32_t bytes = static_cast<uint32_t>(__popc(live)) * R * 128u * 2u;
+          uint8_t* dst = ring + slot * kKvBytes;
+          mbar_arrive_expect_tx(&full[slot], bytes);
+          for (int i = 0; i < kKvTile / R; ++i) {
+            if (!((live >> i) & 1u)) continue;
+            const uint32_t off = static_cast<uint32_t>(i * R) * 128u;
+            tma_load_2d(dst + off, map, &full[slot], 0, rows[i] + head_off);
+            tma_load_2d(dst + kKvHalf + off, map, &full[slot], 64, rows[i] + head_off);
           }
         }
-        const uint32_t bytes = static_cast<uint32_t>(__popc(live)) * R * 128u * 2u;
-        mbar_arrive_expect_tx(&ctl->k_full[st], bytes);
-        for (int i = 0; i < npieces; ++i) {
-          if (!((live >> i) & 1u)) continue;
-          const uint32_t off = static_cast<uint32_t>(i * R) * 128u;
-          tma_load_2d(kt + off, &kmap, &ctl->k_full[st], 0, rows[i] + a.k_head_off);
-          tma_load_2d(kt + kKvHalf + off, &kmap, &ctl->k_full[st], 64, rows[i] + a.k_head_off);
-        }
-        mbar_arrive_expect_tx(&ctl->v_full[st], bytes);
-        for (int i = 0; i < npieces; ++i) {
-          if (!((live >> i) & 1u)) continue;
-          const uint32_t off = static_cast<uint32_t>(i * R) * 128u;
-          tma_load_2d(vt + off, &vmap, &ctl->v_full[st], 0, rows[i] + a.v_head_off);
-          tma_load_2d(vt + kKvHalf + off, &vmap, &ctl->v_full[st], 64, rows[i] + a.v_head_off);
-        }
+        kv_it += t.N;
       }
     }
   } else if (warp == 9) {
     // =============================== MMA issuer ========================================
-    if (lane == 0 && N > 0) {
+    if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(128, kKvTile, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(128, kD, false, true);
       const uint32_t q_addr = smem_u32(q_s);
-      const uint32_t kv_addr = smem_u32(kv_s);
-      auto issue_qk = [&](int w, int n) {
-        const uint32_t qa = q_addr + w * kQBytes;
-        const uint32_t ka = kv_addr + (n % kStages) * 2 * kKvBytes;
+      const uint32_t k_addr = smem_u32(k_s), v_addr = smem_u32(v_s);
+      // Descriptors of the first k-step; later steps add the byte offset / 16 to the start
+      // address field (bits 0-13), which never carries out of it inside shared memory.
+      const uint64_t q_desc0 = sdesc_sw128(q_addr, 16, 1024);
+      const uint64_t k_desc0 = sdesc_sw128(k_addr, 16, 1024);
+      const uint64_t v_desc0 = sdesc_sw128(v_addr, kKvHalf, 1024);
+      auto issue_qk = [&](int w, int kslot) {
+        const uint64_t qd = q_desc0 + static_cast<uint64_t>((w * kQBytes) >> 4);
+        const uint64_t kd = k_desc0 + static_cast<uint64_t>((kslot * kKvBytes) >> 4);
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kQHalf + (ks & 3) * 32;
-          const uint32_t koff = (ks >> 2) * kKvHalf + (ks & 3) * 32;
-          mma_ss(tmem + w * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + koff, 16, 1024),
-                 idesc_qk, ks > 0);
+          const uint32_t off = ((ks >> 2) * kQHalf + (ks & 3) * 32) >> 4;
+          const uint32_t koff = ((ks >> 2) * kKvHalf + (ks & 3) * 32) >> 4;
+          mma_ss(tmem + w * 128, qd + off, kd + koff, idesc_qk, ks > 0);
         }
         mma_commit(&ctl->s_full[w]);
       };
-      auto issue_pv = [&](int w, int n) {
-        const uint32_t va = kv_addr + (n % kStages) * 2 * kKvBytes + kKvBytes;
+      auto issue_pv = [&](int w, int vslot, bool acc) {
+        const uint64_t vd = v_desc0 + static_cast<uint64_t>((vslot * kKvBytes) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < kKvTile / 16; ++ks) {
-          mma_ts(tmem + 256 + w * 128, tmem + w * 128 + ks * 8,
-                 sdesc_sw128(va + ks * 16 * 128, kKvHalf, 1024), idesc_pv, (n > 0 || ks > 0));
-        }
-        if (n == N - 1) mma_commit(&ctl->o_final[w]);
+        for (int ks = 0; ks < kKvTile / 16; ++ks)
+          mma_ts(tmem + 256 + w * 128, tmem + w * 128 + ks * 8, vd + ((ks * 16 * 128) >> 4),
+                 idesc_pv, (acc || ks > 0));
       };
-      bool ok = mbar_wait(&ctl->q_full, 0, a.status, abort_flag);
-      ok = ok && mbar_wait(&ctl->k_full[0], 0, a.status, abort_flag);
-      if (ok) {
+      int kv_it = 0, qcount = 0, pc1 = 0;
+      int ep[2] = {0, 0};                        // epilogues that read O_w so far
+      bool ok = true;
+      for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
+        const TileInfo<CK> t = load_tile<CK>(a, idx);
+        const int N = t.N;
+        if (N == 0) continue;
+        const bool two = t.nsub > 1;
+        const int it0 = kv_it;
+        ok = mbar_wait(&ctl->q_full, qcount & 1, a.status, abort_flag) &&
+             mbar_wait(&ctl->k_full[it0 % kKStages], (it0 / kKStages) & 1, a.status, abort_flag);
+        ++qcount;
+        if (!ok) break;
         tc_fence_after();
-        issue_qk(0, 0);
-        if (n_sub_tiles > 1) issue_qk(1, 0);
-      }
-      for (int n = 0; ok && n < N; ++n) {
-        const int st = n % kStages;
-        if (!mbar_wait(&ctl->v_full[st], (n / kStages) & 1, a.status, abort_flag)) break;
-        if (!mbar_wait(&ctl->p_full[0], n & 1, a.status, abort_flag)) break;
-        tc_fence_after();
-        issue_pv(0, n);
-        const bool more = n + 1 < N;
-        if (more) {
-          if (!mbar_wait(&ctl->k_full[(n + 1) % kStages], ((n + 1) / kStages) & 1, a.status,
-                         abort_flag))
+        issue_qk(0, it0 % kKStages);
+        if (two) issue_qk(1, it0 % kKStages);
+        mma_commit(&ctl->k_empty[it0 % kKStages]);
+        if (N == 1) mma_commit(&ctl->q_empty);
+        for (int n = 0; n < N; ++n) {
+          const int it = it0 + n, vs = it % kVStages;
+          if (!mbar_wait(&ctl->v_full[vs], (it / kVStages) & 1, a.status, abort_flag) ||
+              !mbar_wait(&ctl->p_full[0], it & 1, a.status, abort_flag) ||
+              (n == 0 && ep[0] > 0 &&
+               !mbar_wait(&ctl->o_empty[0], (ep[0] - 1) & 1, a.status, abort_flag))) {
+            ok = false;
             break;
+          }
           tc_fence_after();
-          issue_qk(0, n + 1);
+          issue_pv(0, vs, n > 0);
+          if (n == N - 1) mma_commit(&ctl->o_final[0]);
+          const bool more = n + 1 < N;
+          const int ks_next = (it + 1) % kKStages;
+          if (more) {
+            if (!mbar_wait(&ctl->k_full[ks_next], ((it + 1) / kKStages) & 1, a.status,
+                           abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_qk(0, ks_next);
+          }
+          if (two) {
+            if (!mbar_wait(&ctl->p_full[1], pc1 & 1, a.status, abort_flag) ||
+                (n == 0 && ep[1] > 0 &&
+                 !mbar_wait(&ctl->o_empty[1], (ep[1] - 1) & 1, a.status, abort_flag))) {
+              ok = false;
+              break;
+            }
+            ++pc1;
+            tc_fence_after();
+            issue_pv(1, vs, n > 0);
+            if (n == N - 1) mma_commit(&ctl->o_final[1]);
+          }
+          mma_commit(&ctl->v_empty[vs]);
+          if (more) {
+            if (two) issue_qk(1, ks_next);
+            mma_commit(&ctl->k_empty[ks_next]);
+            if (n + 1 == N - 1) mma_commit(&ctl->q_empty);
+          }
         }
-        if (n_sub_tiles > 1) {
-          if (!mbar_wait(&ctl->p_full[1], n & 1, a.status, abort_flag)) break;
-          tc_fence_after();
-          issue_pv(1, n);
-        }
-        mma_commit(&ctl->kv_empty[st]);
-        if (more && n_sub_tiles > 1) issue_qk(1, n + 1);
+        kv_it += N;
+        ++ep[0];
+        if (two) ++ep[1];
       }
     }
+  }
   } else {
+    regs_increase<kSoftmaxRegs>();
     // =============================== softmax (one row per thread) =======================
     const int w = warp >> 2;                       // sub-tile
     const int m = threadIdx.x & 127;               // row inside the sub-tile
-    const int ntok_w = w == 0 ? ntok0 : ntok1;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_col = tmem + lane_base + w * 128;
     const uint32_t o_col = tmem + lane_base + 256 + w * 128;
-    const int tok = tile.tok0 + w * TM + m / G;    // token index inside the request
-    const bool row_valid = (m < G * TM) && (m / G < ntok_w);
-    const int pos = L - nq + tok;                  // query position
     const float sl2 = a.scale_log2;
     const bool causal = a.causal != 0;
     const int wl = a.window_left;
-    float m_run = -INFINITY, l_run = 0.f;
-    if (w < n_sub_tiles) {
+    int kv_it = 0, sc = 0, oc = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
+      const TileInfo<CK> t = load_tile<CK>(a, idx);
+      const int N = t.N;
+      const int ntok_w = w == 0 ? t.ntok0 : t.ntok1;
+      if (w >= t.nsub) {                           // this sub-tile is empty
+        kv_it += N;
+        continue;
+      }
+      const int L = t.L;
+      const int tok = t.rec.tok0 + w * TM + m / G;   // token index inside the request
+      const bool row_valid = (m < G * TM) && (m / G < ntok_w);
+      const int pos = L - t.nq + tok;                // query position
+      float m_run = -INFINITY, l_run = 0.f;
       for (int n = 0; n < N; ++n) {
-        if (!mbar_wait_warp(&ctl->s_full[w], n & 1, a.status, abort_flag)) break;
+        const int it = kv_it + n;
+        if (!mbar_wait_warp(&ctl->s_full[w], sc & 1, a.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        ++sc;
         tc_fence_after();
         // ---- per-tile column facts, identical for every row ----------------------------
         int k0[NSUB];
@@ -280,92 +386,110 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         int kmin = 0x7fffffff, kmax = -1;
 #pragma unroll
         for (int c = 0; c < NSUB; ++c) {
-          k0[c] = walk.key0(n, c);
+          k0[c] = t.walk.key0(n, c);
           if (k0[c] < 0 || k0[c] + CK > L) zero_v = true;
           if (k0[c] >= 0) {
             kmin = min(kmin, k0[c]);
             kmax = max(kmax, k0[c] + CK - 1);
           }
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) colmask[i] = 0u;
-#pragma unroll
-        for (int c = 0; c < NSUB; ++c) {
-          // bits of the CK columns of sub-chunk c (CK = 8, 16, 32, 64 or 128)
-#pragma unroll
-          for (int part = 0; part < (CK + 31) / 32; ++part) {
-            const int col0 = c * CK + part * 32;          // first column of this 32-span
-            const int span = CK < 32 ? CK : 32;
-            uint32_t bits = 0u;
-            if (k0[c] >= 0) {
-              const int key = k0[c] + part * 32;
-              const int live = L - key;                    // keys < L in this span
-              bits = live >= span ? (span == 32 ? 0xffffffffu : ((1u << span) - 1u))
-                                  : (live > 0 ? ((1u << live) - 1u) : 0u);
-              if (a.valid_bits) {
-                const int wi = key >> 5;
-                const uint32_t word =
-                    wi < a.valid_words
-                        ? __ldg(a.valid_bits + static_cast<long long>(tile.b) * a.valid_words + wi)
-                        : 0u;
-                bits &= (word >> (key & 31));
-              }
-            }
-            colmask[col0 >> 5] |= bits << (col0 & 31);
-          }
-        }
-        // ---- S row -----------------------------------------------------------------------
-        uint32_t sraw[kKvTile];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          tmem_ld32(s_col + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&sraw[q * 32]));
-        tmem_ld_wait();
-        float x[kKvTile];
-#pragma unroll
-        for (int c = 0; c < kKvTile; ++c) x[c] = __uint_as_float(sraw[c]);
         const bool full = !a.valid_bits && !zero_v &&
                           (!causal || kmax <= pos) && (wl < 0 || kmin >= pos - wl);
-        float mt = -INFINITY;
-        if (full) {
+        if (!full) {
 #pragma unroll
-          for (int c = 0; c < kKvTile; ++c) {
-            x[c] *= sl2;
-            mt = fmaxf(mt, x[c]);
-          }
-        } else {
-          int hi_lim[NSUB], lo_lim[NSUB];
+          for (int i = 0; i < 4; ++i) colmask[i] = 0u;
 #pragma unroll
           for (int c = 0; c < NSUB; ++c) {
-            hi_lim[c] = causal ? pos - k0[c] : 0x7fffffff;
-            lo_lim[c] = wl >= 0 ? pos - wl - k0[c] : -0x7fffffff;
-          }
+            // live-key bits of the CK columns of sub-chunk c
 #pragma unroll
-          for (int c = 0; c < kKvTile; ++c) {
-            const int sc = c / CK, r = c % CK;
-            const bool vis = ((colmask[c >> 5] >> (c & 31)) & 1u) && r <= hi_lim[sc] &&
-                             r >= lo_lim[sc];
-            x[c] = vis ? x[c] * sl2 : -INFINITY;
-            mt = fmaxf(mt, x[c]);
+            for (int part = 0; part < (CK + 31) / 32; ++part) {
+              const int col0 = c * CK + part * 32;        // first column of this 32-span
+              const int span = CK < 32 ? CK : 32;
+              uint32_t bits = 0u;
+              if (k0[c] >= 0) {
+                const int key = k0[c] + part * 32;
+                const int live = L - key;                  // keys < L in this span
+                bits = live >= span ? (span == 32 ? 0xffffffffu : ((1u << span) - 1u))
+                                    : (live > 0 ? ((1u << live) - 1u) : 0u);
+                if (a.valid_bits) {
+                  const int wi = key >> 5;
+                  const uint32_t word =
+                      wi < a.valid_words
+                          ? __ldg(a.valid_bits + static_cast<long long>(t.rec.b) * a.valid_words +
+                                  wi)
+                          : 0u;
+                  bits &= (word >> (key & 31));
+                }
+              }
+              colmask[col0 >> 5] |= bits << (col0 & 31);
+            }
           }
         }
+        // ---- S row: four 32-column loads in flight, one wait ----------------------------
+        uint32_t r[kKvTile];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          tmem_ld32(s_col + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[q * 32]));
+        tmem_ld_wait();
+        if (!full) {
+          // Invisible scores become -inf in place.  Column facts (slot live, j < len, valid
+          // bit) are the same for every row: only 32-column words with a dead key are touched.
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t wbits = colmask[q];
+            if (wbits != 0xffffffffu) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (!(wbits & (1u << i))) r[q * 32 + i] = 0xff800000u;
+            }
+          }
+          // causal / window limits only where this row's position cuts the tile
+          if ((causal && kmax > pos) || (wl >= 0 && kmin < pos - wl)) {
+            int hi_lim[NSUB], lo_lim[NSUB];          // per sub-chunk, relative to its first key
+#pragma unroll
+            for (int c = 0; c < NSUB; ++c) {
+              hi_lim[c] = causal ? pos - k0[c] : 0x7fffffff;
+              lo_lim[c] = wl >= 0 ? pos - wl - k0[c] : -0x7fffffff;
+            }
+#pragma unroll
+            for (int c = 0; c < kKvTile; ++c)
+              if (c % CK > hi_lim[c / CK] || c % CK < lo_lim[c / CK]) r[c] = 0xff800000u;
+          }
+        }
+        // row maximum: 8 independent chains of 3-input max, then a short tree
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kKvTile; c += 2)
+          mx[(c >> 1) & 7] = max3f(mx[(c >> 1) & 7], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+        // scores are scaled by sl2 > 0 after the maximum, which commutes with it
+        const float mt =
+            fmaxf(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], fmaxf(mx[5], fmaxf(mx[6], mx[7])))) *
+            sl2;
         // ---- online softmax with a lazily moved maximum ----------------------------------
         float alpha = 1.f;
         if (mt > m_run + kRescaleThreshold || (m_run == -INFINITY && mt > -INFINITY)) {
           alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mt);
           m_run = mt;
         }
-        const float mu = m_run == -INFINITY ? 0.f : m_run;
-        float rs = 0.f;
-        uint32_t pk[kKvTile / 2];
+        const float nmu = m_run == -INFINITY ? 0.f : -m_run;
+        // ---- P = exp2(s * sl2 - mu) and the row sum; bf16 pairs packed in place into r[j] ---
+        float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
 #pragma unroll
-        for (int c = 0; c < kKvTile; c += 2) {
-          const float p0 = fast_exp2(x[c] - mu);
-          const float p1 = fast_exp2(x[c + 1] - mu);
-          rs += p0 + p1;
-          pk[c >> 1] = pack_bf16(p0, p1);
+        for (int j = 0; j < kKvTile / 2; ++j) {
+          float x0, x1;
+          ffma2_bcast(x0, x1, __uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]), sl2, nmu);
+          float p0, p1;
+          exp2_pair_f16(x0, x1, p0, p1);
+          if (j & 1) fadd2(sb0, sb1, p0, p1);
+          else fadd2(sa0, sa1, p0, p1);
+          r[j] = pack_bf16(p0, p1);
         }
-        l_run = l_run * alpha + rs;
-        // O was last written by PV of tile n-1, which completed before S of tile n
+        tmem_st32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_st32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        l_run = l_run * alpha + ((sa0 + sa1) + (sb0 + sb1));
+        // O was last written by PV of the previous KV tile, which completed before this S
         if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
           for (int q = 0; q < 4; ++q) {
@@ -378,19 +502,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             tmem_st32(o_col + q * 32, ov);
           }
         }
-        tmem_st32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         tmem_st_wait();
         if (zero_v && w == 0) {
           // Rows of keys that are not live (past the length, or empty slots) may hold
           // stale or non-finite data; P is 0 there, so make V exactly 0 as well.
-          const int st = n % kStages;
-          if (mbar_wait_warp(&ctl->v_full[st], (n / kStages) & 1, a.status, abort_flag)) {
+          const int vs = it % kVStages;
+          if (mbar_wait_warp(&ctl->v_full[vs], (it / kVStages) & 1, a.status, abort_flag)) {
             const int c = m;                         // this thread clears key slot m
             const int k = k0[c / CK];
             if (k < 0 || k + (c % CK) >= L) {
-              uint8_t* vt = kv_s + st * 2 * kKvBytes + kKvBytes;
-              uint4 z = make_uint4(0u, 0u, 0u, 0u);
+              uint8_t* vt = v_s + vs * kKvBytes;
+              const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 *reinterpret_cast<uint4*>(vt + c * 128 + i * 16) = z;
@@ -404,10 +526,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         mbar_arrive(&ctl->p_full[w]);
       }
       // ---- epilogue ------------------------------------------------------------------------
-      const bool have_o = N > 0 && mbar_wait_warp(&ctl->o_final[w], 0, a.status, abort_flag);
-      if (have_o) tc_fence_after();
-      const int head = tile.g * G + (m % G);
-      const long long orow = static_cast<long long>(tile.q_row0 + w * TM + m / G) * a.Hq + head;
+      bool have_o = false;
+      if (ok && N > 0) {
+        have_o = mbar_wait_warp(&ctl->o_final[w], oc & 1, a.status, abort_flag);
+        ++oc;
+        if (have_o) tc_fence_after();
+      }
+      const int head = t.rec.g * G + (m % G);
+      const long long orow = static_cast<long long>(t.rec.q_row0 + w * TM + m / G) * a.Hq + head;
       const float inv = l_run > 0.f ? a.out_scale / l_run : 0.f;
 #pragma unroll 1
       for (int q = 0; q < 4; ++q) {
@@ -415,6 +541,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (have_o) {
           tmem_ld32(o_col + q * 32, ov);
           tmem_ld_wait();
+          if (q == 3) {                       // O_w fully read: the next tile may overwrite it
+            tc_fence_before();
+            mbar_arrive(&ctl->o_empty[w]);
+          }
         }
         if (row_valid) {
           uint32_t pkd[16];
@@ -431,6 +561,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       }
       if (row_valid && a.lse)
         a.lse[orow] = l_run > 0.f ? (m_run + fast_log2(l_run)) * kLn2 : -INFINITY;
+      kv_it += N;
     }
   }
   tc_fence_before();
@@ -442,6 +573,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   }
 }
 
+int g_num_sms = 0;
+
 template <int CK>
 int launch_ck(const AttnLaunch& a, cudaStream_t st) {
   static bool attr_set = false;
@@ -451,7 +584,14 @@ int launch_ck(const AttnLaunch& a, cudaStream_t st) {
       return -1;
     attr_set = true;
   }
-  attn_tc_kernel<CK><<<a.capacity, kThreads, kSmemBytes, st>>>(a.qmap, a.kmap, a.vmap, a);
+  if (g_num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return -1;
+  }
+  const int grid = a.capacity < g_num_sms ? a.capacity : g_num_sms;
+  attn_tc_kernel<CK><<<grid, kThreads, kSmemBytes, st>>>(a.qmap, a.kmap, a.vmap, a);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

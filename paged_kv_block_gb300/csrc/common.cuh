@@ -54,11 +54,14 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// Test for completion; the thread may sleep (up to about a microsecond) while the phase is
+// incomplete and is woken when it completes, so waiting threads do not spin on the issue
+// slots of the warps they share a sub-partition with.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, 1000;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
@@ -282,6 +285,16 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Move registers between warpgroups (every warp of a warpgroup must execute the same one).
+template <int N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -291,11 +304,64 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (d0, d1) = (a0, a1) * s + (t, t) as one packed fp32x2 FMA.
+__device__ __forceinline__ void ffma2_bcast(float& d0, float& d1, float a0, float a1, float s,
+                                            float t) {
+  asm("{\n\t.reg .b64 ra, rs, rt, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rs, {%4, %4};\n\tmov.b64 rt, {%5, %5};\n\t"
+      "fma.rn.f32x2 rd, ra, rs, rt;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(s), "f"(t));
+}
+// (a0, a1) += (b0, b1) as one packed fp32x2 add.
+__device__ __forceinline__ void fadd2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb;\n\t"
+      "mov.b64 ra, {%0, %1};\n\tmov.b64 rb, {%2, %3};\n\t"
+      "add.rn.f32x2 ra, ra, rb;\n\tmov.b64 {%0, %1}, ra;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
+// (2^x0, 2^x1) through one packed half-precision MUFU op: the arguments are rounded to fp16
+// (11 significant bits), the results come back as fp32.  -inf gives 0; results below the
+// fp16 range flush to 0.
+__device__ __forceinline__ void exp2_pair_f16(float x0, float x1, float& p0, float& p1) {
+  asm("{\n\t.reg .b32 h, e;\n\t.reg .b16 e0, e1;\n\t"
+      "cvt.rn.f16x2.f32 h, %3, %2;\n\t"
+      "ex2.approx.f16x2 e, h;\n\t"
+      "mov.b32 {e0, e1}, e;\n\t"
+      "cvt.f32.f16 %0, e0;\n\tcvt.f32.f16 %1, e1;\n\t}"
+      : "=f"(p0), "=f"(p1)
+      : "f"(x0), "f"(x1));
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// 2^x on the FMA pipe.  Range reduction by rounding to nearest (x = j + f, f in [-0.5, 0.5],
+// using the 1.5 * 2^23 addition trick), 2^f by a cubic whose coefficients were fitted here to
+// minimise the maximum relative error on [-0.5, 0.5] (iteratively reweighted least squares;
+// max relative error 7.5e-5 in fp32), and 2^j added into the exponent field.  Arguments
+// below -125 (including -inf) give exactly 0.
+__device__ __forceinline__ float poly_exp2(float x) {
+  const float xc = fmaxf(x, -125.f);
+  const float t = xc + 12582912.f;
+  const float j = t - 12582912.f;
+  const float f = xc - j;
+  float p = fmaf(fmaf(fmaf(0.0551715009f, f, 0.2426109612f), f, 0.6932609677f), f,
+                 0.9999280572f);
+  p = __int_as_float(__float_as_int(p) + ((__float_as_int(t) - 0x4B400000) << 23));
+  return x < -125.f ? 0.f : p;
+}
+
 __device__ __forceinline__ float fast_log2(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
