@@ -169,7 +169,7 @@ PrefillLayout prefill_layout(const paged_prefill_params* p) {
 
 // ---- decode layout ------------------------------------------------------------------------
 struct DecodeLayout {
-  size_t status, split_off, items, part_lse, part_o, total;
+  size_t status, split_off, counters, items, part_lse, part_o, total;
   int capacity, chunk, max_splits;
 };
 
@@ -211,6 +211,7 @@ DecodeLayout decode_layout(const paged_decode_params* p) {
   s.capacity = static_cast<int>(static_cast<long long>(p->batch) * p->num_kv_heads * s.max_splits);
   s.status = l.take(sizeof(uint32_t) * 4);
   s.split_off = l.take(sizeof(int) * static_cast<size_t>(p->batch + 1));
+  s.counters = l.take(sizeof(int) * (static_cast<size_t>(p->batch) * p->num_kv_heads + 1));
   s.items = l.take(sizeof(SplitItem) * static_cast<size_t>(s.capacity > 0 ? s.capacity : 1));
   s.part_lse = l.take(sizeof(float) * static_cast<size_t>(s.capacity) * G + 4);
   s.part_o = l.take(sizeof(float) * static_cast<size_t>(s.capacity) * G * p->head_dim + 4);
@@ -564,20 +565,26 @@ int paged_decode_run(const paged_decode_params* p, const void* query, const void
   const int Hkv = p->num_kv_heads, ps = p->page_size, D = p->head_dim;
   int* split_off = at<int>(ws, s.split_off);
   SplitItem* items = at<SplitItem>(ws, s.items);
+  int* counters = at<int>(ws, s.counters);
   launch_decode_plan(seq_lens, p->batch, Hkv, s.chunk, p->window_left, s.max_splits, split_off,
-                     items, st);
+                     items, counters, st);
   const int R = ps < 64 ? ps : 64;
   const long long pool_rows = static_cast<long long>(p->num_pages) * (p->combined_cache ? 2 : 1) *
                               Hkv * ps;
-  CUtensorMap kmap, vmap;
+  CUtensorMap kmap, vmap, qmap;
+  const int G = p->num_qo_heads / Hkv;
   if (!encode_rows_map(&kmap, k, pool_rows, D, R) ||
-      !encode_rows_map(&vmap, p->combined_cache ? k : v, pool_rows, D, R))
+      !encode_rows_map(&vmap, p->combined_cache ? k : v, pool_rows, D, R) ||
+      !encode_rows_map(&qmap, query, static_cast<long long>(p->batch) * p->num_qo_heads, D, G))
     return PAGED_ATTN_ERR_CUDA;
   const float scale =
       p->bmm1_scale > 0.f ? p->bmm1_scale : 1.0f / std::sqrt(static_cast<float>(D));
   DecodeLaunch a{};
   a.kmap = &kmap;
   a.vmap = &vmap;
+  a.qmap = &qmap;
+  a.counters = counters;
+  a.work_counter = counters + static_cast<long long>(p->batch) * Hkv;
   a.q = static_cast<const __nv_bfloat16*>(query);
   a.kv_indptr = kv_indptr;
   a.kv_indices = kv_indices;

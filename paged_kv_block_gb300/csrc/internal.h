@@ -51,8 +51,10 @@ void launch_bitmap_plan(const uint8_t* sel, const int* lo, const int* hi, const 
                         const int* blast, int T, int NB, long long capacity, int* indptr,
                         int* indices, uint32_t* status, cudaStream_t st);
 
+// Split-KV work list, and zeroed work / merge counters (B * Hkv + 1 ints).
 void launch_decode_plan(const int* seq_lens, int B, int Hkv, int chunk, int window_left,
-                        int max_splits, int* split_offset, SplitItem* items, cudaStream_t st);
+                        int max_splits, int* split_offset, SplitItem* items, int* counters,
+                        cudaStream_t st);
 
 // Keys per sub-chunk of a 128-key KV tile: the largest of 128, 64 or kv_block_size that
 // divides kv_block_size (dense tiles use 128).
@@ -67,6 +69,9 @@ inline int attn_sub_chunk(int kv_block_size, bool block_sparse) {
 struct DecodeLaunch {
   const CUtensorMap* kmap;   // host copies, passed by value to the kernel
   const CUtensorMap* vmap;
+  const CUtensorMap* qmap;   // query rows [B * Hq, D], box 64 x G
+  int* work_counter;         // next work item (zeroed by the planner)
+  int* counters;             // finished splits per (request, KV head) (zeroed by the planner)
   const __nv_bfloat16* q;    // [B, Hq, D]
   const int* kv_indptr;
   const int* kv_indices;

@@ -303,8 +303,10 @@ __device__ __forceinline__ void decode_split_range(int L, int chunk, int window_
   n = s1 - s0;
 }
 
-__global__ void decode_plan_kernel(const int* __restrict__ lens, int B, int chunk,
-                                   int window_left, int max_splits, int* __restrict__ off) {
+// One CTA: split counts, their exclusive scan, the work items, and zeroed counters.
+__global__ void decode_plan_kernel(const int* __restrict__ lens, int B, int Hkv, int chunk,
+                                   int window_left, int max_splits, int* __restrict__ off,
+                                   SplitItem* __restrict__ items, int* __restrict__ counters) {
   __shared__ int warp_sums[32];
   int carry = 0;
   for (int base = 0; base < B; base += blockDim.x) {
@@ -321,26 +323,26 @@ __global__ void decode_plan_kernel(const int* __restrict__ lens, int B, int chun
     carry += total;
   }
   if (threadIdx.x == 0) off[B] = carry;
-}
-
-__global__ void decode_items_kernel(const int* __restrict__ lens, int Hkv, int chunk,
-                                    int window_left, const int* __restrict__ off,
-                                    SplitItem* __restrict__ items) {
-  const int b = blockIdx.x;
-  int L = lens[b];
-  int lo, s0, n_all;
-  decode_split_range(L, chunk, window_left, lo, s0, n_all);
-  if (L < 0) L = 0;
-  const int n = off[b + 1] - off[b];
-  for (int idx = threadIdx.x; idx < Hkv * n; idx += blockDim.x) {
-    const int g = idx / n, k = idx % n;
-    const long long s = static_cast<long long>(s0) + k;
-    SplitItem it;
-    it.b = b;
-    it.g = g;
-    it.kv_begin = static_cast<int>(max(s * chunk, static_cast<long long>(lo)));
-    it.kv_end = static_cast<int>(min((s + 1) * chunk, static_cast<long long>(L)));
-    items[static_cast<long long>(Hkv) * off[b] + idx] = it;
+  for (int i = threadIdx.x; i <= B * Hkv; i += blockDim.x) counters[i] = 0;
+  __syncthreads();
+  // items of request b: one warp per request
+  const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int b = threadIdx.x >> 5; b < B; b += nw) {
+    int L = lens[b];
+    int lo, s0, n_all;
+    decode_split_range(L, chunk, window_left, lo, s0, n_all);
+    if (L < 0) L = 0;
+    const int n = off[b + 1] - off[b];
+    for (int idx = lane; idx < Hkv * n; idx += 32) {
+      const int g = idx / n, k = idx % n;
+      const long long s = static_cast<long long>(s0) + k;
+      SplitItem it;
+      it.b = b;
+      it.g = g;
+      it.kv_begin = static_cast<int>(max(s * chunk, static_cast<long long>(lo)));
+      it.kv_end = static_cast<int>(min((s + 1) * chunk, static_cast<long long>(L)));
+      items[static_cast<long long>(Hkv) * off[b] + idx] = it;
+    }
   }
 }
 
@@ -403,15 +405,11 @@ void launch_bitmap_plan(const uint8_t* sel, const int* lo, const int* hi, const 
 }
 
 void launch_decode_plan(const int* seq_lens, int B, int Hkv, int chunk, int window_left,
-                        int max_splits, int* split_offset, SplitItem* items, cudaStream_t st) {
-  decode_plan_kernel<<<1, 1024, 0, st>>>(seq_lens, B, chunk, window_left, max_splits,
-                                         split_offset);
+                        int max_splits, int* split_offset, SplitItem* items, int* counters,
+                        cudaStream_t st) {
+  decode_plan_kernel<<<1, 1024, 0, st>>>(seq_lens, B, Hkv, chunk, window_left, max_splits,
+                                         split_offset, items, counters);
   count_launches(1);
-  if (B > 0) {
-    decode_items_kernel<<<B, 256, 0, st>>>(seq_lens, Hkv, chunk, window_left, split_offset,
-                                           items);
-    count_launches(1);
-  }
 }
 
 }  // namespace pa
