@@ -30,10 +30,6 @@ constexpr int kN = 16;                 // query heads of one KV head, padded (MM
 constexpr int kSlots = 128;            // key slots per tile = 32 blocks of 4
 constexpr int kStageBytes = 32768;     // [128 keys][128 d] bf16 as two 64-column halves
 constexpr int kRing = 3;
-// A stage is announced once the copies of the stage after it are issued.  With the MMA
-// order QK(n), PV(n), freeing V(n) needs the second V stage of tile n announced before the
-// producer issues the stage that reuses its slot, which bounds the lag by kRing - 2.
-constexpr int kLag = 1;
 constexpr int kThreads = 288;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
@@ -129,10 +125,7 @@ __global__ void __launch_bounds__(kThreads, 2) qsa_kernel(QsaLaunch a) {
       cp_async16(q_addr + (cc >> 3) * (kN * 128) + r * 128 + (((cc & 7) ^ (r & 7)) << 4), src,
                  r < G ? 16u : 0u);
     }
-    cp_async_commit();
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    mbar_arrive(&ctl->q_full);
+    cp_async_arrive_noinc(&ctl->q_full);
     const uint32_t ring_addr = smem_u32(ring);
     bool ok = true;
     for (int s = 0; s < S && ok; ++s) {
@@ -165,17 +158,10 @@ __global__ void __launch_bounds__(kThreads, 2) qsa_kernel(QsaLaunch a) {
         cp_async16(stage + (cc >> 3) * 16384 + row * 128 + (((cc & 7) ^ (row & 7)) << 4), src,
                    tok >= 0 ? 16u : 0u);
       }
-      cp_async_commit();
-      if (s >= kLag) {
-        cp_async_wait<kLag>();                         // stage s - kLag has landed
-        fence_proxy_async_smem();
-        mbar_arrive(&ctl->full[(s - kLag) % kRing]);
-      }
+      // the stage's barrier completes when this thread's copies (and the other 127's) land
+      cp_async_arrive_noinc(&ctl->full[slot]);
     }
     cp_async_wait<0>();
-    fence_proxy_async_smem();
-    if (ok)
-      for (int s = S - kLag > 0 ? S - kLag : 0; s < S; ++s) mbar_arrive(&ctl->full[s % kRing]);
   } else if (warp == 4) {
     // ================================ MMA issuer ==========================================
     if (lane == 0 && N > 0) {
@@ -183,11 +169,13 @@ __global__ void __launch_bounds__(kThreads, 2) qsa_kernel(QsaLaunch a) {
       constexpr uint32_t idesc_pv = idesc_bf16(128, kN, true, false);
       const uint32_t ring_addr = smem_u32(ring), q_addr = smem_u32(q_s), p_addr = smem_u32(p_s);
       bool ok = mbar_wait(&ctl->q_full, 0, a.status, abort_flag);
+      fence_proxy_async_smem();   // cp.async (generic proxy) writes -> tensor-core reads
       for (int n = 0; ok && n < N; ++n) {
         const int s0 = 4 * n;
         if (!mbar_wait(&ctl->full[s0 % kRing], (s0 / kRing) & 1, a.status, abort_flag) ||
             !mbar_wait(&ctl->full[(s0 + 1) % kRing], ((s0 + 1) / kRing) & 1, a.status, abort_flag))
           break;
+        fence_proxy_async_smem();
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 16; ++ks) {
@@ -203,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 2) qsa_kernel(QsaLaunch a) {
             !mbar_wait(&ctl->full[(s0 + 2) % kRing], ((s0 + 2) / kRing) & 1, a.status, abort_flag) ||
             !mbar_wait(&ctl->full[(s0 + 3) % kRing], ((s0 + 3) / kRing) & 1, a.status, abort_flag))
           break;
+        fence_proxy_async_smem();
         tc_fence_after();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
