@@ -252,6 +252,22 @@ bool encode_q_map(CUtensorMap* map, const void* base, long long rows, int Hq, in
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_block_pair_map(CUtensorMap* map, const void* base, long long tokens, int Hkv, int D) {
+  auto fn = encode_fn();
+  if (!fn || tokens <= 0 || D % 64 || D > 256) return false;
+  // [tokens, Hkv, D] viewed as (64 columns, head, token, 64-column chunk); the chunk stride
+  // (128 B) is smaller than the others, which the copy engine allows.
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(tokens),
+                        static_cast<cuuint64_t>(D / 64)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(Hkv) * D * 2,
+                           128};
+  cuuint32_t box[4] = {64, 2, 4, static_cast<cuuint32_t>(D / 64)};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---- kernel timer and launch counter -------------------------------------------------------
 namespace {
 std::atomic<long long> g_launches{0};

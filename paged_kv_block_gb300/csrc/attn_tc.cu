@@ -145,8 +145,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                const __grid_constant__ CUtensorMap vmap, AttnLaunch a) {
   constexpr int NSUB = kKvTile / CK;   // sub-chunks per KV tile
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* base = smem_align<1024>(smem_raw);
   uint8_t* q_s = base;                                   // 2 sub-tiles
   uint8_t* k_s = q_s + 2 * kQBytes;                      // K ring
   uint8_t* v_s = k_s + kKStages * kKvBytes;              // V ring
@@ -213,7 +212,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         const TileInfo<CK> t = load_tile<CK>(a, idx);
         if (t.N == 0) continue;
         if (is_k) {
-          if (qcount > 0 && !mbar_wait(&ctl->q_empty, (qcount - 1) & 1, a.status, abort_flag)) {
+          if (qcount > 0 && !mbar_wait<true>(&ctl->q_empty, (qcount - 1) & 1, a.status, abort_flag)) {
             ok = false;
             break;
           }
@@ -230,7 +229,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         for (int n = 0; n < t.N; ++n) {
           const int it = kv_it + n, slot = it % stages;
           if (it >= stages &&
-              !mbar_wait(&empty[slot], ((it / stages) - 1) & 1, a.status, abort_flag)) {
+              !mbar_wait<true>(&empty[slot], ((it / stages) - 1) & 1, a.status, abort_flag)) {
             ok = false;
             break;
           }
@@ -288,8 +287,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (N == 0) continue;
         const bool two = t.nsub > 1;
         const int it0 = kv_it;
-        ok = mbar_wait(&ctl->q_full, qcount & 1, a.status, abort_flag) &&
-             mbar_wait(&ctl->k_full[it0 % kKStages], (it0 / kKStages) & 1, a.status, abort_flag);
+        ok = mbar_wait<true>(&ctl->q_full, qcount & 1, a.status, abort_flag) &&
+             mbar_wait<true>(&ctl->k_full[it0 % kKStages], (it0 / kKStages) & 1, a.status, abort_flag);
         ++qcount;
         if (!ok) break;
         tc_fence_after();
@@ -299,10 +298,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (N == 1) mma_commit(&ctl->q_empty);
         for (int n = 0; n < N; ++n) {
           const int it = it0 + n, vs = it % kVStages;
-          if (!mbar_wait(&ctl->v_full[vs], (it / kVStages) & 1, a.status, abort_flag) ||
-              !mbar_wait(&ctl->p_full[0], it & 1, a.status, abort_flag) ||
+          if (!mbar_wait<true>(&ctl->v_full[vs], (it / kVStages) & 1, a.status, abort_flag) ||
+              !mbar_wait<true>(&ctl->p_full[0], it & 1, a.status, abort_flag) ||
               (n == 0 && ep[0] > 0 &&
-               !mbar_wait(&ctl->o_empty[0], (ep[0] - 1) & 1, a.status, abort_flag))) {
+               !mbar_wait<true>(&ctl->o_empty[0], (ep[0] - 1) & 1, a.status, abort_flag))) {
             ok = false;
             break;
           }
@@ -312,7 +311,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           const bool more = n + 1 < N;
           const int ks_next = (it + 1) % kKStages;
           if (more) {
-            if (!mbar_wait(&ctl->k_full[ks_next], ((it + 1) / kKStages) & 1, a.status,
+            if (!mbar_wait<true>(&ctl->k_full[ks_next], ((it + 1) / kKStages) & 1, a.status,
                            abort_flag)) {
               ok = false;
               break;
@@ -321,9 +320,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             issue_qk(0, ks_next);
           }
           if (two) {
-            if (!mbar_wait(&ctl->p_full[1], pc1 & 1, a.status, abort_flag) ||
+            if (!mbar_wait<true>(&ctl->p_full[1], pc1 & 1, a.status, abort_flag) ||
                 (n == 0 && ep[1] > 0 &&
-                 !mbar_wait(&ctl->o_empty[1], (ep[1] - 1) & 1, a.status, abort_flag))) {
+                 !mbar_wait<true>(&ctl->o_empty[1], (ep[1] - 1) & 1, a.status, abort_flag))) {
               ok = false;
               break;
             }
@@ -373,7 +372,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       float m_run = -INFINITY, l_run = 0.f;
       for (int n = 0; n < N; ++n) {
         const int it = kv_it + n;
-        if (!mbar_wait_warp(&ctl->s_full[w], sc & 1, a.status, abort_flag)) {
+        if (!mbar_wait_warp<true>(&ctl->s_full[w], sc & 1, a.status, abort_flag)) {
           ok = false;
           break;
         }
@@ -507,7 +506,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           // Rows of keys that are not live (past the length, or empty slots) may hold
           // stale or non-finite data; P is 0 there, so make V exactly 0 as well.
           const int vs = it % kVStages;
-          if (mbar_wait_warp(&ctl->v_full[vs], (it / kVStages) & 1, a.status, abort_flag)) {
+          if (mbar_wait_warp<true>(&ctl->v_full[vs], (it / kVStages) & 1, a.status, abort_flag)) {
             const int c = m;                         // this thread clears key slot m
             const int k = k0[c / CK];
             if (k < 0 || k + (c % CK) >= L) {
@@ -528,7 +527,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       // ---- epilogue ------------------------------------------------------------------------
       bool have_o = false;
       if (ok && N > 0) {
-        have_o = mbar_wait_warp(&ctl->o_final[w], oc & 1, a.status, abort_flag);
+        have_o = mbar_wait_warp<true>(&ctl->o_final[w], oc & 1, a.status, abort_flag);
         ++oc;
         if (have_o) tc_fence_after();
       }

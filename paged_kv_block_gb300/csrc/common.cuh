@@ -21,6 +21,14 @@ constexpr long long kWaitCycles = 200000000LL;
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// Dynamic shared memory rounded up to kAlign bytes.  The result is the shared array plus an
+// offset, so the compiler still knows that every pointer derived from it addresses shared
+// memory and emits shared-window loads and stores; rounding through an integer would make
+// them generic accesses, which the compiler must order conservatively.
+template <uint32_t kAlign>
+__device__ __forceinline__ uint8_t* smem_align(uint8_t* raw) {
+  return raw + ((kAlign - (smem_u32(raw) & (kAlign - 1))) & (kAlign - 1));
+}
 
 __device__ __forceinline__ void report_error(uint32_t* status, uint32_t bit) {
   if (status) atomicOr(status, bit);
@@ -72,11 +80,29 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // Wait until the phase with the given parity has completed.  Gives up after kWaitCycles,
 // records kErrTimeout and sets *abort (a CTA-wide flag in shared memory) so that every
 // later wait of the CTA returns at once; the kernel then runs to its end without further
-// blocking.  Returns false when the wait did not succeed.
+// blocking.  Returns false when the wait did not succeed.  The first test is inline; the
+// polling loop is a separate function so that it adds no code to the kernels' hot loops.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                                   uint32_t* status, volatile int* abort) {
+  const long long t0 = clock64();
+  while (true) {
+    if (*abort) return false;
+    if (mbar_test(bar, parity)) return true;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort = 1;
+      report_error(status, kErrTimeout);
+      return false;
+    }
+  }
+}
+// kInlineLoop keeps the polling loop inline, for kernels whose register split (setmaxnreg)
+// leaves no room for a call.
+template <bool kInlineLoop = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
                                           volatile int* abort) {
   if (mbar_test(bar, parity)) return true;
-  long long t0 = clock64();
+  if (!kInlineLoop) return mbar_wait_slow(bar, parity, status, abort);
+  const long long t0 = clock64();
   while (true) {
     if (*abort) return false;
     if (mbar_test(bar, parity)) return true;
@@ -90,9 +116,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 
 // Warp-uniform variant for code that follows with warp-collective (.sync.aligned)
 // instructions: the warp proceeds only if every lane's wait succeeded.
+template <bool kInlineLoop = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status,
                                                volatile int* abort) {
-  const bool ok = mbar_wait(bar, parity, status, abort);
+  const bool ok = mbar_wait<kInlineLoop>(bar, parity, status, abort);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -113,6 +140,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -219,6 +254,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
+}
+// 32 lanes x 32 bit, 4 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
 }
 // 32 lanes x 32 bit, 16 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {

@@ -64,8 +64,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap,
                     const __grid_constant__ CUtensorMap qmap, DecodeLaunch a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* tiles = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* tiles = smem_align<1024>(smem_raw);
   const int G = a.Hq / a.Hkv;
   const int qhalf = q_half_bytes(G);
   uint8_t* qslots = tiles + kStages * kStageBytes;

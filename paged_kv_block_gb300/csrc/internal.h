@@ -126,5 +126,8 @@ int launch_attn(const AttnLaunch& a, cudaStream_t st);
 bool encode_rows_map(CUtensorMap* map, const void* base, long long rows, int D, int box_rows);
 bool encode_q_map(CUtensorMap* map, const void* base, long long rows, int Hq, int D,
                   int box_heads, int box_tokens);
+// [tokens, Hkv, D] bf16 with box = 4 tokens x 2 KV heads x all D / 64 column chunks: one
+// 4-token block of a KV-head pair lands as D / 64 8-row, 128-byte-swizzled atoms.
+bool encode_block_pair_map(CUtensorMap* map, const void* base, long long tokens, int Hkv, int D);
 
 }  // namespace pa

@@ -1,20 +1,37 @@
 // Per-query block-bitmap attention forward (FlashInfer page qsa_forward) on tcgen05.
 //
-// One CTA per (query token t, KV head g).  The planner has already turned row t of the
-// bitmap into the ascending list of selected blocks that meet [lo[t], hi[t]]; every block
-// holds block_size = 4 key tokens, so a tile of 32 blocks is 128 key slots.  The work per
-// (t, g) is a gather of ~1 MB of scattered K/V rows used by only G query heads, so the path
-// is bound by the L2 -> SM gather rather than by the tensor pipe.  The MMAs therefore take
-// the keys as the M dimension:
-//   S^T [128 keys x 16]  = K_tile [128 x 256] * Q^T        (Q: G heads padded to 16 rows)
-//   O^T [256 d x 16]    += V_tile^T [256 x 128] * P^T        (two M = 128 halves of d)
+// One CTA per (query token t, pair of KV heads g0, g0 + 1).  The planner has already turned
+// row t of the bitmap into the ascending list of selected blocks that meet [lo[t], hi[t]];
+// every block holds block_size = 4 key tokens.  With the cache laid out [T, Hkv, D], the
+// rows of one block for two neighbouring KV heads, 64 columns of d at a time, form a
+// [4 tokens][2 heads][64 d] box of 8 rows x 128 B: one 128-byte-swizzle atom.  One copy
+// (a 4-D box) brings the four such atoms (the four 64-column chunks) of a block, so the
+// gather is one 4 KB copy per block landing directly in the layout the tensor core reads.  The key
+// rows of a tile are (block, token, head) triples; the MMA's N dimension holds the query
+// heads of both KV heads, and the cross pairs (a key row of one head against a query head
+// of the other) are masked out of the softmax, so each head sees exactly its own attention.
+// The work is bound by the L2 -> SM gather (the unique K/V is a few tens of MB, read many
+// times), so the MMAs take the key rows as the M dimension:
+//   S^T [128 rows x 32] = K_tile [128 x 256] * Q^T        (Q: 2 x G heads, each group
+//                                                            padded to 16)
+//   O^T [256 d x 32]   += V_tile^T [256 x 128] * P^T      (two M = 128 halves of d)
+// A tile is K then V, each 64 KB laid out [16 blocks][4 chunks][8 rows][128 B], so the MMAs
+// see 16 blocks at a 4 KB stride.  The copies run as two independent pipelines, one per half
+// of the blocks (0-7 and 8-15), each with its own barriers: the copy rate of one pipeline
+// (one chain of stage barriers) saturates well below the SM's, and two pipelines nearly
+// double it.  The two pipelines' 32 KB slots interleave into three 64 KB pair slots.  Units
+// are copied in the order the MMAs consume them, K(0), K(1), V(0), K(2), V(1), ..., V(N - 1):
+// S^T(n + 1) is computed before PV(n), so K(n + 1) can be in flight two tiles ahead and the
+// softmax of one tile follows the previous one without waiting for a copy.
 // Roles (288 threads):
-//   warps 0-3  producers: cp.async gathers (zero-filled for dead slots) of 32 KB stages
-//              (K d0-127, K d128-255, V d0-127, V d128-255 of each tile) into a 3-stage ring
-//   warp  4    TMEM owner and MMA issuer (one thread)
-//   warps 5-8  softmax: thread = key slot (TMEM lane) for S^T and = d row for O^T; the
-//              column maxima over the 128 keys come from redux.sync plus a shared-memory
-//              exchange, the row sums are accumulated per thread and reduced at the end.
+//   warps 0-3  producers: per tile publish the key-row table (token of each row, or dead),
+//              fetching the next tile's block spans a tile ahead; warps 2p and 2p + 1 form
+//              pipeline p and copy blocks 8p .. 8p + 3 and 8p + 4 .. 8p + 7
+//   warps 4-7  softmax: thread = key row (TMEM lane) of S^T and = d row of O^T; column
+//              maxima per head group from redux.sync plus a shared-memory exchange; rows
+//              that are dead but were loaded from memory get their V row zeroed, so
+//              non-finite data outside the selection cannot reach the output.
+//   warp 8     TMEM owner and MMA issuer (one thread)
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -26,33 +43,47 @@ namespace pa {
 namespace {
 
 constexpr int kD = 256;
-constexpr int kN = 16;                 // query heads of one KV head, padded (MMA N)
-constexpr int kSlots = 128;            // key slots per tile = 32 blocks of 4
-constexpr int kStageBytes = 32768;     // [128 keys][128 d] bf16 as two 64-column halves
-constexpr int kRing = 3;
+constexpr int kGroupCols = 16;                // query heads of one KV head, padded
+constexpr int kN = 2 * kGroupCols;            // MMA N: the query heads of both KV heads
+constexpr int kBlocksPerTile = 16;
+constexpr int kRows = kBlocksPerTile * 8;     // key rows per tile (MMA M)
+constexpr int kBlockBytes = 4096;             // one block: four 8-row atoms (64-column chunks)
+constexpr int kHalfBytes = 8 * kBlockBytes;   // 8 blocks: one pipeline's part of a K or V tile
+constexpr int kPairBytes = 2 * kHalfBytes;    // a K or V tile: both pipelines' halves
+constexpr int kUnitsPerTile = 2;              // K, V
+constexpr int kPairs = 3;                     // pair slots: K(n), V(n), K(n + 1) in flight
+constexpr int kPipes = 2;
+constexpr int kProducers = 4;                 // producer warps, two per pipeline
+constexpr int kBlocksPerProducer = kBlocksPerTile / kProducers;   // 4
+constexpr int kTabBufs = 4;                   // row tables in flight (the producer runs <= 2 ahead)
+constexpr int kMmaWarp = 8;
 constexpr int kThreads = 288;
+constexpr int kTmemCols = 128;                // S^T buffers at 0 and 96, O^T halves at 32, 64
+__device__ __forceinline__ uint32_t s_col(int n) { return (n & 1) ? 96u : 0u; }
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int kDeadLoaded = -1;               // row outside the selection, loaded from memory
+constexpr int kDeadZero = -2;                 // row the copy fills with zeros (out of range)
 
 struct QsaCtrl {
-  uint64_t full[kRing];
-  uint64_t empty[kRing];
-  uint64_t q_full, s_full, p_full, o_full;
+  uint64_t full[kPipes][kPairs];
+  uint64_t empty[kPipes][kPairs];
+  uint64_t tab_full[kTabBufs];
+  uint64_t s_full[2];                         // S^T of tiles n with n % 2 = index
+  uint64_t q_full, p_full, pv_done, o_full;
   uint32_t tmem_base;
   int abort_flag;
-  int tok_tab[kSlots];
-  float red[2][4][kN];
+  int tab[kTabBufs][kRows];
+  float4 red[2][4][kN / 4];                   // per-warp column maxima, double-buffered
   float lred[4][kN];
 };
 
-constexpr int kQBytes = 4 * kN * 128;          // 4 chunks of [16 rows][128 B]
-constexpr int kPBytes = 2 * kN * 128;          // 2 halves of [16 rows][128 B]
-constexpr int kSmemBytes = kRing * kStageBytes + kQBytes + kPBytes + sizeof(QsaCtrl) + 1024;
+constexpr int kQBytes = 4 * kN * 128;         // 4 d-chunks of [32 rows][128 B]
+constexpr int kPBytes = 2 * kN * 128;         // 2 key-row halves of [32 rows][128 B]
+constexpr int kSmemBytes = kPairs * kPairBytes + kQBytes + kPBytes + sizeof(QsaCtrl) + 1024;
+static_assert(kSmemBytes <= 232448, "qsa_kernel exceeds the per-CTA shared memory limit");
 
 struct QsaLaunch {
-  const __nv_bfloat16* q;
-  const __nv_bfloat16* k;
-  const __nv_bfloat16* v;
   __nv_bfloat16* out;
   float* out32;
   float* lse;
@@ -63,7 +94,7 @@ struct QsaLaunch {
   const int* lo;
   const int* hi;
   uint32_t* status;
-  int T, Hq, Hkv, G;
+  int T, Hq, Hkv, G, pairs;
   float scale_log2;
 };
 
@@ -73,39 +104,133 @@ __device__ __forceinline__ int f2ord(float f) {
 }
 __device__ __forceinline__ float ord2f(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7fffffff); }
 
-__global__ void __launch_bounds__(kThreads, 2) qsa_kernel(QsaLaunch a) {
+// Position of K(n) and V(n) in the copy order K(0), K(1), V(0), K(2), V(1), ..., V(N - 1).
+__device__ __forceinline__ int unit_k(int n) { return n == 0 ? 0 : 2 * n - 1; }
+__device__ __forceinline__ int unit_v(int n, int N) { return n == N - 1 ? 2 * N - 1 : 2 * n + 2; }
+
+// Wait for copies still in flight before the CTA exits after an abort (bounded; ignores the
+// abort flag, which is already set).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_test(bar, parity) && clock64() - t0 < kWaitCycles) {
+  }
+}
+
+// Row r of V of tile n (unit u of the pair sequence) is zeroed once its copy has landed: P is
+// 0 there, but 0 x (inf or NaN) would not be.
+__device__ __noinline__ bool zero_dead_v_row(QsaCtrl* ctl, uint8_t* ring, int u, int r,
+                                             uint32_t* status, volatile int* abort_flag) {
+  const int j = r >> 3, ps = u % kPairs;
+  if (!mbar_wait(&ctl->full[j >> 3][ps], (u / kPairs) & 1, status, abort_flag)) return false;
+  for (int c = 0; c < 4; ++c) {
+    uint4* row = reinterpret_cast<uint4*>(ring + ps * kPairBytes + j * kBlockBytes + c * 1024 +
+                                          (r & 7) * 128);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) row[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  return true;
+}
+
+// O^T columns c *= alpha of column c (held by lane c), both d halves of this warp's lanes.
+__device__ __noinline__ void rescale_o(uint32_t taddr, float alpha_c) {
+  for (int hh = 0; hh < 2; ++hh) {
+    uint32_t ov[kN];
+    tmem_ld32(taddr + 32 * hh, ov);
+    tmem_ld_wait();
+#pragma unroll
+    for (int c = 0; c < kN; ++c)
+      ov[c] = __float_as_uint(__uint_as_float(ov[c]) * __shfl_sync(0xffffffffu, alpha_c, c));
+    tmem_st32(taddr + 32 * hh, ov);
+  }
+  tmem_st_wait();
+}
+
+// Normalise and store this thread's d rows (r, r + 128) of every live column; lane c holds
+// the running maximum of column c.
+__device__ __noinline__ void write_output(const QsaLaunch& a, const QsaCtrl* ctl, uint32_t taddr,
+                                          bool have_o, int t, int g0, bool two, int r, int lane,
+                                          float m_c) {
+  const float L_c = ctl->lred[0][lane] + ctl->lred[1][lane] + ctl->lred[2][lane] +
+                    ctl->lred[3][lane];
+  const float inv_c = L_c > 0.f ? 1.f / L_c : 0.f;
+  if (have_o) tc_fence_after();
+  const long long row0 = static_cast<long long>(t) * a.Hq * kD + r;
+#pragma unroll 1
+  for (int c0 = 0; c0 < kN; c0 += 4) {
+    uint32_t o0[4] = {0u, 0u, 0u, 0u}, o1[4] = {0u, 0u, 0u, 0u};
+    if (have_o) {
+      tmem_ld4(taddr + c0, o0);
+      tmem_ld4(taddr + 32 + c0, o1);
+      tmem_ld_wait();
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = c0 + e;
+      const float inv = __shfl_sync(0xffffffffu, inv_c, c);
+      const int gq = c / kGroupCols, h = c % kGroupCols;
+      if (h >= a.G || (gq == 1 && !two)) continue;
+      const float v0 = __uint_as_float(o0[e]) * inv;
+      const float v1 = __uint_as_float(o1[e]) * inv;
+      const long long o = row0 + static_cast<long long>((g0 + gq) * a.G + h) * kD;
+      a.out[o] = __float2bfloat16_rn(v0);
+      a.out[o + 128] = __float2bfloat16_rn(v1);
+      if (a.out32) {
+        a.out32[o] = v0;
+        a.out32[o + 128] = v1;
+      }
+    }
+  }
+  // lse of column c from lane c of the first warp
+  const int gq = lane / kGroupCols, h = lane % kGroupCols;
+  if (r == lane && a.lse && h < a.G && (gq == 0 || two))
+    a.lse[static_cast<long long>((g0 + gq) * a.G + h) * a.T + t] =
+        L_c > 0.f ? (m_c + fast_log2(L_c)) * kLn2 : -INFINITY;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+           const __grid_constant__ CUtensorMap vmap, QsaLaunch a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* base = smem_align<1024>(smem_raw);
   uint8_t* ring = base;
-  uint8_t* q_s = ring + kRing * kStageBytes;
+  uint8_t* q_s = ring + kPairs * kPairBytes;
   uint8_t* p_s = q_s + kQBytes;
   QsaCtrl* ctl = reinterpret_cast<QsaCtrl*>(p_s + kPBytes);
 
   if (launch_aborted(a.status)) return;
-  const int t = blockIdx.x / a.Hkv, g = blockIdx.x % a.Hkv;
+  const int t = blockIdx.x / a.pairs, g0 = 2 * (blockIdx.x % a.pairs);
+  const bool two = g0 + 1 < a.Hkv;
   const int G = a.G;
   const int beg = __ldg(a.indptr + t);
   const int nblk = __ldg(a.indptr + t + 1) - beg;
-  const int N = nblk > 0 ? (nblk + 31) / 32 : 0;     // tiles
-  const int S = 4 * N;                                // stages
+  const int N = nblk > 0 ? (nblk + kBlocksPerTile - 1) / kBlocksPerTile : 0;   // tiles
+  const int S = kUnitsPerTile * N;                                              // units
   const int lo = __ldg(a.lo + t), hi = __ldg(a.hi + t);
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Q rows G..15 of each group and all of P^T start at zero: the copies never write the
+  // former, and softmax writes only its own group's half of the latter.
+  for (int i = threadIdx.x; i < (kQBytes + kPBytes) / 16; i += kThreads)
+    *reinterpret_cast<uint4*>(q_s + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kRing; ++i) {
-      mbar_init(&ctl->full[i], 128);
-      mbar_init(&ctl->empty[i], 1);
-    }
-    mbar_init(&ctl->q_full, 128);
-    mbar_init(&ctl->s_full, 1);
+    for (int p = 0; p < kPipes; ++p)
+      for (int i = 0; i < kPairs; ++i) {
+        mbar_init(&ctl->full[p][i], kProducers / kPipes);
+        mbar_init(&ctl->empty[p][i], 1);
+      }
+    for (int i = 0; i < kTabBufs; ++i) mbar_init(&ctl->tab_full[i], 32 * kProducers);
+    mbar_init(&ctl->q_full, 1);
+    mbar_init(&ctl->s_full[0], 1);
+    mbar_init(&ctl->s_full[1], 1);
+    mbar_init(&ctl->pv_done, 1);
     mbar_init(&ctl->p_full, 128);
     mbar_init(&ctl->o_full, 1);
     ctl->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
-    tmem_alloc(&ctl->tmem_base, 64);
+  fence_proxy_async_smem();   // the zeroes (generic proxy) before the copies (async proxy)
+  if (warp == kMmaWarp) {
+    tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -114,218 +239,234 @@ __global__ void __launch_bounds__(kThreads, 2) qsa_kernel(QsaLaunch a) {
   const uint32_t tmem = ctl->tmem_base;
   volatile int* abort_flag = &ctl->abort_flag;
 
-  if (warp < 4) {
+  if (warp < kProducers) {
     // ================================ producers ===========================================
-    const int p = threadIdx.x;                         // 0..127
-    const uint32_t q_addr = smem_u32(q_s);
-    for (int i = 0; i < 4; ++i) {                      // Q: 16 rows x 32 chunks of 16 B
-      const int c = p + 128 * i, r = c >> 5, cc = c & 31;
-      const int head = g * G + (r < G ? r : G - 1);
-      const __nv_bfloat16* src = a.q + (static_cast<long long>(t) * a.Hq + head) * kD + cc * 8;
-      cp_async16(q_addr + (cc >> 3) * (kN * 128) + r * 128 + (((cc & 7) ^ (r & 7)) << 4), src,
-                 r < G ? 16u : 0u);
+    const int pw = warp;
+    if (N > 0 && pw == 0) {
+      if (lane == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+        mbar_arrive_expect_tx(&ctl->q_full, (two ? 8u : 4u) * static_cast<uint32_t>(G) * 128u);
+      }
+      __syncwarp();
+      if (lane < (two ? 8 : 4)) {                      // Q: d chunk lane & 3, group lane >> 2
+        const int c = lane & 3, gg = lane >> 2;
+        tma_load_3d(q_s + c * (kN * 128) + gg * (kGroupCols * 128), &qmap, &ctl->q_full, c * 64,
+                    (g0 + gg) * G, t);
+      }
     }
-    cp_async_arrive_noinc(&ctl->q_full);
-    const uint32_t ring_addr = smem_u32(ring);
-    bool ok = true;
-    for (int s = 0; s < S && ok; ++s) {
-      const int n = s >> 2, part = s & 3, slot = s % kRing;
-      if (part == 0) {                                 // key tokens of tile n
-        named_bar(2, 128);
-        const int i = n * 32 + (p >> 2);
-        int tok = -1;
-        if (i < nblk) {
-          const int b = __ldg(a.indices + beg + i);
-          const int tk = __ldg(a.bfirst + b) + (p & 3);
-          if (tk <= __ldg(a.blast + b) && tk >= lo && tk <= hi) tok = tk;
+    // lane l < 4 of producer warp pw (pipeline pl = pw / 2) handles block 4 pw + l of each tile
+    const int pl = pw / 2;
+    const int jb = kBlocksPerProducer * pw + lane;
+    auto block_of = [&](int n) -> int {
+      const int i = n * kBlocksPerTile + jb;
+      return (lane < kBlocksPerProducer && n < N && i < nblk) ? __ldg(a.indices + beg + i) : -1;
+    };
+    // block spans are fetched two tiles ahead of their publication: block ids of tile n + 2 and
+    // first/last tokens of tile n + 1 are in flight while tile n is published
+    int b_cur = block_of(0), first_cur = 0, last_cur = -1;
+    if (b_cur >= 0) {
+      first_cur = __ldg(a.bfirst + b_cur);
+      last_cur = __ldg(a.blast + b_cur);
+    }
+    int b_nx = block_of(1);
+    int first_t[2] = {a.T, a.T};   // token coordinate of this lane's block in tiles of parity 0/1
+    int issued = 0;
+    for (int s = 0; s < S; ++s) {
+      // unit s: K(n) or V(n) in the consumption order
+      const bool is_k = s == 0 || (s & 1 && s != S - 1);
+      const int n = s == 0 ? 0 : (is_k ? (s + 1) >> 1 : (s == S - 1 ? N - 1 : (s - 2) >> 1));
+      const int ps = s % kPairs;
+      if (is_k) {                                      // publish tile n's rows
+        const int f = b_cur >= 0 ? first_cur : a.T;
+        if (n & 1) first_t[1] = f; else first_t[0] = f;
+        if (lane < kBlocksPerProducer) {
+          int* tab = ctl->tab[n % kTabBufs] + jb * 8;
+#pragma unroll
+          for (int o = 0; o < 4; ++o) {
+            const int tok = first_cur + o;
+#pragma unroll
+            for (int gg = 0; gg < 2; ++gg) {
+              int code;
+              if (b_cur < 0 || tok >= a.T || (gg == 1 && !two)) code = kDeadZero;
+              else if (tok <= last_cur && tok >= lo && tok <= hi) code = tok;
+              else code = kDeadLoaded;
+              tab[o * 2 + gg] = code;                  // row = token offset * 2 + head
+            }
+          }
         }
-        ctl->tok_tab[p] = tok;
-        named_bar(2, 128);
+        mbar_arrive(&ctl->tab_full[n % kTabBufs]);
+        // advance the prefetch: spans of tile n + 1 (ids fetched a tile ago), ids of n + 2
+        b_cur = b_nx;
+        if (b_cur >= 0) {
+          first_cur = __ldg(a.bfirst + b_cur);
+          last_cur = __ldg(a.blast + b_cur);
+        }
+        b_nx = block_of(n + 2);
       }
-      if (s >= kRing && !mbar_wait(&ctl->empty[slot], ((s / kRing) - 1) & 1, a.status, abort_flag)) {
-        ok = false;
+      if (s >= kPairs &&
+          !mbar_wait_warp(&ctl->empty[pl][ps], ((s / kPairs) - 1) & 1, a.status, abort_flag))
         break;
-      }
-      const __nv_bfloat16* src_base = part < 2 ? a.k : a.v;
-      const int col0 = (part & 1) * 128;
-      const uint32_t stage = ring_addr + slot * kStageBytes;
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int c = p + 128 * i, row = c >> 4, cc = c & 15;
-        const int tok = ctl->tok_tab[row];
-        const __nv_bfloat16* src =
-            src_base + (static_cast<long long>(tok >= 0 ? tok : 0) * a.Hkv + g) * kD + col0 + cc * 8;
-        cp_async16(stage + (cc >> 3) * 16384 + row * 128 + (((cc & 7) ^ (row & 7)) << 4), src,
-                   tok >= 0 ? 16u : 0u);
-      }
-      // the stage's barrier completes when this thread's copies (and the other 127's) land
-      cp_async_arrive_noinc(&ctl->full[slot]);
+      if (lane == 0) mbar_arrive_expect_tx(&ctl->full[pl][ps], kBlocksPerProducer * kBlockBytes);
+      __syncwarp();
+      if (lane < kBlocksPerProducer)
+        tma_load_4d(ring + ps * kPairBytes + jb * kBlockBytes, is_k ? &kmap : &vmap,
+                    &ctl->full[pl][ps], 0, g0, (n & 1) ? first_t[1] : first_t[0], 0);
+      issued = s + 1;
     }
-    cp_async_wait<0>();
-  } else if (warp == 4) {
+    if (*abort_flag && lane == 0) {                    // copies still in flight after an abort
+      for (int s = issued > kPairs ? issued - kPairs : 0; s < issued; ++s)
+        drain_wait(&ctl->full[pl][s % kPairs], (s / kPairs) & 1);
+      if (N > 0 && pw == 0) drain_wait(&ctl->q_full, 0);
+    }
+  } else if (warp == kMmaWarp) {
     // ================================ MMA issuer ==========================================
     if (lane == 0 && N > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(128, kN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(128, kN, true, false);
       const uint32_t ring_addr = smem_u32(ring), q_addr = smem_u32(q_s), p_addr = smem_u32(p_s);
-      bool ok = mbar_wait(&ctl->q_full, 0, a.status, abort_flag);
-      fence_proxy_async_smem();   // cp.async (generic proxy) writes -> tensor-core reads
-      for (int n = 0; ok && n < N; ++n) {
-        const int s0 = 4 * n;
-        if (!mbar_wait(&ctl->full[s0 % kRing], (s0 / kRing) & 1, a.status, abort_flag) ||
-            !mbar_wait(&ctl->full[(s0 + 1) % kRing], ((s0 + 1) / kRing) & 1, a.status, abort_flag))
-          break;
-        fence_proxy_async_smem();
+      // S^T of tile n + 1 is computed while softmax works on tile n (two S^T buffers), so
+      // softmax runs tile after tile without waiting for an MMA round trip.
+      auto issue_qk = [&](int n) -> bool {
+        const int u = unit_k(n), sk = u % kPairs;
+        if (!mbar_wait(&ctl->full[0][sk], (u / kPairs) & 1, a.status, abort_flag) ||
+            !mbar_wait(&ctl->full[1][sk], (u / kPairs) & 1, a.status, abort_flag))
+          return false;
         tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 16; ++ks) {
-          const int st = (s0 + (ks >> 3)) % kRing, kk = ks & 7;
-          const uint32_t ka = ring_addr + st * kStageBytes + (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint32_t qa = q_addr + (ks >> 2) * (kN * 128) + (ks & 3) * 32;
-          mma_ss(tmem, sdesc_sw128(ka, 16, 1024), sdesc_sw128(qa, 16, 1024), idesc_qk, ks > 0);
+        for (int k = 0; k < 16; ++k) {                 // chunk k / 4, 16 columns (k % 4)
+          const uint32_t ka = ring_addr + sk * kPairBytes + (k >> 2) * 1024 + (k & 3) * 32;
+          const uint32_t qa = q_addr + (k >> 2) * (kN * 128) + (k & 3) * 32;
+          mma_ss(tmem + s_col(n), sdesc_sw128(ka, 16, kBlockBytes), sdesc_sw128(qa, 16, 1024),
+                 idesc_qk, k > 0);
         }
-        mma_commit(&ctl->s_full);
-        mma_commit(&ctl->empty[s0 % kRing]);
-        mma_commit(&ctl->empty[(s0 + 1) % kRing]);
+        mma_commit(&ctl->empty[0][sk]);
+        mma_commit(&ctl->empty[1][sk]);
+        mma_commit(&ctl->s_full[n & 1]);
+        return true;
+      };
+      bool ok = mbar_wait(&ctl->q_full, 0, a.status, abort_flag) && issue_qk(0);
+      for (int n = 0; ok && n < N; ++n) {
+        // S^T(n + 1) may reuse buffer (n + 1) % 2: softmax(n - 1) finished with it before
+        // PV(n - 1) was issued
+        if (n + 1 < N && !issue_qk(n + 1)) break;
+        // O^T[d half h] += V^T P^T over both V units (blocks 0-7, 8-15)
+        const int u = unit_v(n, N), sv = u % kPairs;
         if (!mbar_wait(&ctl->p_full, n & 1, a.status, abort_flag) ||
-            !mbar_wait(&ctl->full[(s0 + 2) % kRing], ((s0 + 2) / kRing) & 1, a.status, abort_flag) ||
-            !mbar_wait(&ctl->full[(s0 + 3) % kRing], ((s0 + 3) / kRing) & 1, a.status, abort_flag))
+            !mbar_wait(&ctl->full[0][sv], (u / kPairs) & 1, a.status, abort_flag) ||
+            !mbar_wait(&ctl->full[1][sv], (u / kPairs) & 1, a.status, abort_flag))
           break;
-        fence_proxy_async_smem();
         tc_fence_after();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int st = (s0 + 2 + h) % kRing;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t va = ring_addr + st * kStageBytes + ks * 2048;
+          for (int ks = 0; ks < 8; ++ks) {             // 16 key rows = 2 blocks per step
+            const uint32_t va = ring_addr + sv * kPairBytes + h * 2048 + ks * 2 * kBlockBytes;
             const uint32_t pa = p_addr + (ks >> 2) * (kN * 128) + (ks & 3) * 32;
-            mma_ss(tmem + 16 + 16 * h, sdesc_sw128(va, 16384, 1024), sdesc_sw128(pa, 16, 1024),
-                   idesc_pv, (n > 0 || ks > 0));
+            mma_ss(tmem + 32 + 32 * h, sdesc_sw128(va, 1024, kBlockBytes),
+                   sdesc_sw128(pa, 16, 1024), idesc_pv, (n > 0 || ks > 0));
           }
         }
-        mma_commit(&ctl->empty[(s0 + 2) % kRing]);
-        mma_commit(&ctl->empty[(s0 + 3) % kRing]);
+        mma_commit(&ctl->empty[0][sv]);
+        mma_commit(&ctl->empty[1][sv]);
+        mma_commit(&ctl->pv_done);
         if (n == N - 1) mma_commit(&ctl->o_full);
       }
     }
-  } else {
+  } else if (warp >= 4) {
     // ================================ softmax =============================================
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;                      // key slot of S^T, d row of O^T
+    const int wq = warp & 3;                           // TMEM lane quadrant of this warp
+    const int r = wq * 32 + lane;                      // key row of S^T, d row of O^T
+    const int gg = lane & 1;                           // KV head of row r within the pair
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = a.scale_log2;
-    float m[kN], l[kN];
+    const int ord_ninf = f2ord(-INFINITY);
+    // Column bookkeeping is spread over the lanes: lane c of every warp keeps the running
+    // maximum of S^T column c (query head c % 16 of KV head g0 + c / 16); each warp holds
+    // an identical copy.  Rows read their 16 columns' values by shuffles, so the per-tile
+    // code stays short.
+    float m_c = -INFINITY;
+    float l[kGroupCols];
 #pragma unroll
-    for (int h = 0; h < kN; ++h) {
-      m[h] = -INFINITY;
-      l[h] = 0.f;
-    }
+    for (int h = 0; h < kGroupCols; ++h) l[h] = 0.f;
     for (int n = 0; n < N; ++n) {
-      if (!mbar_wait_warp(&ctl->s_full, n & 1, a.status, abort_flag)) break;
+      if (!mbar_wait_warp(&ctl->s_full[n & 1], (n >> 1) & 1, a.status, abort_flag)) break;
       tc_fence_after();
-      uint32_t sv[16];
-      tmem_ld16(tmem + lane_base, sv);
+      uint32_t sv[kN];
+      tmem_ld32(tmem + lane_base + s_col(n), sv);
       tmem_ld_wait();
-      const int i = n * 32 + (r >> 2);
-      bool valid = false;
-      if (i < nblk) {
-        const int b = __ldg(a.indices + beg + i);
-        const int tk = __ldg(a.bfirst + b) + (r & 3);
-        valid = tk <= __ldg(a.blast + b) && tk >= lo && tk <= hi;
-      }
-      float x[kN];
+      if (!mbar_wait_warp(&ctl->tab_full[n % kTabBufs], (n / kTabBufs) & 1, a.status, abort_flag))
+        break;
+      const int code = ctl->tab[n % kTabBufs][r];
+      const bool valid = code >= 0;
+      float x[kGroupCols];
 #pragma unroll
-      for (int h = 0; h < kN; ++h)
-        x[h] = (valid && h < G) ? __uint_as_float(sv[h]) * sl2 : -INFINITY;
-      float (*red)[kN] = ctl->red[n & 1];
+      for (int h = 0; h < kGroupCols; ++h)
+        x[h] = (valid && h < G) ? __uint_as_float(gg ? sv[kGroupCols + h] : sv[h]) * sl2 : -INFINITY;
+      float* red = reinterpret_cast<float*>(ctl->red[n & 1][wq]);
 #pragma unroll
-      for (int h = 0; h < kN; ++h) {
-        const int wm = __reduce_max_sync(0xffffffffu, f2ord(x[h]));
-        if (lane == 0) red[wq][h] = ord2f(wm);
+      for (int h = 0; h < kGroupCols; ++h) {
+        const int v = f2ord(x[h]);
+        const int m0 = __reduce_max_sync(0xffffffffu, gg == 0 ? v : ord_ninf);
+        const int m1 = __reduce_max_sync(0xffffffffu, gg == 1 ? v : ord_ninf);
+        if (lane == 0) {
+          red[h] = ord2f(m0);
+          red[kGroupCols + h] = ord2f(m1);
+        }
       }
       named_bar(1, 128);
-      bool need = false;
-      float alpha[kN], mu[kN];
-#pragma unroll
-      for (int h = 0; h < kN; ++h) {
-        const float M = fmaxf(fmaxf(red[0][h], red[1][h]), fmaxf(red[2][h], red[3][h]));
-        alpha[h] = 1.f;
-        if (M > m[h] + kRescaleThreshold || (m[h] == -INFINITY && M > -INFINITY)) {
-          alpha[h] = m[h] == -INFINITY ? 0.f : fast_exp2(m[h] - M);
-          m[h] = M;
-          need = true;
-        }
-        mu[h] = m[h] == -INFINITY ? 0.f : m[h];
+      const float* rd = reinterpret_cast<const float*>(ctl->red[n & 1]);
+      const float M = fmaxf(fmaxf(rd[lane], rd[kN + lane]), fmaxf(rd[2 * kN + lane], rd[3 * kN + lane]));
+      float alpha_c = 1.f;
+      if (M > m_c + kRescaleThreshold || (m_c == -INFINITY && M > -INFINITY)) {
+        alpha_c = m_c == -INFINITY ? 0.f : fast_exp2(m_c - M);
+        m_c = M;
       }
-      // P^T [16 heads][128 keys], K-major with the 128-byte swizzle (two 64-key halves)
+      const bool need = __any_sync(0xffffffffu, alpha_c != 1.f);
+      const float mu_c = m_c == -INFINITY ? 0.f : m_c;
+      // P^T and O^T are read by PV(n - 1): it must have completed before either changes
+      if (n > 0 && !mbar_wait_warp(&ctl->pv_done, (n - 1) & 1, a.status, abort_flag)) break;
+      tc_fence_after();
+      // P^T [32 columns][128 rows], two K-major 64-row chunks with the 128-byte swizzle; this
+      // thread writes its own group's 16 columns, the other group's stay zero
       uint8_t* prow = p_s + (r >> 6) * (kN * 128);
       const int rr = r & 63;
 #pragma unroll
-      for (int h = 0; h < kN; ++h) {
-        const float pv = fast_exp2(x[h] - mu[h]);
-        l[h] = l[h] * alpha[h] + pv;
-        *reinterpret_cast<__nv_bfloat16*>(prow + h * 128 + ((((rr >> 3) ^ (h & 7)) & 7) << 4) +
+      for (int h = 0; h < kGroupCols; ++h) {
+        const int c = gg * kGroupCols + h;
+        const float mu = __shfl_sync(0xffffffffu, mu_c, c);
+        const float ac = __shfl_sync(0xffffffffu, alpha_c, c);
+        const float pv = fast_exp2(x[h] - mu);
+        l[h] = l[h] * ac + pv;
+        *reinterpret_cast<__nv_bfloat16*>(prow + c * 128 + ((((rr >> 3) ^ (c & 7)) & 7) << 4) +
                                           (rr & 7) * 2) = __float2bfloat16_rn(pv);
       }
-      if (n > 0 && need) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t ov[16];
-          tmem_ld16(tmem + lane_base + 16 + 16 * hh, ov);
-          tmem_ld_wait();
-#pragma unroll
-          for (int h = 0; h < kN; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
-          tmem_st16(tmem + lane_base + 16 + 16 * hh, ov);
-        }
-        tmem_st_wait();
-      }
-      fence_proxy_async_smem();
+      if (code == kDeadLoaded &&
+          !zero_dead_v_row(ctl, ring, unit_v(n, N), r, a.status, abort_flag))
+        n = N;                                         // aborted: leave after this arrival
+      if (n > 0 && need) rescale_o(tmem + lane_base + 32, alpha_c);
+      fence_proxy_async_smem();   // P^T and zeroed V rows (generic) -> tensor-core reads
       tc_fence_before();
       mbar_arrive(&ctl->p_full);
     }
     // ---- epilogue: column sums, normalise, write out / out_fp32 / lse ---------------------
 #pragma unroll
-    for (int h = 0; h < kN; ++h) {
+    for (int h = 0; h < kGroupCols; ++h) {
       float v = l[h];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) ctl->lred[wq][h] = v;
+      for (int o = 2; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);   // same group
+      if (lane < 2) ctl->lred[wq][lane * kGroupCols + h] = v;
     }
     named_bar(1, 128);
     const bool have_o = N > 0 && mbar_wait_warp(&ctl->o_full, 0, a.status, abort_flag);
-    uint32_t olo[16], ohi[16];
-    if (have_o) {
-      tc_fence_after();
-      tmem_ld16(tmem + lane_base + 16, olo);
-      tmem_ld16(tmem + lane_base + 32, ohi);
-      tmem_ld_wait();
-    }
-#pragma unroll
-    for (int h = 0; h < kN; ++h) {
-      if (h >= G) break;
-      const float L = ctl->lred[0][h] + ctl->lred[1][h] + ctl->lred[2][h] + ctl->lred[3][h];
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      const float v0 = have_o ? __uint_as_float(olo[h]) * inv : 0.f;
-      const float v1 = have_o ? __uint_as_float(ohi[h]) * inv : 0.f;
-      const long long o = (static_cast<long long>(t) * a.Hq + g * G + h) * kD;
-      a.out[o + r] = __float2bfloat16_rn(v0);
-      a.out[o + 128 + r] = __float2bfloat16_rn(v1);
-      if (a.out32) {
-        a.out32[o + r] = v0;
-        a.out32[o + 128 + r] = v1;
-      }
-      if (r == 0 && a.lse)
-        a.lse[static_cast<long long>(g * G + h) * a.T + t] =
-            L > 0.f ? (m[h] + fast_log2(L)) * kLn2 : -INFINITY;
-    }
+    write_output(a, ctl, tmem + lane_base + 32, have_o, t, g0, two, r, lane, m_c);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 64);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -335,15 +476,23 @@ int launch_qsa(const paged_attn_params* p, const paged_attn_meta* m, const void*
                const void* v, void* out, float* out_fp32, float* lse, const int* indptr,
                const int* indices, uint32_t* status, cudaStream_t st) {
   const int G = p->num_qo_heads / p->num_kv_heads;
-  if (G > kN || p->head_dim != kD) return PAGED_ATTN_ERR_UNSUPPORTED;
+  if (G > kGroupCols || p->head_dim != kD) return PAGED_ATTN_ERR_UNSUPPORTED;
   if (!out || !m->lo_dev || !m->hi_dev || !m->block_first_dev || !m->block_last_dev)
     return PAGED_ATTN_ERR_INVALID_ARGUMENT;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
        reinterpret_cast<uintptr_t>(v)) & 15u)
     return PAGED_ATTN_ERR_INVALID_ARGUMENT;
-  const long long units = static_cast<long long>(p->q_len) * p->num_kv_heads;
+  const int pairs = (p->num_kv_heads + 1) / 2;
+  const long long units = static_cast<long long>(p->q_len) * pairs;
   if (units == 0) return PAGED_ATTN_OK;
   if (units >= (1LL << 31)) return PAGED_ATTN_ERR_UNSUPPORTED;
+  CUtensorMap qmap, kmap, vmap;
+  // Q [T, Hq, D]: box = the G query heads of one KV head, 64 columns; K and V [T, Hkv, D]:
+  // box = 4 tokens x 2 KV heads x two 64-column chunks (two swizzle atoms)
+  if (!encode_q_map(&qmap, q, p->q_len, p->num_qo_heads, kD, G, 1) ||
+      !encode_block_pair_map(&kmap, k, p->q_len, p->num_kv_heads, kD) ||
+      !encode_block_pair_map(&vmap, v, p->q_len, p->num_kv_heads, kD))
+    return PAGED_ATTN_ERR_CUDA;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(qsa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -352,9 +501,6 @@ int launch_qsa(const paged_attn_params* p, const paged_attn_meta* m, const void*
     attr_set = true;
   }
   QsaLaunch a{};
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.k = static_cast<const __nv_bfloat16*>(k);
-  a.v = static_cast<const __nv_bfloat16*>(v);
   a.out = static_cast<__nv_bfloat16*>(out);
   a.out32 = out_fp32;
   a.lse = lse;
@@ -369,10 +515,11 @@ int launch_qsa(const paged_attn_params* p, const paged_attn_meta* m, const void*
   a.Hq = p->num_qo_heads;
   a.Hkv = p->num_kv_heads;
   a.G = G;
+  a.pairs = pairs;
   a.scale_log2 = p->sm_scale * 1.4426950408889634f;
   void* tok;
   timer_begin(st, &tok);
-  qsa_kernel<<<static_cast<unsigned>(units), kThreads, kSmemBytes, st>>>(a);
+  qsa_kernel<<<static_cast<unsigned>(units), kThreads, kSmemBytes, st>>>(qmap, kmap, vmap, a);
   timer_end(st, tok);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? PAGED_ATTN_OK : PAGED_ATTN_ERR_CUDA;

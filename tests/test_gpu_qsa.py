@@ -56,6 +56,7 @@ CASES = [
     ([100, 60], 16, 1, 3, 5, True),
     ([48, 8], 2, 2, 2, 100, True),
     ([520], 24, 2, 16, 256, False),
+    ([96, 40], 6, 3, 4, 10, False),    # odd Hkv > 1: the last head has no partner
 ]
 
 
@@ -69,6 +70,26 @@ def test_qsa_matches_oracle(case):
         p["lo"] = p["lo"] + torch.tensor([(t * 7) % 5 for t in range(T)], dtype=torch.int32)
     out, out32, lse, ws, params = _run(p)
     o_ref, l_ref = _oracle(p)
+    check_out(out, o_ref)
+    check_out(out32, o_ref)
+    check_lse(lse, l_ref)
+    _check_plan(p, ws, params)
+
+
+def test_qsa_unselected_nonfinite_tokens_do_not_leak():
+    # 3-token blocks: the 4th token of every 4-token span belongs to no block, so no query
+    # may see it.  It is NaN in K and V; a kernel that loads whole spans must mask it out of
+    # both S and the V accumulation.
+    p = W.make_qsa_problem(420, [64, 36], Hq=8, Hkv=2, D=256, block_size=4, n_near=3,
+                           n_random=6, scale=1.0 / 16)
+    p["block_last"] = p["block_first"] + 2
+    T = p["q"].shape[0]
+    unused = torch.arange(3, T, 4)
+    p["k"][unused] = float("nan")
+    p["v"][unused] = float("nan")
+    out, out32, lse, ws, params = _run(p)
+    o_ref, l_ref = _oracle(p)
+    assert np.isfinite(o_ref).all()
     check_out(out, o_ref)
     check_out(out32, o_ref)
     check_lse(lse, l_ref)
