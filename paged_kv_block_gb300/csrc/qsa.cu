@@ -62,25 +62,31 @@ constexpr int kTmemCols = 128;                // S^T buffers at 0 and 96, O^T ha
 __device__ __forceinline__ uint32_t s_col(int n) { return (n & 1) ? 96u : 0u; }
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;
-constexpr int kDeadLoaded = -1;               // row outside the selection, loaded from memory
-constexpr int kDeadZero = -2;                 // row the copy fills with zeros (out of range)
+// key-row codes of the per-tile table
+constexpr int8_t kLive = 1;                   // a selected token inside [lo, hi]
+constexpr int8_t kDeadLoaded = -1;            // row outside the selection, loaded from memory
+constexpr int8_t kDeadZero = 0;               // row the copy fills with zeros (out of range)
 
 struct QsaCtrl {
   uint64_t full[kPipes][kPairs];
   uint64_t empty[kPipes][kPairs];
   uint64_t tab_full[kTabBufs];
   uint64_t s_full[2];                         // S^T of tiles n with n % 2 = index
-  uint64_t q_full, p_full, pv_done, o_full;
+  uint64_t p_full[2];                         // P^T of tiles n with n % 2 = index written
+  uint64_t pv_done[2];                        // PV of tiles n with n % 2 = index complete
+  uint64_t q_full, o_full;
   uint32_t tmem_base;
   int abort_flag;
-  int tab[kTabBufs][kRows];
-  float4 red[2][4][kN / 4];                   // per-warp column maxima, double-buffered
+  int8_t tab[kTabBufs][kRows];
+  float4 red[4][kN / 4];                      // per-warp column maxima
   float lred[4][kN];
 };
 
 constexpr int kQBytes = 4 * kN * 128;         // 4 d-chunks of [32 rows][128 B]
-constexpr int kPBytes = 2 * kN * 128;         // 2 key-row halves of [32 rows][128 B]
-constexpr int kSmemBytes = kPairs * kPairBytes + kQBytes + kPBytes + sizeof(QsaCtrl) + 1024;
+constexpr int kPBytes = 2 * kN * 128;         // one P^T: 2 key-row halves of [32 rows][128 B]
+constexpr int kPBufs = 2;
+constexpr int kSmemBytes =
+    kPairs * kPairBytes + kQBytes + kPBufs * kPBytes + sizeof(QsaCtrl) + 1024;
 static_assert(kSmemBytes <= 232448, "qsa_kernel exceeds the per-CTA shared memory limit");
 
 struct QsaLaunch {
@@ -195,7 +201,7 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
   uint8_t* ring = base;
   uint8_t* q_s = ring + kPairs * kPairBytes;
   uint8_t* p_s = q_s + kQBytes;
-  QsaCtrl* ctl = reinterpret_cast<QsaCtrl*>(p_s + kPBytes);
+  QsaCtrl* ctl = reinterpret_cast<QsaCtrl*>(p_s + kPBufs * kPBytes);
 
   if (launch_aborted(a.status)) return;
   const int t = blockIdx.x / a.pairs, g0 = 2 * (blockIdx.x % a.pairs);
@@ -210,7 +216,7 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
 
   // Q rows G..15 of each group and all of P^T start at zero: the copies never write the
   // former, and softmax writes only its own group's half of the latter.
-  for (int i = threadIdx.x; i < (kQBytes + kPBytes) / 16; i += kThreads)
+  for (int i = threadIdx.x; i < (kQBytes + kPBufs * kPBytes) / 16; i += kThreads)
     *reinterpret_cast<uint4*>(q_s + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x == 0) {
     for (int p = 0; p < kPipes; ++p)
@@ -222,8 +228,10 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
     mbar_init(&ctl->q_full, 1);
     mbar_init(&ctl->s_full[0], 1);
     mbar_init(&ctl->s_full[1], 1);
-    mbar_init(&ctl->pv_done, 1);
-    mbar_init(&ctl->p_full, 128);
+    mbar_init(&ctl->pv_done[0], 1);
+    mbar_init(&ctl->pv_done[1], 1);
+    mbar_init(&ctl->p_full[0], 128);
+    mbar_init(&ctl->p_full[1], 128);
     mbar_init(&ctl->o_full, 1);
     ctl->abort_flag = 0;
     fence_mbar_init();
@@ -281,15 +289,15 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
         const int f = b_cur >= 0 ? first_cur : a.T;
         if (n & 1) first_t[1] = f; else first_t[0] = f;
         if (lane < kBlocksPerProducer) {
-          int* tab = ctl->tab[n % kTabBufs] + jb * 8;
+          int8_t* tab = ctl->tab[n % kTabBufs] + jb * 8;
 #pragma unroll
           for (int o = 0; o < 4; ++o) {
             const int tok = first_cur + o;
 #pragma unroll
             for (int gg = 0; gg < 2; ++gg) {
-              int code;
+              int8_t code;
               if (b_cur < 0 || tok >= a.T || (gg == 1 && !two)) code = kDeadZero;
-              else if (tok <= last_cur && tok >= lo && tok <= hi) code = tok;
+              else if (tok <= last_cur && tok >= lo && tok <= hi) code = kLive;
               else code = kDeadLoaded;
               tab[o * 2 + gg] = code;                  // row = token offset * 2 + head
             }
@@ -352,7 +360,7 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
         if (n + 1 < N && !issue_qk(n + 1)) break;
         // O^T[d half h] += V^T P^T over both V units (blocks 0-7, 8-15)
         const int u = unit_v(n, N), sv = u % kPairs;
-        if (!mbar_wait(&ctl->p_full, n & 1, a.status, abort_flag) ||
+        if (!mbar_wait(&ctl->p_full[n & 1], (n >> 1) & 1, a.status, abort_flag) ||
             !mbar_wait(&ctl->full[0][sv], (u / kPairs) & 1, a.status, abort_flag) ||
             !mbar_wait(&ctl->full[1][sv], (u / kPairs) & 1, a.status, abort_flag))
           break;
@@ -362,14 +370,14 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {             // 16 key rows = 2 blocks per step
             const uint32_t va = ring_addr + sv * kPairBytes + h * 2048 + ks * 2 * kBlockBytes;
-            const uint32_t pa = p_addr + (ks >> 2) * (kN * 128) + (ks & 3) * 32;
+            const uint32_t pa = p_addr + (n & 1) * kPBytes + (ks >> 2) * (kN * 128) + (ks & 3) * 32;
             mma_ss(tmem + 32 + 32 * h, sdesc_sw128(va, 1024, kBlockBytes),
                    sdesc_sw128(pa, 16, 1024), idesc_pv, (n > 0 || ks > 0));
           }
         }
         mma_commit(&ctl->empty[0][sv]);
         mma_commit(&ctl->empty[1][sv]);
-        mma_commit(&ctl->pv_done);
+        mma_commit(&ctl->pv_done[n & 1]);
         if (n == N - 1) mma_commit(&ctl->o_full);
       }
     }
@@ -398,38 +406,48 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
       if (!mbar_wait_warp(&ctl->tab_full[n % kTabBufs], (n / kTabBufs) & 1, a.status, abort_flag))
         break;
       const int code = ctl->tab[n % kTabBufs][r];
-      const bool valid = code >= 0;
+      const bool valid = code == kLive;
       float x[kGroupCols];
 #pragma unroll
       for (int h = 0; h < kGroupCols; ++h)
         x[h] = (valid && h < G) ? __uint_as_float(gg ? sv[kGroupCols + h] : sv[h]) * sl2 : -INFINITY;
-      float* red = reinterpret_cast<float*>(ctl->red[n & 1][wq]);
+      // The running maxima change only when some score exceeds them by the rescale threshold,
+      // which after the first tile is rare: test for that first and compute the exact
+      // column maxima of the tile only when it happens.
+      bool exceed = false;
 #pragma unroll
-      for (int h = 0; h < kGroupCols; ++h) {
-        const int v = f2ord(x[h]);
-        const int m0 = __reduce_max_sync(0xffffffffu, gg == 0 ? v : ord_ninf);
-        const int m1 = __reduce_max_sync(0xffffffffu, gg == 1 ? v : ord_ninf);
-        if (lane == 0) {
-          red[h] = ord2f(m0);
-          red[kGroupCols + h] = ord2f(m1);
-        }
-      }
-      named_bar(1, 128);
-      const float* rd = reinterpret_cast<const float*>(ctl->red[n & 1]);
-      const float M = fmaxf(fmaxf(rd[lane], rd[kN + lane]), fmaxf(rd[2 * kN + lane], rd[3 * kN + lane]));
+      for (int h = 0; h < kGroupCols; ++h)
+        exceed |= x[h] > __shfl_sync(0xffffffffu, m_c, gg * kGroupCols + h) + kRescaleThreshold;
       float alpha_c = 1.f;
-      if (M > m_c + kRescaleThreshold || (m_c == -INFINITY && M > -INFINITY)) {
-        alpha_c = m_c == -INFINITY ? 0.f : fast_exp2(m_c - M);
-        m_c = M;
+      if (named_bar_or(1, 128, exceed)) {
+        float* red = reinterpret_cast<float*>(ctl->red[wq]);
+#pragma unroll
+        for (int h = 0; h < kGroupCols; ++h) {
+          const int v = f2ord(x[h]);
+          const int m0 = __reduce_max_sync(0xffffffffu, gg == 0 ? v : ord_ninf);
+          const int m1 = __reduce_max_sync(0xffffffffu, gg == 1 ? v : ord_ninf);
+          if (lane == 0) {
+            red[h] = ord2f(m0);
+            red[kGroupCols + h] = ord2f(m1);
+          }
+        }
+        named_bar(1, 128);
+        const float* rd = reinterpret_cast<const float*>(ctl->red);
+        const float M =
+            fmaxf(fmaxf(rd[lane], rd[kN + lane]), fmaxf(rd[2 * kN + lane], rd[3 * kN + lane]));
+        if (M > m_c + kRescaleThreshold || (m_c == -INFINITY && M > -INFINITY)) {
+          alpha_c = m_c == -INFINITY ? 0.f : fast_exp2(m_c - M);
+          m_c = M;
+        }
       }
       const bool need = __any_sync(0xffffffffu, alpha_c != 1.f);
       const float mu_c = m_c == -INFINITY ? 0.f : m_c;
-      // P^T and O^T are read by PV(n - 1): it must have completed before either changes
-      if (n > 0 && !mbar_wait_warp(&ctl->pv_done, (n - 1) & 1, a.status, abort_flag)) break;
-      tc_fence_after();
+      // P^T buffer n % 2 was read by PV(n - 2), which must have completed
+      if (n > 1 && !mbar_wait_warp(&ctl->pv_done[n & 1], ((n - 2) >> 1) & 1, a.status, abort_flag))
+        break;
       // P^T [32 columns][128 rows], two K-major 64-row chunks with the 128-byte swizzle; this
       // thread writes its own group's 16 columns, the other group's stay zero
-      uint8_t* prow = p_s + (r >> 6) * (kN * 128);
+      uint8_t* prow = p_s + (n & 1) * kPBytes + (r >> 6) * (kN * 128);
       const int rr = r & 63;
 #pragma unroll
       for (int h = 0; h < kGroupCols; ++h) {
@@ -444,10 +462,16 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
       if (code == kDeadLoaded &&
           !zero_dead_v_row(ctl, ring, unit_v(n, N), r, a.status, abort_flag))
         n = N;                                         // aborted: leave after this arrival
-      if (n > 0 && need) rescale_o(tmem + lane_base + 32, alpha_c);
+      if (n > 0 && need) {
+        // O^T is accumulated by PV(n - 1): it must have completed before the rescale
+        if (!mbar_wait_warp(&ctl->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, a.status, abort_flag))
+          break;
+        tc_fence_after();
+        rescale_o(tmem + lane_base + 32, alpha_c);
+      }
       fence_proxy_async_smem();   // P^T and zeroed V rows (generic) -> tensor-core reads
       tc_fence_before();
-      mbar_arrive(&ctl->p_full);
+      mbar_arrive(&ctl->p_full[n & 1]);
     }
     // ---- epilogue: column sums, normalise, write out / out_fp32 / lse ---------------------
 #pragma unroll
