@@ -108,35 +108,19 @@ __device__ __forceinline__ TileInfo<CK> load_tile(const AttnLaunch& a, int idx) 
   return t;
 }
 
-// Pool rows of the page pieces of KV tile n (R rows each, R = min(CK, page size)); returns a
-// bit mask of the pieces that hold live keys.  Pieces past the length are not loaded.
+// Page piece `lane` of KV tile n: keys [key, key + R) of one page (R = min(CK, page size)).
+// Returns the piece's first key, or -1 (no piece, empty slot, past the length); the page-table
+// load it issues is first used by the caller after its next barrier wait, so the loads of
+// the whole tile (one per lane) overlap that wait.
 template <int CK>
-__device__ __forceinline__ uint32_t gather_rows(const AttnLaunch& a, const TileInfo<CK>& t,
-                                                const int* pt, int n, int (&rows)[kKvTile / 8]) {
+__device__ __forceinline__ int piece_key(const AttnLaunch& a, const TileInfo<CK>& t, int n, int lane) {
   const int ps = a.page_size;
   const int R = CK < ps ? CK : ps;
+  if (lane >= kKvTile / R) return -1;
+  const int k0 = t.walk.key0(n, (lane * R) / CK);
+  const int key = k0 + (lane * R) % CK;
   const int max_page_idx = (t.L + ps - 1) / ps;
-  uint32_t live = 0;
-  int idx = 0;
-#pragma unroll 1
-  for (int c = 0; c < kKvTile / CK; ++c) {
-    const int k0 = t.walk.key0(n, c);
-#pragma unroll 1
-    for (int p = 0; p < CK / R; ++p, ++idx) {
-      const int key = k0 + p * R;
-      if (k0 < 0 || key >= t.L) continue;
-      const int pidx = key / ps;
-      if (pidx >= max_page_idx) continue;
-      const int page = __ldg(pt + pidx);
-      if (page < 0 || page >= a.num_pages) {
-        report_error(a.status, kErrMetadata);
-        continue;
-      }
-      rows[idx] = page * a.page_rows + t.rec.g * ps + key % ps;
-      live |= 1u << idx;
-    }
-  }
-  return live;
+  return (k0 >= 0 && key < t.L && key / ps < max_page_idx) ? key : -1;
 }
 
 template <int CK>
@@ -190,63 +174,76 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   regs_decrease<kControlRegs>();
   if (warp == 8 || warp == 10) {
     // =============================== producers =========================================
+    // warp 8 copies Q (lane 0) and K, warp 10 copies V; lane i copies page piece i of a tile
+    const bool is_k = warp == 8;
     if (lane == 0) {
-      const bool is_k = warp == 8;
       if (is_k) {
         tma_prefetch_desc(&qmap);
         tma_prefetch_desc(&kmap);
       } else {
         tma_prefetch_desc(&vmap);
       }
-      const int ps = a.page_size;
-      const int R = CK < ps ? CK : ps;
-      const int stages = is_k ? kKStages : kVStages;
-      uint8_t* ring = is_k ? k_s : v_s;
-      uint64_t* full = is_k ? ctl->k_full : ctl->v_full;
-      uint64_t* empty = is_k ? ctl->k_empty : ctl->v_empty;
-      const CUtensorMap* map = is_k ? &kmap : &vmap;
-      const int head_off = is_k ? a.k_head_off : a.v_head_off;
-      int kv_it = 0, qcount = 0;
-      bool ok = true;
-      for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
-        const TileInfo<CK> t = load_tile<CK>(a, idx);
-        if (t.N == 0) continue;
-        if (is_k) {
-          if (qcount > 0 && !mbar_wait<true>(&ctl->q_empty, (qcount - 1) & 1, a.status, abort_flag)) {
-            ok = false;
-            break;
-          }
+    }
+    const int ps = a.page_size;
+    const int R = CK < ps ? CK : ps;
+    const int stages = is_k ? kKStages : kVStages;
+    uint8_t* ring = is_k ? k_s : v_s;
+    uint64_t* full = is_k ? ctl->k_full : ctl->v_full;
+    uint64_t* empty = is_k ? ctl->k_empty : ctl->v_empty;
+    const CUtensorMap* map = is_k ? &kmap : &vmap;
+    const int head_off = is_k ? a.k_head_off : a.v_head_off;
+    int kv_it = 0, qcount = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
+      const TileInfo<CK> t = load_tile<CK>(a, idx);
+      if (t.N == 0) continue;
+      if (is_k) {
+        if (qcount > 0 &&
+            !mbar_wait_warp<true>(&ctl->q_empty, (qcount - 1) & 1, a.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
           const uint32_t qbox = 128u * G * TM;
           mbar_arrive_expect_tx(&ctl->q_full, qbox * 2 * t.nsub);
           for (int w = 0; w < t.nsub; ++w)
             for (int h = 0; h < 2; ++h)
               tma_load_3d(q_s + w * kQBytes + h * kQHalf, &qmap, &ctl->q_full, h * 64,
                           t.rec.g * G, t.rec.q_row0 + w * TM);
-          ++qcount;
         }
-        const int* pt = a.pt_indptr ? a.pt + __ldg(a.pt_indptr + t.rec.b)
-                                    : a.pt + static_cast<long long>(t.rec.b) * a.pt_stride;
-        for (int n = 0; n < t.N; ++n) {
-          const int it = kv_it + n, slot = it % stages;
-          if (it >= stages &&
-              !mbar_wait<true>(&empty[slot], ((it / stages) - 1) & 1, a.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          int rows[kKvTile / 8];
-          const uint32_t live = gather_rows<CK>(a, t, pt, n, rows);
-          const uint32_t bytes = static_cast<uint32_t>(__popc(live)) * R * 128u * 2u;
-          uint8_t* dst = ring + slot * kKvBytes;
-          mbar_arrive_expect_tx(&full[slot], bytes);
-          for (int i = 0; i < kKvTile / R; ++i) {
-            if (!((live >> i) & 1u)) continue;
-            const uint32_t off = static_cast<uint32_t>(i * R) * 128u;
-            tma_load_2d(dst + off, map, &full[slot], 0, rows[i] + head_off);
-            tma_load_2d(dst + kKvHalf + off, map, &full[slot], 64, rows[i] + head_off);
-          }
-        }
-        kv_it += t.N;
+        ++qcount;
       }
+      const int* pt = a.pt_indptr ? a.pt + __ldg(a.pt_indptr + t.rec.b)
+                                  : a.pt + static_cast<long long>(t.rec.b) * a.pt_stride;
+      int key = piece_key<CK>(a, t, 0, lane);
+      int page = key >= 0 ? __ldg(pt + key / ps) : 0;
+      for (int n = 0; n < t.N; ++n) {
+        const int it = kv_it + n, slot = it % stages;
+        if (it >= stages &&
+            !mbar_wait_warp<true>(&empty[slot], ((it / stages) - 1) & 1, a.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        bool live = key >= 0;
+        if (live && (page < 0 || page >= a.num_pages)) {
+          report_error(a.status, kErrMetadata);
+          live = false;
+        }
+        const uint32_t nlive = __popc(__ballot_sync(0xffffffffu, live));
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], nlive * R * 128u * 2u);
+        __syncwarp();
+        if (live) {
+          uint8_t* dst = ring + slot * kKvBytes + static_cast<uint32_t>(lane * R) * 128u;
+          const int row = page * a.page_rows + t.rec.g * ps + key % ps + head_off;
+          tma_load_2d(dst, map, &full[slot], 0, row);
+          tma_load_2d(dst + kKvHalf, map, &full[slot], 64, row);
+        }
+        if (n + 1 < t.N) {                       // next tile's page ids, used after the wait
+          key = piece_key<CK>(a, t, n + 1, lane);
+          page = key >= 0 ? __ldg(pt + key / ps) : 0;
+        }
+      }
+      kv_it += t.N;
     }
   } else if (warp == 9) {
     // =============================== MMA issuer ========================================
