@@ -476,8 +476,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         for (int j = 0; j < kKvTile / 2; ++j) {
           float x0, x1;
           ffma2_bcast(x0, x1, __uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]), sl2, nmu);
-          float p0, p1;
-          exp2_pair_f16(x0, x1, p0, p1);
+          // two f32 ex2 per pair outrun the f16x2 form, whose three conversions cost more
+          // than the second ex2
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
           if (j & 1) fadd2(sb0, sb1, p0, p1);
           else fadd2(sa0, sa1, p0, p1);
           r[j] = pack_bf16(p0, p1);
