@@ -13,6 +13,9 @@
 //   warp  8    TMA producer of Q (once per tile) and K (3-stage ring)
 //   warp  9    TMEM owner and MMA issuer (one thread): S_w = Q_w K^T and O_w += P_w V
 //   warp 10    TMA producer of V (2-stage ring)
+//   warp 11    column facts of each KV tile (first key of each sub-chunk, live-key mask, key
+//              range), a few tiles ahead into a small ring, so that the softmax reads them
+//              from shared memory instead of issuing block-id and valid-bit loads
 // K and V of a 128-key tile are gathered one TMA box per page piece (a page, or the part of
 // a page inside a selected block) and 64-column half.
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512); P_w is
@@ -45,7 +48,20 @@ static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "re
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
+constexpr int kFacts = 4;                      // column-facts ring entries
+
+// Facts of one KV tile that are the same for every row.
+struct TileFacts {
+  int k0[kKvTile / 8];     // first key of each sub-chunk (-1: empty slot)
+  uint32_t colmask[4];     // live keys: slot used, key < length, valid bit set
+  int kmin, kmax;          // key range of the used sub-chunks
+  int zero_v;              // some key slot is not live (V rows to zero)
+  int pad;
+};
+
 struct Ctrl {
+  TileFacts facts[kFacts];
+  uint64_t facts_full[kFacts], facts_empty[kFacts];
   uint64_t q_full, q_empty;
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
@@ -123,7 +139,7 @@ __device__ __forceinline__ int piece_key(const AttnLaunch& a, const TileInfo<CK>
   return (k0 >= 0 && key < t.L && key / ps < max_page_idx) ? key : -1;
 }
 
-template <int CK>
+template <int CK, bool FACTS>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, AttnLaunch a) {
@@ -139,6 +155,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   if (static_cast<int>(blockIdx.x) >= n_live || launch_aborted(a.status)) return;
   const int G = a.G;
   const int TM = kMTileRows / G;                         // tokens per sub-tile
+  // Column facts need block-id or valid-bit loads only for block-sparse rows or valid bits
+  // (FACTS); dense tiles compute them from the tile index in the softmax itself.
+  constexpr bool use_facts = FACTS;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -151,6 +170,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&ctl->v_full[s], 1);
       mbar_init(&ctl->v_empty[s], 1);
+    }
+    for (int f = 0; f < kFacts; ++f) {
+      mbar_init(&ctl->facts_full[f], 1);
+      mbar_init(&ctl->facts_empty[f], 8);      // one arrival per softmax warp
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&ctl->s_full[w], 1);
@@ -242,6 +265,68 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           key = piece_key<CK>(a, t, n + 1, lane);
           page = key >= 0 ? __ldg(pt + key / ps) : 0;
         }
+      }
+      kv_it += t.N;
+    }
+  } else if (warp == 11 && use_facts) {
+    // =============================== column facts ======================================
+    constexpr int PARTS = (CK + 31) / 32;        // 32-key spans per sub-chunk
+    constexpr int SPAN = CK < 32 ? CK : 32;
+    int kv_it = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
+      const TileInfo<CK> t = load_tile<CK>(a, idx);
+      for (int n = 0; n < t.N; ++n) {
+        const int it = kv_it + n, slot = it % kFacts;
+        if (it >= kFacts &&
+            !mbar_wait_warp<true>(&ctl->facts_empty[slot], ((it / kFacts) - 1) & 1, a.status,
+                                  abort_flag)) {
+          ok = false;
+          break;
+        }
+        TileFacts* f = &ctl->facts[slot];
+        const bool has_c = lane < NSUB;          // lane c: sub-chunk c
+        const int k0 = has_c ? t.walk.key0(n, lane) : -1;
+        if (has_c) f->k0[lane] = k0;
+        // lane s < NSUB * PARTS: span `part` of sub-chunk c
+        const int c_of = min(lane / PARTS, NSUB - 1);
+        const int kc = __shfl_sync(0xffffffffu, k0, c_of);
+        uint32_t bits = 0u;
+        int col0 = -32;
+        if (lane < NSUB * PARTS) {
+          const int part = lane % PARTS;
+          col0 = c_of * CK + part * 32;
+          if (kc >= 0) {
+            const int key = kc + part * 32;
+            const int live = t.L - key;          // keys < L in this span
+            bits = live >= SPAN ? (SPAN == 32 ? 0xffffffffu : ((1u << SPAN) - 1u))
+                                : (live > 0 ? ((1u << live) - 1u) : 0u);
+            if (a.valid_bits) {
+              const int wi = key >> 5;
+              const uint32_t word =
+                  wi < a.valid_words
+                      ? __ldg(a.valid_bits + static_cast<long long>(t.rec.b) * a.valid_words + wi)
+                      : 0u;
+              bits &= (word >> (key & 31));
+            }
+          }
+        }
+        uint32_t words[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          words[i] = __reduce_or_sync(0xffffffffu, (col0 >> 5) == i ? bits << (col0 & 31) : 0u);
+        const bool zero = __any_sync(0xffffffffu, has_c && (k0 < 0 || k0 + CK > t.L));
+        const int kmin = __reduce_min_sync(0xffffffffu, (has_c && k0 >= 0) ? k0 : 0x7fffffff);
+        const int kmax = __reduce_max_sync(0xffffffffu, (has_c && k0 >= 0) ? k0 + CK - 1 : -1);
+        if (lane == 0) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) f->colmask[i] = words[i];
+          f->kmin = kmin;
+          f->kmax = kmax;
+          f->zero_v = zero;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->facts_full[slot]);
       }
       kv_it += t.N;
     }
@@ -359,6 +444,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       const int N = t.N;
       const int ntok_w = w == 0 ? t.ntok0 : t.ntok1;
       if (w >= t.nsub) {                           // this sub-tile is empty
+        for (int n = 0; ok && use_facts && n < N; ++n) {   // release the tiles' column facts
+          const int it = kv_it + n;
+          ok = mbar_wait_warp<true>(&ctl->facts_full[it % kFacts], (it / kFacts) & 1, a.status,
+                                    abort_flag);
+          if (ok && lane == 0) mbar_arrive(&ctl->facts_empty[it % kFacts]);
+        }
         kv_it += N;
         continue;
       }
@@ -378,46 +469,68 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // ---- per-tile column facts, identical for every row ----------------------------
         int k0[NSUB];
         uint32_t colmask[4];
-        bool zero_v = false;
-        int kmin = 0x7fffffff, kmax = -1;
-#pragma unroll
-        for (int c = 0; c < NSUB; ++c) {
-          k0[c] = t.walk.key0(n, c);
-          if (k0[c] < 0 || k0[c] + CK > L) zero_v = true;
-          if (k0[c] >= 0) {
-            kmin = min(kmin, k0[c]);
-            kmax = max(kmax, k0[c] + CK - 1);
+        int kmin, kmax;
+        bool zero_v, full;
+        if constexpr (FACTS) {                     // from the facts warp
+          if (!mbar_wait_warp<true>(&ctl->facts_full[it % kFacts], (it / kFacts) & 1, a.status,
+                                    abort_flag)) {
+            ok = false;
+            break;
           }
-        }
-        const bool full = !a.valid_bits && !zero_v &&
-                          (!causal || kmax <= pos) && (wl < 0 || kmin >= pos - wl);
-        if (!full) {
+          const TileFacts* fc = &ctl->facts[it % kFacts];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) colmask[i] = 0u;
+          for (int c = 0; c < NSUB; ++c) k0[c] = fc->k0[c];
 #pragma unroll
+          for (int i = 0; i < 4; ++i) colmask[i] = fc->colmask[i];
+          kmin = fc->kmin;
+          kmax = fc->kmax;
+          zero_v = fc->zero_v != 0;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->facts_empty[it % kFacts]);
+          full = !a.valid_bits && !zero_v && (!causal || kmax <= pos) && (wl < 0 || kmin >= pos - wl);
+        } else {                                   // dense rows: facts from the tile index
+          zero_v = false;
+          kmin = 0x7fffffff;
+          kmax = -1;
+  #pragma unroll
           for (int c = 0; c < NSUB; ++c) {
-            // live-key bits of the CK columns of sub-chunk c
-#pragma unroll
-            for (int part = 0; part < (CK + 31) / 32; ++part) {
-              const int col0 = c * CK + part * 32;        // first column of this 32-span
-              const int span = CK < 32 ? CK : 32;
-              uint32_t bits = 0u;
-              if (k0[c] >= 0) {
-                const int key = k0[c] + part * 32;
-                const int live = L - key;                  // keys < L in this span
-                bits = live >= span ? (span == 32 ? 0xffffffffu : ((1u << span) - 1u))
-                                    : (live > 0 ? ((1u << live) - 1u) : 0u);
-                if (a.valid_bits) {
-                  const int wi = key >> 5;
-                  const uint32_t word =
-                      wi < a.valid_words
-                          ? __ldg(a.valid_bits + static_cast<long long>(t.rec.b) * a.valid_words +
-                                  wi)
-                          : 0u;
-                  bits &= (word >> (key & 31));
+            k0[c] = t.walk.key0(n, c);
+            if (k0[c] < 0 || k0[c] + CK > L) zero_v = true;
+            if (k0[c] >= 0) {
+              kmin = min(kmin, k0[c]);
+              kmax = max(kmax, k0[c] + CK - 1);
+            }
+          }
+          full = !a.valid_bits && !zero_v &&
+                            (!causal || kmax <= pos) && (wl < 0 || kmin >= pos - wl);
+          if (!full) {
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) colmask[i] = 0u;
+  #pragma unroll
+            for (int c = 0; c < NSUB; ++c) {
+              // live-key bits of the CK columns of sub-chunk c
+  #pragma unroll
+              for (int part = 0; part < (CK + 31) / 32; ++part) {
+                const int col0 = c * CK + part * 32;        // first column of this 32-span
+                const int span = CK < 32 ? CK : 32;
+                uint32_t bits = 0u;
+                if (k0[c] >= 0) {
+                  const int key = k0[c] + part * 32;
+                  const int live = L - key;                  // keys < L in this span
+                  bits = live >= span ? (span == 32 ? 0xffffffffu : ((1u << span) - 1u))
+                                      : (live > 0 ? ((1u << live) - 1u) : 0u);
+                  if (a.valid_bits) {
+                    const int wi = key >> 5;
+                    const uint32_t word =
+                        wi < a.valid_words
+                            ? __ldg(a.valid_bits + static_cast<long long>(t.rec.b) * a.valid_words +
+                                    wi)
+                            : 0u;
+                    bits &= (word >> (key & 31));
+                  }
                 }
+                colmask[col0 >> 5] |= bits << (col0 & 31);
               }
-              colmask[col0 >> 5] |= bits << (col0 & 31);
             }
           }
         }
@@ -572,11 +685,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
 int g_num_sms = 0;
 
-template <int CK>
+template <int CK, bool FACTS>
 int launch_ck(const AttnLaunch& a, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_tc_kernel<CK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_tc_kernel<CK, FACTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess)
       return -1;
     attr_set = true;
@@ -588,7 +701,7 @@ int launch_ck(const AttnLaunch& a, cudaStream_t st) {
       return -1;
   }
   const int grid = a.capacity < g_num_sms ? a.capacity : g_num_sms;
-  attn_tc_kernel<CK><<<grid, kThreads, kSmemBytes, st>>>(a.qmap, a.kmap, a.vmap, a);
+  attn_tc_kernel<CK, FACTS><<<grid, kThreads, kSmemBytes, st>>>(a.qmap, a.kmap, a.vmap, a);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
@@ -598,11 +711,13 @@ int launch_ck(const AttnLaunch& a, cudaStream_t st) {
 int launch_attn(const AttnLaunch& a, cudaStream_t st) {
   if (a.capacity <= 0) return 0;
   switch (attn_sub_chunk(a.kv_block_size, a.block_sparse != 0)) {
-    case 8: return launch_ck<8>(a, st);
-    case 16: return launch_ck<16>(a, st);
-    case 32: return launch_ck<32>(a, st);
-    case 64: return launch_ck<64>(a, st);
-    case 128: return launch_ck<128>(a, st);
+    case 8: return launch_ck<8, true>(a, st);
+    case 16: return launch_ck<16, true>(a, st);
+    case 32: return launch_ck<32, true>(a, st);
+    case 64: return launch_ck<64, true>(a, st);
+    case 128:
+      return (a.block_sparse || a.valid_bits) ? launch_ck<128, true>(a, st)
+                                              : launch_ck<128, false>(a, st);
     default: return -2;
   }
 }
