@@ -226,6 +226,31 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         const uint32_t vt = kt + kTileBytes;
         const int kbase = first_key + s * kStageKeys + warp * 16;   // first key of this warp
 
+        // ---- this warp's 16 keys of K and V into registers; the stage is released at once,
+        // so the producer refills it while the warp computes -----------------------------
+        const int mi = lane >> 3, r8 = lane & 7;
+        uint32_t kb[kD / 16][4], vb[kD / 16][4];
+        {
+          const uint32_t key_local = warp * 16 + (mi >> 1) * 8 + r8;
+#pragma unroll
+          for (int ks = 0; ks < kD / 16; ++ks) {
+            const int dim = ks * 16 + (mi & 1) * 8;
+            ldsm_x4(kt + (dim >> 6) * kHalfBytes + swz(key_local, (dim & 63) >> 3), kb[ks][0],
+                    kb[ks][1], kb[ks][2], kb[ks][3]);
+          }
+        }
+        {
+          const uint32_t key_local = warp * 16 + (mi & 1) * 8 + r8;
+#pragma unroll
+          for (int j = 0; j < kD / 8; j += 2) {
+            const int dim = (j + (mi >> 1)) * 8;
+            ldsm_x4_t(vt + (dim >> 6) * kHalfBytes + swz(key_local, (dim & 63) >> 3),
+                      vb[j >> 1][0], vb[j >> 1][1], vb[j >> 1][2], vb[j >> 1][3]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->empty[slot]);
+
         // ---- S = Q K^T over this warp's 16 keys --------------------------------------
         // even and odd k-steps accumulate separately: two independent MMA chains per tile
         float sc[2][4], sd[2][4];
@@ -234,15 +259,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
 #pragma unroll
           for (int e = 0; e < 4; ++e) sc[nt][e] = sd[nt][e] = 0.f;
         {
-          const int mi = lane >> 3, r = lane & 7;
-          const uint32_t key_local = warp * 16 + (mi >> 1) * 8 + r;
-          uint32_t kb[kD / 16][4];
-#pragma unroll
-          for (int ks = 0; ks < kD / 16; ++ks) {
-            const int dim = ks * 16 + (mi & 1) * 8;
-            ldsm_x4(kt + (dim >> 6) * kHalfBytes + swz(key_local, (dim & 63) >> 3), kb[ks][0],
-                    kb[ks][1], kb[ks][2], kb[ks][3]);
-          }
 #pragma unroll
           for (int ks = 0; ks < kD / 16; ks += 2) {
             mma_16816(sc[0], qa[ks], kb[ks][0], kb[ks][1]);
@@ -320,14 +336,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         const uint32_t m_lo = (vk[0][0] ? 0x0000FFFFu : 0u) | (vk[0][1] ? 0xFFFF0000u : 0u);
         const uint32_t m_hi = (vk[1][0] ? 0x0000FFFFu : 0u) | (vk[1][1] ? 0xFFFF0000u : 0u);
         {
-          const int mi = lane >> 3, r = lane & 7;
-          const uint32_t key_local = warp * 16 + (mi & 1) * 8 + r;
 #pragma unroll
           for (int j = 0; j < kD / 8; j += 2) {
-            const int dim = (j + (mi >> 1)) * 8;
-            const uint32_t addr = vt + (dim >> 6) * kHalfBytes + swz(key_local, (dim & 63) >> 3);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(addr, b0, b1, b2, b3);
+            uint32_t b0 = vb[j >> 1][0], b1 = vb[j >> 1][1], b2 = vb[j >> 1][2], b3 = vb[j >> 1][3];
             if (any_invalid) {   // stale or unused rows may hold non-finite values
               b0 &= m_lo;
               b1 &= m_hi;
@@ -338,8 +349,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             mma_16816(o[j + 1], aP, b2, b3);
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->empty[slot]);
       }
       if (!ok) break;
 
