@@ -196,7 +196,7 @@ typedef struct paged_decode_params {
   float bmm1_scale;     /* softmax scale; <= 0 selects 1/sqrt(D)                          */
   float bmm2_scale;     /* multiplies the normalised output ([DEC] bmm2_scale)             */
   int split_chunk;      /* keys per split-KV partition, a multiple of 128; 0 = automatic:
-                           128 * max(1, B * Hkv * ceil(max_seq_len / 128) / (48 * SMs))     */
+                           128 * max(1, B * Hkv * ceil(max_seq_len / 128) / (16 * SMs))     */
 } paged_decode_params;
 
 /* Workspace bytes for the decode plan and the fp32 split partials. */

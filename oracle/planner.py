@@ -91,9 +91,9 @@ def plan_prefill_tiles(Hkv, qo_indptr, seq_lens_kv, tile_tokens, mask_type="dens
 
 def decode_split_chunk(B, Hkv, max_seq_len, num_sms):
     """Keys per split-KV partition, from static arguments only: 128 x max(1, floor(B * Hkv *
-    ceil(max_seq_len / 128) / (48 * num_sms))), capped at ceil(max_seq_len / 128) tiles."""
+    ceil(max_seq_len / 128) / (16 * num_sms))), capped at ceil(max_seq_len / 128) tiles."""
     tiles = max(1, -(-max_seq_len // 128))
-    ct = max(1, (B * Hkv * tiles) // (48 * num_sms))
+    ct = max(1, (B * Hkv * tiles) // (16 * num_sms))
     return 128 * min(ct, tiles)
 
 

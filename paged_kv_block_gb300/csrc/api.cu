@@ -195,7 +195,7 @@ bool decode_params_ok(const paged_decode_params* p) {
 int decode_chunk(const paged_decode_params* p) {
   if (p->split_chunk > 0) return p->split_chunk;
   const long long tiles = ceil_div_ll(p->max_seq_len, 128);
-  long long ct = static_cast<long long>(p->batch) * p->num_kv_heads * tiles / (48LL * num_sms());
+  long long ct = static_cast<long long>(p->batch) * p->num_kv_heads * tiles / (16LL * num_sms());
   if (ct < 1) ct = 1;
   if (ct > tiles) ct = tiles;
   return static_cast<int>(128 * ct);

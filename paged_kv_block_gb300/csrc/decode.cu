@@ -28,7 +28,10 @@ constexpr int kHalfBytes = kStageKeys * 128;         // 64 keys x 64 dims x bf16
 constexpr int kTileBytes = 2 * kHalfBytes;            // one K (or V) stage tile
 constexpr int kStageBytes = 2 * kTileBytes;           // K + V
 constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kMergeWarp = kConsumerWarps + 1;
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kMergeSlots = 2;
 constexpr int kItemSlots = 2;
 constexpr int kMaxG = 16;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -39,8 +42,10 @@ struct DecodeSmem {
   uint64_t item_full[kItemSlots];
   uint64_t item_empty[kItemSlots];
   int item_id[kItemSlots];
+  uint64_t merge_full[kMergeSlots];
+  uint64_t merge_empty[kMergeSlots];
+  int4 merge_job[kMergeSlots];   // (request, KV head, item, splits); request -1 ends the queue
   int abort_flag;
-  int last_flag;
   float red_m[kConsumerWarps][kMaxG];
   float red_l[kConsumerWarps][kMaxG];
 };
@@ -84,13 +89,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       mbar_init(&sm->item_full[s], 1);
       mbar_init(&sm->item_empty[s], kConsumerWarps);
     }
+    for (int s = 0; s < kMergeSlots; ++s) {
+      mbar_init(&sm->merge_full[s], 1);
+      mbar_init(&sm->merge_empty[s], 1);
+    }
     sm->abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
   volatile int* abort_flag = &sm->abort_flag;
 
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
     // ------------------------------ producer (whole warp) -----------------------------
     // Lane p handles page piece p of every stage (R keys of one page); the page ids of the
     // next stage are loaded while the current stage is issued.
@@ -172,17 +181,79 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       }
       if (!ok) break;
     }
+  } else if (warp == kMergeWarp) {
+    // ------------------------------ split merger ---------------------------------------
+    // For each item of a multi-split request: make its partials visible GPU-wide, count the
+    // split, and if it is the last of (b, g) to finish, merge all splits (lane -> 4 columns).
+    for (int jcount = 0;; ++jcount) {
+      const int js = jcount % kMergeSlots;
+      if (!mbar_wait_warp(&sm->merge_full[js], (jcount / kMergeSlots) & 1, a.status, abort_flag))
+        break;
+      const int4 job = sm->merge_job[js];
+      if (job.x < 0) break;
+      const int b = job.x, g = job.y, n_split = job.w;
+      __threadfence();   // the consumers' partials (ordered before the hand-off) -> GPU scope
+      int prev = 0;
+      if (lane == 0) prev = atomicAdd(a.counters + b * a.Hkv + g, 1);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev == n_split - 1) {
+        __threadfence();
+        const long long base = static_cast<long long>(a.Hkv) * a.split_offset[b] +
+                               static_cast<long long>(g) * n_split;
+        for (int h = 0; h < G; ++h) {
+          float M = -INFINITY;
+          for (int s = lane; s < n_split; s += 32)
+            M = fmaxf(M, __ldcg(a.part_lse + (base + s) * G + h));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+          const float Mu = M == -INFINITY ? 0.f : M;
+          float wsum = 0.f;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int s = 0; s < n_split; ++s) {
+            const float wgt = __expf(__ldcg(a.part_lse + (base + s) * G + h) - Mu);
+            wsum += wgt;
+            if (wgt > 0.f) {
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                                   a.part_o + ((base + s) * G + h) * kD) + lane);
+              acc.x += wgt * v.x;
+              acc.y += wgt * v.y;
+              acc.z += wgt * v.z;
+              acc.w += wgt * v.w;
+            }
+          }
+          const float sc = wsum > 0.f ? a.out_scale / wsum : 0.f;
+          const long long orow = static_cast<long long>(b) * a.Hq + g * G + h;
+          __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(a.out + orow * kD) + lane * 2;
+          dst[0] = __floats2bfloat162_rn(acc.x * sc, acc.y * sc);
+          dst[1] = __floats2bfloat162_rn(acc.z * sc, acc.w * sc);
+          if (a.lse && lane == 0) a.lse[orow] = wsum > 0.f ? Mu + __logf(wsum) : -INFINITY;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm->merge_empty[js]);
+    }
   } else {
     // ------------------------------ consumers ------------------------------------------
     const int gr = lane >> 2, tq = lane & 3;   // fragment row group, thread-in-quad
     const float sl2 = a.scale_log2;
     int sg = 0;
+    int jcount = 0;                            // merge jobs handed to the merge warp
     for (int icount = 0;; ++icount) {
       const int islot = icount % kItemSlots;
       if (!mbar_wait_warp(&sm->item_full[islot], (icount / kItemSlots) & 1, a.status, abort_flag))
         break;
       const int item = sm->item_id[islot];
-      if (item < 0) break;
+      if (item < 0) {
+        if (threadIdx.x == 0) {                  // end of the merge queue
+          const int js = jcount % kMergeSlots;
+          if (jcount < kMergeSlots ||
+              mbar_wait(&sm->merge_empty[js], ((jcount / kMergeSlots) - 1) & 1, a.status, abort_flag)) {
+            sm->merge_job[js] = make_int4(-1, 0, 0, 0);
+            mbar_arrive(&sm->merge_full[js]);
+          }
+        }
+        break;
+      }
       const SplitItem it = a.items[item];
       const int b = it.b, g = it.g;
       const int kv_begin = it.kv_begin, kv_end = it.kv_end;
@@ -410,35 +481,18 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         }
       }
       if (n_split > 1) {
-        // the last split of (b, g) to finish merges all of them
-        __threadfence();
-        named_bar(1, kConsumerWarps * 32);
+        // the fence, the split counter and, for the last split of (b, g), the merge run on the
+        // merge warp, so the consumers go on to the next item at once
+        named_bar(1, kConsumerWarps * 32);         // every partial of this item is written
         if (threadIdx.x == 0) {
-          const int prev = atomicAdd(a.counters + b * a.Hkv + g, 1);
-          sm->last_flag = prev == n_split - 1;
-        }
-        named_bar(1, kConsumerWarps * 32);
-        if (sm->last_flag) {
-          __threadfence();
-          const long long base = static_cast<long long>(a.Hkv) * a.split_offset[b] +
-                                 static_cast<long long>(g) * n_split;
-          for (int h = 0; h < G; ++h) {
-            float M = -INFINITY;
-            for (int s = 0; s < n_split; ++s)
-              M = fmaxf(M, __ldcg(a.part_lse + (base + s) * G + h));
-            const float Mu = M == -INFINITY ? 0.f : M;
-            float wsum = 0.f, acc = 0.f;
-            for (int s = 0; s < n_split; ++s) {
-              const float wgt = __expf(__ldcg(a.part_lse + (base + s) * G + h) - Mu);
-              wsum += wgt;
-              if (wgt > 0.f) acc += wgt * __ldcg(a.part_o + ((base + s) * G + h) * kD + d);
-            }
-            const long long orow = static_cast<long long>(b) * a.Hq + g * G + h;
-            a.out[orow * kD + d] =
-                __float2bfloat16_rn(wsum > 0.f ? acc / wsum * a.out_scale : 0.f);
-            if (a.lse && d == 0) a.lse[orow] = wsum > 0.f ? Mu + __logf(wsum) : -INFINITY;
+          const int js = jcount % kMergeSlots;
+          if (jcount < kMergeSlots ||
+              mbar_wait(&sm->merge_empty[js], ((jcount / kMergeSlots) - 1) & 1, a.status, abort_flag)) {
+            sm->merge_job[js] = make_int4(b, g, item, n_split);
+            mbar_arrive(&sm->merge_full[js]);
           }
         }
+        ++jcount;
       }
       named_bar(1, kConsumerWarps * 32);   // the combine buffers are free again
     }

@@ -78,7 +78,8 @@ def test_decode_splits_partition_the_visible_keys():
 
 
 def test_decode_chunk_formula():
-    assert PL.decode_split_chunk(64, 8, 8192, 152) == 512
+    # floor(64 * 8 * 64 / (16 * 152)) = 13 tiles of 128 keys
+    assert PL.decode_split_chunk(64, 8, 8192, 152) == 1664
     assert PL.decode_split_chunk(1, 1, 100, 152) == 128
     assert PL.decode_split_chunk(4096, 8, 1000, 148) == 128 * 8
     assert PL.decode_split_chunk(4096, 8, 1 << 20, 148) % 128 == 0
