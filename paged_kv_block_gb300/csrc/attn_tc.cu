@@ -560,9 +560,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
               hi_lim[c] = causal ? pos - k0[c] : 0x7fffffff;
               lo_lim[c] = wl >= 0 ? pos - wl - k0[c] : -0x7fffffff;
             }
+            if constexpr (!FACTS) {
+              // one unsigned range test and a select per column (the limits differ per row, so
+              // a data-dependent branch here would diverge across the warp)
+              int span[NSUB];
 #pragma unroll
-            for (int c = 0; c < kKvTile; ++c)
-              if (c % CK > hi_lim[c / CK] || c % CK < lo_lim[c / CK]) r[c] = 0xff800000u;
+              for (int c = 0; c < NSUB; ++c) {
+                // limits clamped into the sub-chunk; an empty range masks every column
+                int lo_c = max(lo_lim[c], 0), hi_c = min(hi_lim[c], CK - 1);
+                if (hi_c < lo_c) lo_c = hi_c = CK;
+                lo_lim[c] = lo_c;
+                span[c] = hi_c - lo_c;
+              }
+#pragma unroll
+              for (int c = 0; c < kKvTile; ++c) {
+                const bool out = static_cast<unsigned>(c % CK - lo_lim[c / CK]) >
+                                 static_cast<unsigned>(span[c / CK]);
+                r[c] = out ? 0xff800000u : r[c];
+              }
+            } else {
+              // (block-sparse tiles keep the plain per-column test, which compiles better there)
+#pragma unroll
+              for (int c = 0; c < kKvTile; ++c)
+                if (c % CK > hi_lim[c / CK] || c % CK < lo_lim[c / CK]) r[c] = 0xff800000u;
+            }
           }
         }
         // row maximum: 8 independent chains of 3-input max, then a short tree
