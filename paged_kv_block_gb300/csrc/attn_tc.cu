@@ -103,9 +103,9 @@ struct TileInfo {
 };
 
 template <int CK>
-__device__ __forceinline__ TileInfo<CK> load_tile(const AttnLaunch& a, int idx) {
+__device__ __forceinline__ TileInfo<CK> tile_from_rec(const AttnLaunch& a, const TileRec& rec) {
   TileInfo<CK> t;
-  t.rec = a.tiles[idx];
+  t.rec = rec;
   const int TM = kMTileRows / a.G;
   t.ntok0 = min(t.rec.ntok, TM);
   t.ntok1 = t.rec.ntok - t.ntok0;
@@ -122,6 +122,11 @@ __device__ __forceinline__ TileInfo<CK> load_tile(const AttnLaunch& a, int idx) 
   t.walk.total_sub = t.walk.dense ? 0 : (t.rec.kv_end - t.rec.kv_begin) * t.walk.spb;
   t.N = t.walk.num_tiles();
   return t;
+}
+
+template <int CK>
+__device__ __forceinline__ TileInfo<CK> load_tile(const AttnLaunch& a, int idx) {
+  return tile_from_rec<CK>(a, a.tiles[idx]);
 }
 
 // Page piece `lane` of KV tile n: keys [key, key + R) of one page (R = min(CK, page size)).
@@ -217,9 +222,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int head_off = is_k ? a.k_head_off : a.v_head_off;
     int kv_it = 0, qcount = 0;
     bool ok = true;
+    TileRec rec_nx = a.tiles[blockIdx.x];       // record of the next work tile, loaded a tile ahead
     for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
-      const TileInfo<CK> t = load_tile<CK>(a, idx);
+      const TileInfo<CK> t = tile_from_rec<CK>(a, rec_nx);
+      if (idx + static_cast<int>(gridDim.x) < n_live) rec_nx = a.tiles[idx + gridDim.x];
       if (t.N == 0) continue;
+      // page ids of the first KV tile: loaded before the wait for the Q buffer
+      const int* pt = a.pt_indptr ? a.pt + __ldg(a.pt_indptr + t.rec.b)
+                                  : a.pt + static_cast<long long>(t.rec.b) * a.pt_stride;
+      int key = piece_key<CK>(a, t, 0, lane);
+      int page = key >= 0 ? __ldg(pt + key / ps) : 0;
       if (is_k) {
         if (qcount > 0 &&
             !mbar_wait_warp<true>(&ctl->q_empty, (qcount - 1) & 1, a.status, abort_flag)) {
@@ -236,10 +248,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
         ++qcount;
       }
-      const int* pt = a.pt_indptr ? a.pt + __ldg(a.pt_indptr + t.rec.b)
-                                  : a.pt + static_cast<long long>(t.rec.b) * a.pt_stride;
-      int key = piece_key<CK>(a, t, 0, lane);
-      int page = key >= 0 ? __ldg(pt + key / ps) : 0;
       for (int n = 0; n < t.N; ++n) {
         const int it = kv_it + n, slot = it % stages;
         if (it >= stages &&
@@ -274,8 +282,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     constexpr int SPAN = CK < 32 ? CK : 32;
     int kv_it = 0;
     bool ok = true;
+    TileRec rec_nx = a.tiles[blockIdx.x];       // record of the next work tile, loaded a tile ahead
     for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
-      const TileInfo<CK> t = load_tile<CK>(a, idx);
+      const TileInfo<CK> t = tile_from_rec<CK>(a, rec_nx);
+      if (idx + static_cast<int>(gridDim.x) < n_live) rec_nx = a.tiles[idx + gridDim.x];
       for (int n = 0; n < t.N; ++n) {
         const int it = kv_it + n, slot = it % kFacts;
         if (it >= kFacts &&
@@ -363,8 +373,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       int kv_it = 0, qcount = 0, pc1 = 0;
       int ep[2] = {0, 0};                        // epilogues that read O_w so far
       bool ok = true;
+      TileRec rec_nx = a.tiles[blockIdx.x];     // record of the next work tile, a tile ahead
       for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
-        const TileInfo<CK> t = load_tile<CK>(a, idx);
+        const TileInfo<CK> t = tile_from_rec<CK>(a, rec_nx);
+        if (idx + static_cast<int>(gridDim.x) < n_live) rec_nx = a.tiles[idx + gridDim.x];
         const int N = t.N;
         if (N == 0) continue;
         const bool two = t.nsub > 1;
