@@ -241,44 +241,80 @@ def batch_prefill(q, k_cache, v_cache, qo_indptr, block_tables, seq_lens_kv, *,
 
 
 # ----------------------------------------------------------------------------------------
-# [DEC] single-token decode over a CSR-paged cache
+# [DEC] decode over a CSR-paged cache: one query, SQ fixed queries, or packed queries
 # ----------------------------------------------------------------------------------------
 
 def batch_decode(query, kv_indptr, kv_indices, seq_lens, *, kv_cache=None, k_cache=None,
                  v_cache=None, bmm1_scale=None, bmm2_scale=1.0, mask_type="dense",
-                 window_left=-1, rows=None):
-    """[DEC] forward for seq_len_q = 1: query [B, Hq, D]; the query sits at p = len - 1, so
-    the causal mask keeps every live key; window_left = w >= 0 keeps j >= len - 1 - w.
-    bmm1_scale is the softmax scale (default 1/sqrt(D)); bmm2_scale multiplies the output.
-    Returns O [B, Hq, D], LSE [B, Hq]."""
+                 window_left=-1, seq_len_q=1, qo_indptr=None, rows=None):
+    """[DEC] forward (signature and notes on seq_len_q / qo_indptr).  Query layouts:
+
+      * seq_len_q = 1, no qo_indptr: query [B, Hq, D]; O [B, Hq, D], LSE [B, Hq];
+      * seq_len_q = SQ > 1: token-major query [B, SQ, Hq, D]; O and LSE [B, SQ, ...];
+      * qo_indptr given: packed query [total_q, Hq, D], request b owning rows
+        qo_indptr[b]:qo_indptr[b+1]; O [total_q, Hq, D], LSE [total_q, Hq].
+
+    Query i of a request with nq queries and L keys sits at p = L - nq + i: keys j < L are
+    candidates, the causal mask keeps j <= p, and window_left = w >= 0 keeps j >= p - w.
+    With one query p = L - 1, so the causal mask keeps every live key.  bmm1_scale is the
+    softmax scale (default 1/sqrt(D)); bmm2_scale multiplies the normalised output.
+    rows: optional list of request indices to evaluate (the rest is NaN)."""
     if window_left >= 0 and mask_type != "causal":
         raise ValueError("window_left >= 0 requires the causal mask")
     qf = f64(query)
-    B, Hq, D = qf.shape
+    lens = i64(seq_lens)
+    B = lens.size
+    if qo_indptr is not None:
+        qo = i64(qo_indptr)
+        qp = qf
+    elif seq_len_q > 1:
+        qo = np.arange(B + 1, dtype=np.int64) * seq_len_q
+        qp = qf.reshape((B * seq_len_q,) + qf.shape[2:])
+    else:
+        qo = np.arange(B + 1, dtype=np.int64)
+        qp = qf
+    T, Hq, D = qp.shape
     Kp, Vp = split_pools(kv_cache, k_cache, v_cache)
     Hkv = Kp.shape[1]
     G = Hq // Hkv
     scale = (1.0 / math.sqrt(D)) if bmm1_scale is None else float(bmm1_scale)
-    indptr, indices, lens = i64(kv_indptr), i64(kv_indices), i64(seq_lens)
+    indptr, indices = i64(kv_indptr), i64(kv_indices)
     want = set(int(r) for r in rows) if rows is not None else None
-    out = np.full((B, Hq, D), np.nan if rows is not None else 0.0)
-    lse = np.full((B, Hq), np.nan if rows is not None else -np.inf)
+    out = np.full((T, Hq, D), np.nan if rows is not None else 0.0)
+    lse = np.full((T, Hq), np.nan if rows is not None else -np.inf)
     for b in range(B):
         if want is not None and b not in want:
             continue
+        r0, r1 = int(qo[b]), int(qo[b + 1])
         L = int(lens[b])
         pages = indices[indptr[b]:indptr[b + 1]]
         K = gather_pages(Kp, pages, L)
         V = gather_pages(Vp, pages, L)
-        vis = np.ones((1, L), bool)
-        if window_left >= 0:
-            vis &= np.arange(L)[None, :] >= (L - 1 - window_left)
+        keys = np.arange(L)
+        p = L - (r1 - r0) + np.arange(r1 - r0)
+        vis = np.ones((r1 - r0, L), bool)
+        if mask_type == "causal":
+            vis &= keys[None, :] <= p[:, None]
+            if window_left >= 0:
+                vis &= keys[None, :] >= (p - window_left)[:, None]
         for g in range(Hkv):
-            o, s = masked_softmax_attention(qf[b, None, g * G:(g + 1) * G], K[:, g], V[:, g],
+            o, s = masked_softmax_attention(qp[r0:r1, g * G:(g + 1) * G], K[:, g], V[:, g],
                                             vis, scale, bmm2_scale)
-            out[b, g * G:(g + 1) * G] = o[0]
-            lse[b, g * G:(g + 1) * G] = s[0]
+            out[r0:r1, g * G:(g + 1) * G] = o
+            lse[r0:r1, g * G:(g + 1) * G] = s
+    if qo_indptr is None and seq_len_q > 1:
+        return out.reshape(B, seq_len_q, Hq, D), lse.reshape(B, seq_len_q, Hq)
     return out, lse
+
+
+def decode_visible_pairs(Hq, seq_lens, q_lens, mask_type="dense", window_left=-1):
+    """Visible (query row, query head, key) triples of a [DEC] problem whose request b has
+    q_lens[b] queries (the counting rule of the forward above)."""
+    lens = i64(seq_lens)
+    nq = i64(q_lens)
+    qo = np.zeros(lens.size + 1, dtype=np.int64)
+    qo[1:] = np.cumsum(nq)
+    return prefill_visible_pairs(Hq, qo, lens, mask_type, window_left)
 
 
 def merge_partials(o_parts, lse_parts):

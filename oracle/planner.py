@@ -97,19 +97,21 @@ def decode_split_chunk(B, Hkv, max_seq_len, num_sms):
     return 128 * min(ct, tiles)
 
 
-def plan_decode(seq_lens, Hkv, chunk, window_left=-1):
-    """Split-KV work list.  Request b with L keys (the visible ones start at lo = max(0,
-    L - 1 - window_left) with a window, else 0) is cut at multiples of `chunk`: splits
-    s in [lo // chunk, max(ceil(L / chunk), lo // chunk + 1)).  split_offset is the
-    exclusive prefix sum of the split counts; item Hkv * split_offset[b] + g * n_b + k is
-    (b, g, kv_begin, kv_end) of the k-th split, kv_begin = max(s * chunk, lo) and
-    kv_end = min((s + 1) * chunk, L)."""
+def plan_decode(seq_lens, Hkv, chunk, window_left=-1, q_lens=None):
+    """Split-KV work list.  Request b with L keys and nq queries (q_lens[b], default 1) has
+    its visible keys in [lo, L): lo = max(0, L - nq - window_left) with a window (the first
+    key the earliest query, at position L - nq, keeps), else 0.  [lo, L) is cut at
+    multiples of `chunk`: splits s in [lo // chunk, max(ceil(L / chunk), lo // chunk + 1)).
+    split_offset is the exclusive prefix sum of the split counts; item Hkv * split_offset[b]
+    + g * n_b + k is (b, g, kv_begin, kv_end) of the k-th split, kv_begin = max(s * chunk,
+    lo) and kv_end = min((s + 1) * chunk, L)."""
     lens = i64(seq_lens)
     B = lens.size
+    nqs = np.ones(B, np.int64) if q_lens is None else i64(q_lens)
     counts, firsts = [], []
-    for L in lens:
-        L = int(L)
-        lo = max(0, L - 1 - window_left) if window_left >= 0 else 0
+    for L, nq in zip(lens, nqs):
+        L, nq = int(L), int(nq)
+        lo = max(0, L - nq - window_left) if window_left >= 0 else 0
         s0 = lo // chunk
         s1 = max(-(-L // chunk), s0 + 1)
         counts.append(s1 - s0)

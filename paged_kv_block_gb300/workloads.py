@@ -271,12 +271,28 @@ def make_prefill_problem(seed, q_lens, prefix_lens, Hq, Hkv, D, page_size, *, ma
 # ----------------------------------------------------------------------------------------
 
 def make_decode_problem(seed, seq_lens, Hq, Hkv, D, page_size, *, combined=True, spare_frac=0.10,
-                        mask_type="dense", window_left=-1, bmm2_scale=1.0):
-    """Single-token decode: query [B, Hq, D]; CSR page table; combined or separate cache."""
+                        mask_type="dense", window_left=-1, bmm2_scale=1.0, seq_len_q=1,
+                        q_lens=None):
+    """Decode over a CSR page table, combined or separate cache.  Queries: [B, Hq, D] for
+    one query per request; [B, SQ, Hq, D] for seq_len_q = SQ > 1; packed [total_q, Hq, D]
+    with qo_indptr when q_lens (queries of each request) is given."""
     gen = _gen(seed)
     seq_lens = [int(x) for x in seq_lens]
     B = len(seq_lens)
-    q = _normal_bf16(gen, (B, Hq, D))
+    if q_lens is not None:
+        q_lens = [int(x) for x in q_lens]
+        if len(q_lens) != B or min(q_lens, default=1) < 1:
+            raise ValueError("q_lens needs one positive count per request")
+        q = _normal_bf16(gen, (sum(q_lens), Hq, D))
+        qo = torch.zeros(B + 1, dtype=torch.int32)
+        qo[1:] = torch.cumsum(torch.tensor(q_lens, dtype=torch.int64), 0).to(torch.int32)
+        sq, max_sq = 1, max(q_lens, default=1)
+    elif seq_len_q > 1:
+        q = _normal_bf16(gen, (B, seq_len_q, Hq, D))
+        qo, sq, max_sq = None, int(seq_len_q), int(seq_len_q)
+    else:
+        q = _normal_bf16(gen, (B, Hq, D))
+        qo, sq, max_sq = None, 1, 1
     pools = make_page_pools(gen, seq_lens, Hkv, D, page_size, None, combined, spare_frac)
     kv_indptr, kv_indices = _csr(pools["pages"])
     prob = dict(form="decode", q=q, kv_indptr=kv_indptr, kv_indices=kv_indices,
@@ -284,6 +300,8 @@ def make_decode_problem(seed, seq_lens, Hq, Hkv, D, page_size, *, combined=True,
                 max_seq_len=max(seq_lens) if seq_lens else 1, page_size=page_size,
                 mask_type=mask_type, window_left=int(window_left),
                 sm_scale=1.0 / math.sqrt(D), bmm2_scale=float(bmm2_scale),
+                seq_len_q=sq, qo_indptr=qo, max_seq_len_q=max_sq,
+                q_lens=q_lens if q_lens is not None else [sq] * B,
                 num_pages=pools["num_pages"], spare_pages=pools["spare"])
     if combined:
         prob["kv_cache"] = pools["kv_cache"]

@@ -157,3 +157,44 @@ def qsa_bruteforce(prob):
             o, s = _softmax_row(_vec(q[t, h].float()), keys, vals, prob["scale"])
             O[t, h], LSE[h, t] = o, s
     return O, LSE
+
+
+def decode_visible(prob, b, i):
+    """Visible keys of query i of request b in a decode problem (one, fixed or packed
+    queries): the query sits at len - nq + i."""
+    nq = int(prob["q_lens"][b])
+    L = int(prob["seq_lens"][b])
+    p = L - nq + i
+    w = prob["window_left"]
+    out = []
+    for j in range(L):
+        if prob["mask_type"] == "causal":
+            if j > p:
+                continue
+            if w >= 0 and j < p - w:
+                continue
+        out.append(j)
+    return out
+
+
+def decode_bruteforce(prob):
+    """O and LSE in the query's own layout ([B, Hq, D], [B, SQ, Hq, D] or packed)."""
+    q = prob["q"]
+    Hq, D = q.shape[-2], q.shape[-1]
+    Hkv = (prob["k_cache"] if "k_cache" in prob else prob["kv_cache"][:, 0]).shape[1]
+    G = Hq // Hkv
+    qrows = q.reshape(-1, Hq, D)
+    O = np.zeros((qrows.shape[0], Hq, D))
+    LSE = np.zeros((qrows.shape[0], Hq))
+    row = 0
+    for b in range(len(prob["seq_lens"])):
+        for i in range(int(prob["q_lens"][b])):
+            js = decode_visible(prob, b, i)
+            for h in range(Hq):
+                keys = [_kv_row(prob, b, j, h // G, "k") for j in js]
+                vals = [_kv_row(prob, b, j, h // G, "v") for j in js]
+                o, s = _softmax_row(_vec(qrows[row, h].float()), keys, vals, prob["sm_scale"],
+                                    prob["bmm2_scale"])
+                O[row, h], LSE[row, h] = o, s
+            row += 1
+    return O.reshape(tuple(q.shape)), LSE.reshape(tuple(q.shape[:-1]))

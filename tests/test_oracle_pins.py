@@ -53,7 +53,8 @@ def _run_decode(p, **kw):
                           kv_cache=p.get("kv_cache"), k_cache=p.get("k_cache"),
                           v_cache=p.get("v_cache"), bmm1_scale=p["sm_scale"],
                           bmm2_scale=p["bmm2_scale"], mask_type=p["mask_type"],
-                          window_left=p["window_left"], **kw)
+                          window_left=p["window_left"], seq_len_q=p.get("seq_len_q", 1),
+                          qo_indptr=p.get("qo_indptr"), **kw)
 
 
 def _run_qsa(p, **kw):
@@ -90,6 +91,26 @@ def test_prefill_matches_bruteforce(seed, mask, window, oscale):
                                output_scale=oscale)
     o, s = _run_prefill(p)
     ob, sb = BF.prefill_bruteforce(p)
+    _close(o, ob)
+    _close(s, sb)
+
+
+@pytest.mark.parametrize("seed,kw", [
+    (5, dict(seq_lens=[9, 14], mask_type="dense")),
+    (6, dict(seq_lens=[9, 14], mask_type="causal", window_left=3, combined=False)),
+    (7, dict(seq_lens=[7, 12], seq_len_q=3, mask_type="causal")),
+    (8, dict(seq_lens=[7, 12], seq_len_q=3, mask_type="dense", bmm2_scale=0.5)),
+    (9, dict(seq_lens=[5, 13, 6], q_lens=[1, 4, 2], mask_type="causal", window_left=2)),
+    (10, dict(seq_lens=[2, 10], q_lens=[3, 1], mask_type="causal", combined=False)),
+])
+def test_decode_matches_bruteforce(seed, kw):
+    """One, fixed and packed query layouts; request 0 of the last case has more queries
+    than keys, so its first query sits before the first key and sees nothing."""
+    kw = dict(kw)
+    lens = kw.pop("seq_lens")
+    p = W.make_decode_problem(seed, lens, Hq=4, Hkv=2, D=8, page_size=4, **kw)
+    o, s = _run_decode(p)
+    ob, sb = BF.decode_bruteforce(p)
     _close(o, ob)
     _close(s, sb)
 
@@ -415,6 +436,60 @@ def test_zero_query_counts_visible_keys():
         _close(s[:, t], [math.log(n) if n else -math.inf] * 2, 1e-14)
 
 
+def test_zero_query_decode_counts_visible_keys():
+    """q = 0 in multi-query decode: LSE = log of the number of visible keys, which for query
+    i of nq at position p = L - nq + i is min(p, L - 1) + 1 - max(0, p - w) under the causal
+    mask (L without it)."""
+    lens, q_lens, w = [11, 6, 20], [3, 6, 1], 4
+    for mask, win in (("causal", -1), ("causal", w), ("dense", -1)):
+        p = W.make_decode_problem(34, lens, Hq=2, Hkv=1, D=8, page_size=4, q_lens=q_lens,
+                                  mask_type=mask, window_left=win)
+        p["q"] = torch.zeros_like(p["q"])
+        _, s = _run_decode(p)
+        row = 0
+        for L, nq in zip(lens, q_lens):
+            for i in range(nq):
+                pos = L - nq + i
+                if mask == "causal":
+                    n = min(pos, L - 1) + 1 - (max(0, pos - win) if win >= 0 else 0)
+                else:
+                    n = L
+                _close(s[row], [math.log(n) if n > 0 else -math.inf] * 2, 1e-14)
+                row += 1
+
+
+def test_multi_query_decode_equals_prefill():
+    """Decode with packed queries over a CSR table and prefill over the same pages as a
+    row-strided table are the same computation."""
+    lens, q_lens = [23, 9, 31], [4, 9, 2]
+    p = W.make_decode_problem(35, lens, Hq=4, Hkv=2, D=16, page_size=8, q_lens=q_lens,
+                              mask_type="causal", window_left=5, combined=False,
+                              bmm2_scale=1.25)
+    o_dec, s_dec = _run_decode(p)
+    C = max(-(-L // 8) for L in lens)
+    tables = torch.zeros(len(lens), C, dtype=torch.int32)
+    for b in range(len(lens)):
+        pg = p["kv_indices"][int(p["kv_indptr"][b]):int(p["kv_indptr"][b + 1])]
+        tables[b, :len(pg)] = pg
+    o_pre, s_pre = A.batch_prefill(p["q"], p["k_cache"], p["v_cache"], p["qo_indptr"], tables,
+                                   p["seq_lens"], mask_type="causal", window_left=5,
+                                   sm_scale=p["sm_scale"], output_scale=1.25)
+    _close(o_dec, o_pre, 0)
+    _close(s_dec, s_pre, 0)
+
+
+def test_fixed_and_packed_decode_layouts_agree():
+    lens = [17, 5]
+    p = W.make_decode_problem(36, lens, Hq=4, Hkv=1, D=8, page_size=4, seq_len_q=3,
+                              mask_type="causal", window_left=6)
+    o_fix, s_fix = _run_decode(p)
+    packed = dict(p, q=p["q"].reshape(6, 4, 8), seq_len_q=1,
+                  qo_indptr=torch.tensor([0, 3, 6], dtype=torch.int32))
+    o_pk, s_pk = _run_decode(packed)
+    _close(o_fix.reshape(6, 4, 8), o_pk, 0)
+    _close(s_fix.reshape(6, 4), s_pk, 0)
+
+
 def test_single_and_duplicate_keys():
     q = np.array([[[0.5, -1.0, 2.0]]])
     K = np.array([[1.0, 2.0, 3.0], [1.0, 2.0, 3.0], [4.0, 0.0, 1.0]])
@@ -446,6 +521,26 @@ def test_planted_causal_off_by_one_is_caught(monkeypatch):
     monkeypatch.setattr(A, "masked_softmax_attention", shifted)
     o, _ = _run_prefill(p)
     assert np.abs(o - ref_o).max() > 1e-3
+
+
+def test_planted_top_left_decode_alignment_is_caught(monkeypatch):
+    """Placing multi-query decode queries at positions 0..nq-1 (top-left) instead of the
+    last nq positions must disagree with the brute force."""
+    p = W.make_decode_problem(43, [10], Hq=2, Hkv=1, D=8, page_size=4, seq_len_q=3,
+                              mask_type="causal")
+    ob, _ = BF.decode_bruteforce(p)
+    o, _ = _run_decode(p)
+    _close(o, ob)
+    real = A.masked_softmax_attention
+
+    def top_left(q, keys, vals, visible, scale, out_scale=1.0):
+        n, L = visible.shape
+        vis = np.arange(L)[None, :] <= np.arange(n)[:, None]
+        return real(q, keys, vals, vis, scale, out_scale)
+
+    monkeypatch.setattr(A, "masked_softmax_attention", top_left)
+    o2, _ = _run_decode(p)
+    assert np.abs(o2 - ob).max() > 1e-3
 
 
 def test_planted_gqa_mapping_is_caught():

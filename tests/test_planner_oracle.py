@@ -77,6 +77,27 @@ def test_decode_splits_partition_the_visible_keys():
                     assert np.all(rows[1:, 2] % chunk == 0)
 
 
+def test_multi_query_decode_splits_cover_the_visible_union():
+    """With nq queries per request the splits of (b, g) tile exactly the keys that at least
+    one query of b sees (the brute-force visibility rule), cut at chunk multiples."""
+    lens, q_lens = [1, 6, 130, 300, 1000, 2], [1, 6, 3, 8, 16, 2]
+    for mask, w in (("dense", -1), ("causal", -1), ("causal", 0), ("causal", 100)):
+        prob = dict(q_lens=q_lens, seq_lens=lens, mask_type=mask, window_left=w)
+        for chunk in (128, 256):
+            off, items = PL.plan_decode(lens, 2, chunk, w, q_lens=q_lens)
+            for b, L in enumerate(lens):
+                seen = sorted(set(j for i in range(q_lens[b])
+                                  for j in BF.decode_visible(prob, b, i)))
+                n = off[b + 1] - off[b]
+                for g in range(2):
+                    rows = items[2 * off[b] + g * n: 2 * off[b] + (g + 1) * n]
+                    assert rows[0, 2] == seen[0] and rows[-1, 3] == seen[-1] + 1
+                    assert seen == list(range(seen[0], seen[-1] + 1))
+                    assert np.all(rows[1:, 2] == rows[:-1, 3])
+                    assert np.all(rows[1:, 2] % chunk == 0)
+                    assert np.all(rows[:, 3] - rows[:, 2] <= chunk)
+
+
 def test_decode_chunk_formula():
     # floor(64 * 8 * 64 / (16 * 152)) = 13 tiles of 128 keys
     assert PL.decode_split_chunk(64, 8, 8192, 152) == 1664
