@@ -7,8 +7,8 @@
  *     attention over packed K/V   -> paged_attn_plan / paged_attn_run
  *   - packed-Q dense / causal / sliding-window prefill over separate HND page pools with
  *     a row-strided page table   -> paged_prefill_run
- *   - single-token decode over a CSR-paged cache with split-KV partials and a merge
- *                                  -> paged_decode_run
+ *   - decode over a CSR-paged cache (one, SQ fixed or packed queries per request) with
+ *     split-KV partials and a merge -> paged_decode_run
  * The operations are those of the FlashInfer API pages
  *   [BSA] flashinfer.attention.prims_ts.block_sparse_attention_with_paged_kv_cache
  *   [PRE] flashinfer.attention.prims_ts.batch_prefill_with_paged_kv_cache
@@ -183,7 +183,7 @@ int paged_prefill_run(const paged_prefill_params* params, const void* q_dev,
                       const int32_t* seq_lens_kv_dev, void* out_dev, float* lse_dev,
                       void* workspace_dev, size_t workspace_bytes, void* stream);
 
-/* ---- [DEC] single-token decode with split-KV ----------------------------------------- */
+/* ---- [DEC] decode with split-KV --------------------------------------------------------- */
 typedef struct paged_decode_params {
   int batch;            /* B                                                              */
   int num_qo_heads, num_kv_heads, head_dim; /* D = 128; G = Hq / Hkv <= 16                */
@@ -192,11 +192,20 @@ typedef struct paged_decode_params {
   int combined_cache;   /* 1: [P, 2, Hkv, ps, D]; 0: separate K and V pools                */
   int max_seq_len;      /* static bound on seq_lens, <= 2147483520 ([DEC] max_seq_len)   */
   int mask_type;        /* PAGED_ATTN_MASK_*; with one query both keep every live key     */
-  int window_left;      /* -1 = no window; w >= 0 (causal) keeps keys j >= len - 1 - w    */
+  int window_left;      /* -1 = no window; w >= 0 (causal) keeps keys j >= p - w for the
+                           query at position p = len - nq + i                            */
   float bmm1_scale;     /* softmax scale; <= 0 selects 1/sqrt(D)                          */
   float bmm2_scale;     /* multiplies the normalised output ([DEC] bmm2_scale)             */
   int split_chunk;      /* keys per split-KV partition, a multiple of 128; 0 = automatic:
                            128 * max(1, B * Hkv * ceil(max_seq_len / 128) / (16 * SMs))     */
+  /* Query layout ([DEC] seq_len_q, qo_indptr, max_seq_len_q).  Zero-initialised fields give
+   * one query per request, query [B, Hq, D]. */
+  int seq_len_q;        /* fixed form: SQ queries per request; SQ > 1 gives token-major
+                           query / out [B, SQ, Hq, D] and LSE [B, SQ, Hq]                 */
+  int max_seq_len_q;    /* > 0 selects the packed form: paged_decode_run takes qo_indptr,
+                           query / out are [total_q, Hq, D], and every request has between
+                           1 and max_seq_len_q queries (the static bound of [DEC])         */
+  int total_q;          /* packed form: rows of query and out, = qo_indptr[B]              */
 } paged_decode_params;
 
 /* Workspace bytes for the decode plan and the fp32 split partials. */
@@ -207,17 +216,27 @@ size_t paged_decode_workspace_size(const paged_decode_params* params);
 int paged_decode_split_chunk(const paged_decode_params* params);
 
 /* Plan (split-KV work list), run the partial kernel and merge ([DEC] signature).
- *   query_dev [B, Hq, D]; k_dev: combined cache or K pool; v_dev: V pool or NULL;
+ *   query_dev: [B, Hq, D] (one query per request), [B, SQ, Hq, D] (seq_len_q = SQ > 1) or
+ *   [total_q, Hq, D] (packed form); k_dev: combined cache or K pool; v_dev: V pool or NULL;
  *   kv_indptr_dev [B + 1], kv_indices_dev: CSR page ids ([DEC] notes: indptr starts at 0,
  *   ends at the number of indices, and each request owns ceil(len / page_size) entries);
- *   seq_lens_dev [B] (1 <= len <= max_seq_len); out_dev [B, Hq, D] bf16;
- *   lse_dev [B, Hq] fp32 (optional).
+ *   seq_lens_dev [B] (1 <= len <= max_seq_len);
+ *   qo_indptr_dev [B + 1]: packed form only (NULL otherwise); request b owns query rows
+ *   qo_indptr[b] .. qo_indptr[b + 1]; the offsets start at 0, each step is between 1 and
+ *   max_seq_len_q, and they end at total_q ([DEC] notes; a plan that sees them break
+ *   this sets the metadata status bit and rows outside [0, total_q) are never written);
+ *   out_dev: bf16 in the query's layout; lse_dev: fp32, one per output row and head
+ *   (optional).
+ * Under the causal mask every request needs nq <= len ([DEC] notes); a query before the
+ * first key sees nothing and gets 0 / -inf.  A (request, KV head) unit of at most 64 rows
+ * (G x queries) runs on the split-KV decode kernel; larger units run as dense tiles on the
+ * tensor-core kernel (the prefill kernel over the CSR table), no split-KV workspace used.
  * The workspace is exclusive to one launch in flight ([DEC] notes on workspace_buffer). */
 int paged_decode_run(const paged_decode_params* params, const void* query_dev,
                      const void* k_dev, const void* v_dev, const int32_t* kv_indptr_dev,
                      const int32_t* kv_indices_dev, const int32_t* seq_lens_dev,
-                     void* out_dev, float* lse_dev, void* workspace_dev,
-                     size_t workspace_bytes, void* stream);
+                     const int32_t* qo_indptr_dev, void* out_dev, float* lse_dev,
+                     void* workspace_dev, size_t workspace_bytes, void* stream);
 
 /* Decode without a workspace argument.  The pages describe no counterpart of this entry
  * point; it exists for callers that cannot allocate device memory at call time (code inside
@@ -238,7 +257,8 @@ int paged_decode_run(const paged_decode_params* params, const void* query_dev,
 int paged_decode_run_static(const paged_decode_params* params, const void* query_dev,
                             const void* k_dev, const void* v_dev, const int32_t* kv_indptr_dev,
                             const int32_t* kv_indices_dev, const int32_t* seq_lens_dev,
-                            void* out_dev, float* lse_dev, void* stream);
+                            const int32_t* qo_indptr_dev, void* out_dev, float* lse_dev,
+                            void* stream);
 
 /* ---- plan inspection -------------------------------------------------------------------- */
 

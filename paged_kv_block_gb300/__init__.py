@@ -64,7 +64,8 @@ class DecodeParams(C.Structure):
                 ("head_dim", C.c_int), ("page_size", C.c_int), ("num_pages", C.c_int),
                 ("combined_cache", C.c_int), ("max_seq_len", C.c_int), ("mask_type", C.c_int),
                 ("window_left", C.c_int), ("bmm1_scale", C.c_float), ("bmm2_scale", C.c_float),
-                ("split_chunk", C.c_int)]
+                ("split_chunk", C.c_int), ("seq_len_q", C.c_int), ("max_seq_len_q", C.c_int),
+                ("total_q", C.c_int)]
 
 
 class PlanLayout(C.Structure):
@@ -92,12 +93,12 @@ _EXPORTS = {
                           + [C.c_size_t, C.c_void_p]),
     "paged_decode_workspace_size": (C.c_size_t, [C.POINTER(DecodeParams)]),
     "paged_decode_split_chunk": (C.c_int, [C.POINTER(DecodeParams)]),
-    "paged_decode_run": (C.c_int, [C.POINTER(DecodeParams)] + [C.c_void_p] * 9
+    "paged_decode_run": (C.c_int, [C.POINTER(DecodeParams)] + [C.c_void_p] * 10
                          + [C.c_size_t, C.c_void_p]),
     "paged_attn_plan_layout_of": (C.c_int, [C.POINTER(AttnParams), C.POINTER(PlanLayout)]),
     "paged_prefill_plan_layout_of": (C.c_int, [C.POINTER(PrefillParams), C.POINTER(PlanLayout)]),
     "paged_decode_plan_layout_of": (C.c_int, [C.POINTER(DecodeParams), C.POINTER(PlanLayout)]),
-    "paged_decode_run_static": (C.c_int, [C.POINTER(DecodeParams)] + [C.c_void_p] * 9),
+    "paged_decode_run_static": (C.c_int, [C.POINTER(DecodeParams)] + [C.c_void_p] * 10),
     "paged_attn_workspace_status": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(C.c_uint32)]),
     "paged_attn_strerror": (C.c_char_p, [C.c_int]),
     "paged_attn_kernel_timer": (C.c_int, [C.c_int]),
@@ -220,10 +221,12 @@ def paged_decode_split_chunk(params: DecodeParams) -> int:
 
 
 def paged_decode_run(params: DecodeParams, query, k, v, kv_indptr, kv_indices, seq_lens, out,
-                     lse, workspace, stream=None) -> None:
+                     lse, workspace, stream=None, qo_indptr=None) -> None:
+    """qo_indptr: packed query offsets (params.max_seq_len_q > 0), else None."""
     _check(lib().paged_decode_run(C.byref(params), _dev(query, "query"), _dev(k, "k"),
                                   _dev(v, "v"), _dev(kv_indptr, "kv_indptr"),
                                   _dev(kv_indices, "kv_indices"), _dev(seq_lens, "seq_lens"),
+                                  _dev(qo_indptr, "qo_indptr"),
                                   _dev(out, "out"), _dev(lse, "lse"),
                                   _dev(workspace, "workspace"),
                                   workspace.numel() * workspace.element_size(), _stream(stream)),
@@ -242,13 +245,14 @@ def plan_layout(params) -> PlanLayout:
 
 
 def paged_decode_run_static(params: DecodeParams, query, k, v, kv_indptr, kv_indices, seq_lens,
-                            out, lse, stream=None) -> None:
+                            out, lse, stream=None, qo_indptr=None) -> None:
     """paged_decode_run for callers that cannot allocate: the scratch is a fixed array
     inside the library (see the C header for its size and the sharing rules)."""
     _check(lib().paged_decode_run_static(C.byref(params), _dev(query, "query"), _dev(k, "k"),
                                          _dev(v, "v"), _dev(kv_indptr, "kv_indptr"),
                                          _dev(kv_indices, "kv_indices"),
-                                         _dev(seq_lens, "seq_lens"), _dev(out, "out"),
+                                         _dev(seq_lens, "seq_lens"),
+                                         _dev(qo_indptr, "qo_indptr"), _dev(out, "out"),
                                          _dev(lse, "lse"), _stream(stream)),
            "paged_decode_run_static")
 
@@ -376,34 +380,55 @@ def batch_prefill_with_paged_kv_cache(q, k_cache, v_cache, qo_indptr, block_tabl
 
 
 def decode_params(query, kv_cache, max_seq_len, *, bmm1_scale=None, bmm2_scale=1.0,
-                  mask_type="dense", window_left=-1, split_chunk=0) -> DecodeParams:
-    B, Hq, D = query.shape
+                  mask_type="dense", window_left=-1, split_chunk=0, seq_len_q=1,
+                  qo_indptr=None, max_seq_len_q=None) -> DecodeParams:
+    """Static arguments of a decode call.  query is [B, Hq, D] (one query per request),
+    [B, SQ, Hq, D] (seq_len_q = SQ > 1) or packed [total_q, Hq, D] with qo_indptr, whose
+    static bound max_seq_len_q is then required."""
     _, _, combined, Hkv, ps, P, _ = _pools(kv_cache)
+    sq, max_sq, total_q = 1, 0, 0
+    if qo_indptr is not None:
+        if max_seq_len_q is None:
+            raise ValueError("the packed form needs max_seq_len_q")
+        total_q, Hq, D = query.shape
+        B = qo_indptr.numel() - 1
+        max_sq = int(max_seq_len_q)
+    elif seq_len_q > 1:
+        B, sq, Hq, D = query.shape
+        if sq != seq_len_q:
+            raise ValueError("query.shape[1] must equal seq_len_q")
+    else:
+        B, Hq, D = query.shape
     return DecodeParams(batch=B, num_qo_heads=Hq, num_kv_heads=Hkv, head_dim=D, page_size=ps,
                         num_pages=P, combined_cache=combined, max_seq_len=int(max_seq_len),
                         mask_type=MASK[mask_type], window_left=int(window_left),
                         bmm1_scale=float(bmm1_scale or 0.0), bmm2_scale=float(bmm2_scale),
-                        split_chunk=int(split_chunk))
+                        split_chunk=int(split_chunk), seq_len_q=int(sq), max_seq_len_q=max_sq,
+                        total_q=int(total_q))
 
 
 def batch_decode_with_paged_kv_cache(query, kv_cache, workspace_buffer, paged_kv_indptr,
-                                     paged_kv_indices, seq_lens, max_seq_len, *,
-                                     bmm1_scale=None, bmm2_scale=1.0, out=None, lse=None,
-                                     mask_type="dense", window_left=-1, kv_layout="HND",
-                                     split_chunk=0, stream=None):
-    """Single-token decode with split-KV; returns (out, lse)."""
+                                     paged_kv_indices, seq_lens, max_seq_len, *, seq_len_q=1,
+                                     qo_indptr=None, max_seq_len_q=None, bmm1_scale=None,
+                                     bmm2_scale=1.0, out=None, lse=None, mask_type="dense",
+                                     window_left=-1, kv_layout="HND", split_chunk=0,
+                                     stream=None):
+    """Decode with split-KV over a CSR page table; returns (out, lse).  One query per
+    request ([B, Hq, D]), seq_len_q fixed queries ([B, SQ, Hq, D]) or packed queries
+    ([total_q, Hq, D] with qo_indptr and its bound max_seq_len_q)."""
     if kv_layout != "HND":
         raise ValueError("only the HND layout is supported")
     params = decode_params(query, kv_cache, max_seq_len, bmm1_scale=bmm1_scale,
                            bmm2_scale=bmm2_scale, mask_type=mask_type, window_left=window_left,
-                           split_chunk=split_chunk)
+                           split_chunk=split_chunk, seq_len_q=seq_len_q, qo_indptr=qo_indptr,
+                           max_seq_len_q=max_seq_len_q)
     k, v, *_ = _pools(kv_cache)
     if out is None:
         out = torch.empty_like(query)
     if workspace_buffer is None:
         workspace_buffer = _workspace(paged_decode_workspace_size(params), query.device)
     paged_decode_run(params, query, k, v, paged_kv_indptr, paged_kv_indices, seq_lens, out, lse,
-                     workspace_buffer, stream)
+                     workspace_buffer, stream, qo_indptr=qo_indptr)
     return out, lse
 
 

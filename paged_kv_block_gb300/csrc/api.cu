@@ -168,10 +168,23 @@ PrefillLayout prefill_layout(const paged_prefill_params* p) {
 }
 
 // ---- decode layout ------------------------------------------------------------------------
+// Rows of one (request, KV head) unit: G x (queries per request).  Up to kDecodeMaxRows the
+// split-KV decode kernel runs; beyond, the work is prefill-shaped and runs as dense tiles of
+// the tensor-core kernel over the CSR page table.
+constexpr int kDecodeMaxRows = 64;
+
 struct DecodeLayout {
-  size_t status, split_off, counters, items, part_lse, part_o, total;
+  size_t status, split_off, counters, items, part_lse, part_o;   // split-KV route
+  size_t n_tiles, tile_off, tmp, sorted, hist, offs;             // tile route
+  size_t total;
   int capacity, chunk, max_splits;
+  int q_per_item, q_rows, rows, tiled, max_cost, tile_tokens;
 };
+
+bool decode_packed(const paged_decode_params* p) { return p->max_seq_len_q > 0; }
+int decode_q_per_item(const paged_decode_params* p) {
+  return decode_packed(p) ? p->max_seq_len_q : (p->seq_len_q > 1 ? p->seq_len_q : 1);
+}
 
 bool decode_params_ok(const paged_decode_params* p) {
   if (!p) return false;
@@ -186,9 +199,19 @@ bool decode_params_ok(const paged_decode_params* p) {
   if (p->window_left < -1) return false;
   if (p->window_left >= 0 && p->mask_type != PAGED_ATTN_MASK_CAUSAL) return false;
   if (p->split_chunk < 0 || p->split_chunk % 128) return false;
+  if (p->seq_len_q < 0 || p->max_seq_len_q < 0 || p->total_q < 0) return false;
+  if (decode_packed(p)) {
+    if (p->seq_len_q > 1) return false;                    // one form at a time
+    if (p->total_q < p->batch) return false;               // every request owns >= 1 row
+    if (static_cast<long long>(p->batch) * p->max_seq_len_q < p->total_q) return false;
+  } else if (static_cast<long long>(p->batch) * decode_q_per_item(p) >= (1LL << 31)) {
+    return false;
+  }
   const long long rows = static_cast<long long>(p->num_pages) * (p->combined_cache ? 2 : 1) *
                          p->num_kv_heads * p->page_size;
   if (rows >= (1LL << 31)) return false;
+  if (static_cast<long long>(G) * decode_q_per_item(p) > kDecodeMaxRows && G * 2 > kMTileRows)
+    return false;
   return true;
 }
 
@@ -205,16 +228,36 @@ DecodeLayout decode_layout(const paged_decode_params* p) {
   DecodeLayout s{};
   Layout l;
   const int G = p->num_qo_heads / p->num_kv_heads;
+  s.q_per_item = decode_q_per_item(p);
+  s.q_rows = decode_packed(p) ? p->total_q : p->batch * s.q_per_item;
+  const long long rows = static_cast<long long>(G) * s.q_per_item;
+  s.tiled = rows > kDecodeMaxRows;
+  s.rows = s.tiled ? 0 : static_cast<int>(rows);
   s.chunk = decode_chunk(p);
-  s.max_splits = static_cast<int>(ceil_div_ll(p->max_seq_len, s.chunk));
-  if (s.max_splits < 1) s.max_splits = 1;
-  s.capacity = static_cast<int>(static_cast<long long>(p->batch) * p->num_kv_heads * s.max_splits);
   s.status = l.take(sizeof(uint32_t) * 4);
-  s.split_off = l.take(sizeof(int) * static_cast<size_t>(p->batch + 1));
-  s.counters = l.take(sizeof(int) * (static_cast<size_t>(p->batch) * p->num_kv_heads + 1));
-  s.items = l.take(sizeof(SplitItem) * static_cast<size_t>(s.capacity > 0 ? s.capacity : 1));
-  s.part_lse = l.take(sizeof(float) * static_cast<size_t>(s.capacity) * G + 4);
-  s.part_o = l.take(sizeof(float) * static_cast<size_t>(s.capacity) * G * p->head_dim + 4);
+  if (!s.tiled) {
+    s.max_splits = static_cast<int>(ceil_div_ll(p->max_seq_len, s.chunk));
+    if (s.max_splits < 1) s.max_splits = 1;
+    s.capacity = static_cast<int>(static_cast<long long>(p->batch) * p->num_kv_heads * s.max_splits);
+    s.split_off = l.take(sizeof(int) * static_cast<size_t>(p->batch + 1));
+    s.counters = l.take(sizeof(int) * (static_cast<size_t>(p->batch) * p->num_kv_heads + 1));
+    s.items = l.take(sizeof(SplitItem) * static_cast<size_t>(s.capacity > 0 ? s.capacity : 1));
+    s.part_lse = l.take(sizeof(float) * static_cast<size_t>(s.capacity) * s.rows + 4);
+    s.part_o = l.take(sizeof(float) * static_cast<size_t>(s.capacity) * s.rows * p->head_dim + 4);
+  } else {
+    s.n_tiles = s.status + sizeof(uint32_t);
+    s.tile_tokens = cta_tile_tokens(G);
+    s.capacity = static_cast<int>(static_cast<long long>(p->num_kv_heads) *
+                                  (ceil_div(s.q_rows, s.tile_tokens) + p->batch));
+    const long long mc = ceil_div_ll(p->max_seq_len, kKvTile);
+    s.max_cost = static_cast<int>(mc < kMaxSortCost ? mc : kMaxSortCost);
+    s.tile_off = l.take(sizeof(int) * static_cast<size_t>(p->batch + 1));
+    s.tmp = l.take(sizeof(TileRec) * static_cast<size_t>(s.capacity > 0 ? s.capacity : 1));
+    s.sorted = l.take(sizeof(TileRec) * static_cast<size_t>(s.capacity > 0 ? s.capacity : 1));
+    const size_t ints = tile_sort_scratch_ints(s.capacity, s.max_cost);
+    s.hist = l.take(ints * sizeof(int));
+    s.offs = l.take(ints * sizeof(int));
+  }
   s.total = l.off;
   return s;
 }
@@ -303,6 +346,78 @@ void timer_end(cudaStream_t st, void* token) {
 int launch_qsa(const paged_attn_params* p, const paged_attn_meta* m, const void* q,
                const void* k, const void* v, void* out, float* out_fp32, float* lse,
                const int* indptr, const int* indices, uint32_t* status, cudaStream_t st);
+
+namespace {
+
+// Decode whose (request, KV head) units exceed kDecodeMaxRows rows: the dense tile planner
+// and the tensor-core kernel, with the decode page table (CSR) and query layout.
+int decode_run_tiled(const paged_decode_params* p, const DecodeLayout& s, const void* query,
+                     const void* k, const void* v, const int32_t* kv_indptr,
+                     const int32_t* kv_indices, const int32_t* seq_lens,
+                     const int32_t* qo_indptr, void* out, float* lse, void* ws,
+                     cudaStream_t st) {
+  const int Hq = p->num_qo_heads, Hkv = p->num_kv_heads, G = Hq / Hkv, D = p->head_dim;
+  const int ps = p->page_size;
+  const int causal = p->mask_type == PAGED_ATTN_MASK_CAUSAL;
+  const int q_len = qo_indptr ? 0 : s.q_per_item;
+  uint32_t* status = at<uint32_t>(ws, s.status);
+  int* n_tiles = at<int>(ws, s.n_tiles);
+  TileRec* tmp = at<TileRec>(ws, s.tmp);
+  TileRec* sorted = at<TileRec>(ws, s.sorted);
+  launch_prefill_tiles(qo_indptr, q_len, seq_lens, p->batch, Hkv, s.tile_tokens, causal,
+                       p->window_left, s.capacity, at<int>(ws, s.tile_off), n_tiles, tmp, status,
+                       st);
+  launch_tile_sort(tmp, sorted, n_tiles, 0, s.capacity, s.max_cost, at<int>(ws, s.hist),
+                   at<int>(ws, s.offs), st);
+  const float scale =
+      p->bmm1_scale > 0.f ? p->bmm1_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  AttnLaunch a{};
+  const int R = page_piece_rows(ps, kKvTile);
+  const long long pool_rows = static_cast<long long>(p->num_pages) * (p->combined_cache ? 2 : 1) *
+                              Hkv * ps;
+  if (!encode_q_map(&a.qmap, query, s.q_rows, Hq, D, G, sub_tile_tokens(G)) ||
+      !encode_rows_map(&a.kmap, k, pool_rows, D, R) ||
+      !encode_rows_map(&a.vmap, p->combined_cache ? k : v, pool_rows, D, R))
+    return PAGED_ATTN_ERR_CUDA;
+  a.tiles = sorted;
+  a.n_tiles = n_tiles;
+  a.capacity = s.capacity;
+  a.pt = kv_indices;
+  a.pt_indptr = kv_indptr;
+  a.pt_stride = 0;
+  a.seq_lens = seq_lens;
+  a.qo_indptr = qo_indptr;
+  a.q_len = q_len;
+  a.valid_bits = nullptr;
+  a.valid_words = 0;
+  a.block_sparse = 0;
+  a.block_indices = nullptr;
+  a.kv_block_size = kKvTile;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.status = status;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = G;
+  a.D = D;
+  a.page_size = ps;
+  a.page_rows = (p->combined_cache ? 2 : 1) * Hkv * ps;
+  a.k_head_off = 0;
+  a.v_head_off = p->combined_cache ? Hkv * ps : 0;
+  a.num_pages = p->num_pages;
+  a.causal = causal;
+  a.window_left = p->window_left;
+  a.scale_log2 = scale * kLog2e;
+  a.out_scale = p->bmm2_scale;
+  void* tok;
+  timer_begin(st, &tok);
+  const int rc = launch_attn(a, st);
+  timer_end(st, tok);
+  if (rc == -2) return PAGED_ATTN_ERR_UNSUPPORTED;
+  return rc == 0 ? PAGED_ATTN_OK : PAGED_ATTN_ERR_CUDA;
+}
+
+}  // namespace
 
 }  // namespace pa
 
@@ -432,7 +547,7 @@ int paged_attn_run(const paged_attn_params* p, const paged_attn_meta* m, const v
   const int Hq = p->num_qo_heads, Hkv = p->num_kv_heads, G = Hq / Hkv, ps = p->page_size;
   AttnLaunch a{};
   const int ck = attn_sub_chunk(p->kv_block_size, true);
-  const int R = ck < ps ? ck : ps;
+  const int R = page_piece_rows(ps, ck);
   const long long pool_rows = static_cast<long long>(p->num_pages) * (p->combined_cache ? 2 : 1) *
                               Hkv * ps;
   if (!encode_q_map(&a.qmap, q, static_cast<long long>(p->batch) * p->q_len, Hq, D, G,
@@ -504,13 +619,14 @@ int paged_prefill_run(const paged_prefill_params* p, const void* q, const void* 
   int* n_tiles = at<int>(ws, s.n_tiles);
   TileRec* tmp = at<TileRec>(ws, s.tmp);
   TileRec* sorted = at<TileRec>(ws, s.sorted);
-  launch_prefill_tiles(qo_indptr, seq_lens, p->batch, Hkv, s.tile_tokens, causal, p->window_left,
-                       s.capacity, at<int>(ws, s.tile_off), n_tiles, tmp, status, st);
+  launch_prefill_tiles(qo_indptr, 0, seq_lens, p->batch, Hkv, s.tile_tokens, causal,
+                       p->window_left, s.capacity, at<int>(ws, s.tile_off), n_tiles, tmp, status,
+                       st);
   launch_tile_sort(tmp, sorted, n_tiles, 0, s.capacity, s.max_cost, at<int>(ws, s.hist),
                    at<int>(ws, s.offs), st);
   const float scale = p->sm_scale > 0.f ? p->sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
   AttnLaunch a{};
-  const int R = ps < kKvTile ? ps : kKvTile;
+  const int R = page_piece_rows(ps, kKvTile);
   const long long pool_rows = static_cast<long long>(p->num_pages) * Hkv * ps;
   if (!encode_q_map(&a.qmap, q, p->total_q, Hq, D, G, sub_tile_tokens(G)) ||
       !encode_rows_map(&a.kmap, kc, pool_rows, D, R) || !encode_rows_map(&a.vmap, vc, pool_rows, D, R))
@@ -565,11 +681,12 @@ int paged_decode_split_chunk(const paged_decode_params* p) {
 
 int paged_decode_run(const paged_decode_params* p, const void* query, const void* k,
                      const void* v, const int32_t* kv_indptr, const int32_t* kv_indices,
-                     const int32_t* seq_lens, void* out, float* lse, void* ws, size_t ws_bytes,
-                     void* stream) {
+                     const int32_t* seq_lens, const int32_t* qo_indptr, void* out, float* lse,
+                     void* ws, size_t ws_bytes, void* stream) {
   if (!decode_params_ok(p) || !query || !k || !kv_indptr || !kv_indices || !seq_lens || !out)
     return PAGED_ATTN_ERR_INVALID_ARGUMENT;
   if (!p->combined_cache && !v) return PAGED_ATTN_ERR_INVALID_ARGUMENT;
+  if (decode_packed(p) != (qo_indptr != nullptr)) return PAGED_ATTN_ERR_INVALID_ARGUMENT;
   if (!aligned16(query) || !aligned16(k) || (v && !aligned16(v)) || !aligned16(out))
     return PAGED_ATTN_ERR_INVALID_ARGUMENT;
   const DecodeLayout s = decode_layout(p);
@@ -577,21 +694,25 @@ int paged_decode_run(const paged_decode_params* p, const void* query, const void
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* status = at<uint32_t>(ws, s.status);
   if (cudaMemsetAsync(status, 0, 4 * sizeof(uint32_t), st) != cudaSuccess) return PAGED_ATTN_ERR_CUDA;
-  if (p->batch == 0) return PAGED_ATTN_OK;
+  if (p->batch == 0 || s.q_rows == 0) return PAGED_ATTN_OK;
+  if (s.tiled)
+    return decode_run_tiled(p, s, query, k, v, kv_indptr, kv_indices, seq_lens, qo_indptr, out,
+                            lse, ws, st);
   const int Hkv = p->num_kv_heads, ps = p->page_size, D = p->head_dim;
+  const int G = p->num_qo_heads / Hkv;
   int* split_off = at<int>(ws, s.split_off);
   SplitItem* items = at<SplitItem>(ws, s.items);
   int* counters = at<int>(ws, s.counters);
-  launch_decode_plan(seq_lens, p->batch, Hkv, s.chunk, p->window_left, s.max_splits, split_off,
-                     items, counters, st);
-  const int R = ps < 64 ? ps : 64;
+  const int q_len = qo_indptr ? 0 : s.q_per_item;
+  launch_decode_plan(seq_lens, qo_indptr, q_len, s.q_per_item, s.q_rows, p->batch, Hkv, s.chunk,
+                     p->window_left, s.max_splits, split_off, items, counters, status, st);
+  const int R = page_piece_rows(ps, 64);
   const long long pool_rows = static_cast<long long>(p->num_pages) * (p->combined_cache ? 2 : 1) *
                               Hkv * ps;
   CUtensorMap kmap, vmap, qmap;
-  const int G = p->num_qo_heads / Hkv;
   if (!encode_rows_map(&kmap, k, pool_rows, D, R) ||
       !encode_rows_map(&vmap, p->combined_cache ? k : v, pool_rows, D, R) ||
-      !encode_rows_map(&qmap, query, static_cast<long long>(p->batch) * p->num_qo_heads, D, G))
+      !encode_q_map(&qmap, query, s.q_rows, p->num_qo_heads, D, G, s.q_per_item))
     return PAGED_ATTN_ERR_CUDA;
   const float scale =
       p->bmm1_scale > 0.f ? p->bmm1_scale : 1.0f / std::sqrt(static_cast<float>(D));
@@ -601,7 +722,12 @@ int paged_decode_run(const paged_decode_params* p, const void* query, const void
   a.qmap = &qmap;
   a.counters = counters;
   a.work_counter = counters + static_cast<long long>(p->batch) * Hkv;
-  a.q = static_cast<const __nv_bfloat16*>(query);
+  a.qo_indptr = qo_indptr;
+  a.q_len = q_len;
+  a.q_rows = s.q_rows;
+  a.rows = s.rows;
+  a.nrb = s.rows <= 16 ? 1 : (s.rows <= 32 ? 2 : 4);
+  a.causal = p->mask_type == PAGED_ATTN_MASK_CAUSAL;
   a.kv_indptr = kv_indptr;
   a.kv_indices = kv_indices;
   a.seq_lens = seq_lens;
@@ -663,10 +789,17 @@ int paged_decode_plan_layout_of(const paged_decode_params* p, paged_attn_plan_la
   const DecodeLayout s = decode_layout(p);
   *o = paged_attn_plan_layout{};
   o->status_offset = s.status;
-  o->split_offset_offset = s.split_off;
-  o->items_offset = s.items;
-  o->items_capacity = s.capacity;
-  o->split_chunk = s.chunk;
+  if (s.tiled) {
+    o->tiles_offset = s.sorted;
+    o->tiles_capacity = s.capacity;
+    o->count_offset = s.n_tiles;
+    o->tile_tokens = s.tile_tokens;
+  } else {
+    o->split_offset_offset = s.split_off;
+    o->items_offset = s.items;
+    o->items_capacity = s.capacity;
+    o->split_chunk = s.chunk;
+  }
   return PAGED_ATTN_OK;
 }
 

@@ -129,14 +129,14 @@ __device__ __forceinline__ TileInfo<CK> load_tile(const AttnLaunch& a, int idx) 
   return tile_from_rec<CK>(a, a.tiles[idx]);
 }
 
-// Page piece `lane` of KV tile n: keys [key, key + R) of one page (R = min(CK, page size)).
+// Page piece `lane` of KV tile n: keys [key, key + R) of one page (R = page_piece_rows).
 // Returns the piece's first key, or -1 (no piece, empty slot, past the length); the page-table
 // load it issues is first used by the caller after its next barrier wait, so the loads of
 // the whole tile (one per lane) overlap that wait.
 template <int CK>
 __device__ __forceinline__ int piece_key(const AttnLaunch& a, const TileInfo<CK>& t, int n, int lane) {
   const int ps = a.page_size;
-  const int R = CK < ps ? CK : ps;
+  const int R = page_piece_rows(ps, CK);
   if (lane >= kKvTile / R) return -1;
   const int k0 = t.walk.key0(n, (lane * R) / CK);
   const int key = k0 + (lane * R) % CK;
@@ -213,7 +213,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       }
     }
     const int ps = a.page_size;
-    const int R = CK < ps ? CK : ps;
+    const int R = page_piece_rows(ps, CK);
     const int stages = is_k ? kKStages : kVStages;
     uint8_t* ring = is_k ? k_s : v_s;
     uint64_t* full = is_k ? ctl->k_full : ctl->v_full;

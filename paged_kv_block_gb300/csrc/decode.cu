@@ -1,17 +1,22 @@
-// Single-token paged decode with split-KV (FlashInfer page prims_ts_batch_decode_with_kv_cache).
+// Paged decode with split-KV (FlashInfer page prims_ts_batch_decode_with_kv_cache): one
+// query per request, SQ fixed queries per request ([B, SQ, Hq, D]) or packed queries
+// (qo_indptr), each query at position len - nq + i under the causal / window mask.
 //
 // Persistent: two CTAs per SM pull (request, KV head, key split) work items from a counter.
-// In each CTA a producer warp fetches the item's query rows (one TMA box per 64-column half)
-// and streams the split's K/V pages into a 3-stage shared-memory ring with TMA (128-byte
-// swizzled boxes, one per page piece and half), running ahead across items so the ring never
-// drains between them.  Four consumer warps each take 16 keys of every 64-key stage and run
-// S = Q K^T and O += P V with warp MMAs (the G query heads of the KV head are the rows of the
-// 16-row A operand).  At the end of an item the warps combine their states; a request with a
-// single split writes its output directly, otherwise the split's normalised fp32 partial and
-// natural-log LSE go to the workspace and the last split of the (request, KV head) to finish
-// merges them.
+// An item's rows are the M = (queries per request) x G (query, head) pairs of its KV head,
+// row m = (query m / G, head m % G), M <= 64, in R = 1, 2 or 4 blocks of 16 rows.  In each
+// CTA a producer warp fetches the item's query rows (one TMA box of G heads x queries per
+// 64-column half) and streams the split's K/V pages into a 3-stage shared-memory ring with
+// TMA (128-byte swizzled boxes, one per page piece and half), running ahead across items so
+// the ring never drains between them.  Four consumer warps split each 64-key stage: warp w
+// takes row block w / (4 / R) and a (16 R)-key slice, 16 keys at a time, and runs
+// S = Q K^T and O += P V with warp MMAs (16 rows of the A operand).  At the end of an item
+// the warps combine their states in the shared memory of the item's last stage, which they
+// release only afterwards; a request with a single split writes its output directly,
+// otherwise the split's normalised fp32 partial and natural-log LSE go to the workspace and
+// the last split of the (request, KV head) to finish merges them.
 //
-// The kernel is bound by HBM bandwidth: every K/V byte is read once and used by G heads.
+// The kernel is bound by HBM bandwidth: every K/V byte is read once and used by all M rows.
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -33,7 +38,7 @@ constexpr int kMergeWarp = kConsumerWarps + 1;
 constexpr int kThreads = (kConsumerWarps + 2) * 32;
 constexpr int kMergeSlots = 2;
 constexpr int kItemSlots = 2;
-constexpr int kMaxG = 16;
+constexpr int kMaxRows = 64;   // rows (query, head pairs) of one item
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct DecodeSmem {
@@ -46,24 +51,28 @@ struct DecodeSmem {
   uint64_t merge_empty[kMergeSlots];
   int4 merge_job[kMergeSlots];   // (request, KV head, item, splits); request -1 ends the queue
   int abort_flag;
-  float red_m[kConsumerWarps][kMaxG];
-  float red_l[kConsumerWarps][kMaxG];
+  float red_m[kMaxRows];   // per (key slice, row) maxima and sums of the combine
+  float red_l[kMaxRows];
 };
 
-// Shared memory: ring | Q slots (two 64-column halves of G rows, each half in its own
-// 1 KB-aligned swizzle span) | per-warp O rows of the combine | control.  Sized by G so that
-// two CTAs fit on an SM for G <= 8.
-__host__ __device__ constexpr int q_half_bytes(int G) { return G <= 8 ? 1024 : 2048; }
-__host__ __device__ constexpr int red_bytes(int G) { return kConsumerWarps * G * kD * 4; }
-__host__ __device__ constexpr int smem_bytes(int G) {
-  return kStages * kStageBytes + kItemSlots * 2 * q_half_bytes(G) + red_bytes(G) +
+// Shared memory: ring | Q slots (two 64-column halves of M rows, each half in its own
+// 1 KB-aligned swizzle span) | control.  The combine at the end of an item borrows the
+// item's last ring stage (32 KB = 64 rows x 128 fp32 columns), so two CTAs fit on an SM
+// for M <= 16.
+__host__ __device__ constexpr int q_half_bytes(int M) { return (M * 128 + 1023) / 1024 * 1024; }
+__host__ __device__ constexpr int smem_bytes(int M) {
+  return kStages * kStageBytes + kItemSlots * 2 * q_half_bytes(M) +
          static_cast<int>(sizeof(DecodeSmem)) + 1024;
 }
+static_assert(kMaxRows * kD * 4 <= kStageBytes, "the combine must fit in one ring stage");
 
 __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
   return row * 128u + (((chunk ^ (row & 7u)) & 7u) << 4);
 }
 
+// NRB: 16-row blocks per item (1, 2 or 4).  ROWMASK: rows differ in their visible keys
+// (causal mask with several queries per item); otherwise every row sees the whole split.
+template <int NRB, bool ROWMASK>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
                     const __grid_constant__ CUtensorMap vmap,
@@ -71,11 +80,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
   extern __shared__ uint8_t smem_raw[];
   uint8_t* tiles = smem_align<1024>(smem_raw);
   const int G = a.Hq / a.Hkv;
-  const int qhalf = q_half_bytes(G);
+  const int M = a.rows;
+  const int qhalf = q_half_bytes(M);
   uint8_t* qslots = tiles + kStages * kStageBytes;
-  float* red_o = reinterpret_cast<float*>(qslots + kItemSlots * 2 * qhalf);
-  DecodeSmem* sm =
-      reinterpret_cast<DecodeSmem*>(reinterpret_cast<uint8_t*>(red_o) + red_bytes(G));
+  DecodeSmem* sm = reinterpret_cast<DecodeSmem*>(qslots + kItemSlots * 2 * qhalf);
 
   if (launch_aborted(a.status)) return;
   const int n_items = a.Hkv * a.split_offset[a.B];
@@ -109,8 +117,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       tma_prefetch_desc(&qmap);
     }
     const int ps = a.page_size;
-    const int R = ps < kStageKeys ? ps : kStageKeys;
-    const int pieces = kStageKeys / R;                       // <= 8 (page size >= 8)
+    const int R = page_piece_rows(ps, kStageKeys);
+    const int pieces = kStageKeys / R;                       // <= 8 (pieces of >= 8 keys)
     int sg = 0;
     for (int icount = 0;; ++icount) {
       int item = 0;
@@ -132,9 +140,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       if (lane == 0) {
         sm->item_id[islot] = item;
         uint8_t* qdst = qslots + islot * 2 * qhalf;
-        mbar_arrive_expect_tx(&sm->item_full[islot], 2u * G * 128u);
-        tma_load_2d(qdst, &qmap, &sm->item_full[islot], 0, it.b * a.Hq + it.g * G);
-        tma_load_2d(qdst + qhalf, &qmap, &sm->item_full[islot], 64, it.b * a.Hq + it.g * G);
+        // box: 64 columns x G heads x (M / G) queries; rows past the tensor read as zero
+        const int q_row0 = a.qo_indptr ? __ldg(a.qo_indptr + it.b) : it.b * a.q_len;
+        mbar_arrive_expect_tx(&sm->item_full[islot], 2u * M * 128u);
+        tma_load_3d(qdst, &qmap, &sm->item_full[islot], 0, it.g * G, q_row0);
+        tma_load_3d(qdst + qhalf, &qmap, &sm->item_full[islot], 64, it.g * G, q_row0);
       }
       const int L = a.seq_lens[it.b];
       const int first_key = (it.kv_begin / kStageKeys) * kStageKeys;
@@ -200,21 +210,24 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         __threadfence();
         const long long base = static_cast<long long>(a.Hkv) * a.split_offset[b] +
                                static_cast<long long>(g) * n_split;
-        for (int h = 0; h < G; ++h) {
-          float M = -INFINITY;
+        const int nq = a.qo_indptr ? a.qo_indptr[b + 1] - a.qo_indptr[b] : a.q_len;
+        const int q_row0 = a.qo_indptr ? a.qo_indptr[b] : b * a.q_len;
+        const int live_rows = nq <= 0 ? 0 : (nq * G < M ? nq * G : M);
+        for (int m = 0; m < live_rows; ++m) {
+          float Mx = -INFINITY;
           for (int s = lane; s < n_split; s += 32)
-            M = fmaxf(M, __ldcg(a.part_lse + (base + s) * G + h));
+            Mx = fmaxf(Mx, __ldcg(a.part_lse + (base + s) * M + m));
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-          const float Mu = M == -INFINITY ? 0.f : M;
+          for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+          const float Mu = Mx == -INFINITY ? 0.f : Mx;
           float wsum = 0.f;
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
           for (int s = 0; s < n_split; ++s) {
-            const float wgt = __expf(__ldcg(a.part_lse + (base + s) * G + h) - Mu);
+            const float wgt = __expf(__ldcg(a.part_lse + (base + s) * M + m) - Mu);
             wsum += wgt;
             if (wgt > 0.f) {
               const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                                   a.part_o + ((base + s) * G + h) * kD) + lane);
+                                   a.part_o + ((base + s) * M + m) * kD) + lane);
               acc.x += wgt * v.x;
               acc.y += wgt * v.y;
               acc.z += wgt * v.z;
@@ -222,7 +235,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
             }
           }
           const float sc = wsum > 0.f ? a.out_scale / wsum : 0.f;
-          const long long orow = static_cast<long long>(b) * a.Hq + g * G + h;
+          const int qrow = q_row0 + m / G;
+          if (qrow < 0 || qrow >= a.q_rows) continue;
+          const long long orow = static_cast<long long>(qrow) * a.Hq + g * G + m % G;
           __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(a.out + orow * kD) + lane * 2;
           dst[0] = __floats2bfloat162_rn(acc.x * sc, acc.y * sc);
           dst[1] = __floats2bfloat162_rn(acc.z * sc, acc.w * sc);
@@ -236,6 +251,10 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     // ------------------------------ consumers ------------------------------------------
     const int gr = lane >> 2, tq = lane & 3;   // fragment row group, thread-in-quad
     const float sl2 = a.scale_log2;
+    constexpr int nrb = NRB;
+    constexpr int kg = kConsumerWarps / NRB;    // key slices per stage
+    const int rb = warp / kg, kq = warp % kg;   // this warp's row block and key slice
+    constexpr int slice_keys = kStageKeys / kg; // 16 * NRB
     int sg = 0;
     int jcount = 0;                            // merge jobs handed to the merge warp
     for (int icount = 0;; ++icount) {
@@ -260,22 +279,42 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
       const int first_key = (kv_begin / kStageKeys) * kStageKeys;
       const int n_stages =
           kv_end > first_key ? (kv_end - first_key + kStageKeys - 1) / kStageKeys : 0;
-      // Q as the A operand from the item's Q slot: rows = heads of the group (rows >= G: 0).
+      const int nq = a.qo_indptr ? a.qo_indptr[b + 1] - a.qo_indptr[b] : a.q_len;
+      const int q_row0 = a.qo_indptr ? a.qo_indptr[b] : b * a.q_len;
+      const int L = a.seq_lens[b];
+      // keys [klo, khi) of the split that each of this lane's two rows sees: query i sits at
+      // L - nq + i; rows past the item's queries keep the split range (never written)
+      int klo[2], khi[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int row = rb * 16 + gr + r * 8;
+        const int i = row / G;
+        klo[r] = kv_begin;
+        khi[r] = kv_end;
+        if (ROWMASK && row < M && i < nq) {
+          const long long pos = static_cast<long long>(L) - nq + i;
+          if (a.causal && pos + 1 < khi[r]) khi[r] = static_cast<int>(pos + 1);
+          if (a.window_left >= 0 && pos - a.window_left > klo[r])
+            klo[r] = static_cast<int>(pos - a.window_left);
+        }
+      }
+      // Q as the A operand from the item's Q slot: rows rb * 16 .. + 15 (rows >= M: 0)
       uint32_t qa[kD / 16][4];
       {
         const uint8_t* qs = qslots + islot * 2 * qhalf;
         auto ld = [&](int row, int col) -> uint32_t {
-          if (row >= G) return 0u;
+          if (row >= M) return 0u;
           return *reinterpret_cast<const uint32_t*>(
               qs + (col >> 6) * qhalf + swz(row, (col & 63) >> 3) + (col & 7) * 2);
         };
+        const int r0 = rb * 16 + gr;
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
           const int c0 = ks * 16 + tq * 2;
-          qa[ks][0] = ld(gr, c0);
-          qa[ks][1] = ld(gr + 8, c0);
-          qa[ks][2] = ld(gr, c0 + 8);
-          qa[ks][3] = ld(gr + 8, c0 + 8);
+          qa[ks][0] = ld(r0, c0);
+          qa[ks][1] = ld(r0 + 8, c0);
+          qa[ks][2] = ld(r0, c0 + 8);
+          qa[ks][3] = ld(r0 + 8, c0 + 8);
         }
       }
       __syncwarp();
@@ -295,187 +334,209 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         const uint32_t kt = smem_u32(tiles + slot * kStageBytes);
         const uint32_t vt = kt + kTileBytes;
-        const int kbase = first_key + s * kStageKeys + warp * 16;   // first key of this warp
+#pragma unroll 1
+        for (int sub = 0; sub < nrb; ++sub) {
+          const int key0 = kq * slice_keys + sub * 16;          // within the stage
+          const int kbase = first_key + s * kStageKeys + key0;   // first key of the step
 
-        // ---- this warp's 16 keys of K and V into registers; the stage is released at once,
-        // so the producer refills it while the warp computes -----------------------------
-        const int mi = lane >> 3, r8 = lane & 7;
-        uint32_t kb[kD / 16][4], vb[kD / 16][4];
-        {
-          const uint32_t key_local = warp * 16 + (mi >> 1) * 8 + r8;
+          // ---- 16 keys of K and V into registers; after the slice's last step the stage
+          // is released at once (except the item's last stage, which the combine reuses),
+          // so the producer refills it while the warp computes --------------------------
+          const int mi = lane >> 3, r8 = lane & 7;
+          uint32_t kb[kD / 16][4], vb[kD / 16][4];
+          {
+            const uint32_t key_local = key0 + (mi >> 1) * 8 + r8;
 #pragma unroll
-          for (int ks = 0; ks < kD / 16; ++ks) {
-            const int dim = ks * 16 + (mi & 1) * 8;
-            ldsm_x4(kt + (dim >> 6) * kHalfBytes + swz(key_local, (dim & 63) >> 3), kb[ks][0],
-                    kb[ks][1], kb[ks][2], kb[ks][3]);
+            for (int ks = 0; ks < kD / 16; ++ks) {
+              const int dim = ks * 16 + (mi & 1) * 8;
+              ldsm_x4(kt + (dim >> 6) * kHalfBytes + swz(key_local, (dim & 63) >> 3), kb[ks][0],
+                      kb[ks][1], kb[ks][2], kb[ks][3]);
+            }
           }
-        }
-        {
-          const uint32_t key_local = warp * 16 + (mi & 1) * 8 + r8;
+          {
+            const uint32_t key_local = key0 + (mi & 1) * 8 + r8;
 #pragma unroll
-          for (int j = 0; j < kD / 8; j += 2) {
-            const int dim = (j + (mi >> 1)) * 8;
-            ldsm_x4_t(vt + (dim >> 6) * kHalfBytes + swz(key_local, (dim & 63) >> 3),
-                      vb[j >> 1][0], vb[j >> 1][1], vb[j >> 1][2], vb[j >> 1][3]);
+            for (int j = 0; j < kD / 8; j += 2) {
+              const int dim = (j + (mi >> 1)) * 8;
+              ldsm_x4_t(vt + (dim >> 6) * kHalfBytes + swz(key_local, (dim & 63) >> 3),
+                        vb[j >> 1][0], vb[j >> 1][1], vb[j >> 1][2], vb[j >> 1][3]);
+            }
           }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->empty[slot]);
+          __syncwarp();
+          if (lane == 0 && sub == nrb - 1 && s + 1 < n_stages) mbar_arrive(&sm->empty[slot]);
 
-        // ---- S = Q K^T over this warp's 16 keys --------------------------------------
-        // even and odd k-steps accumulate separately: two independent MMA chains per tile
-        float sc[2][4], sd[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sc[nt][e] = sd[nt][e] = 0.f;
-        {
-#pragma unroll
-          for (int ks = 0; ks < kD / 16; ks += 2) {
-            mma_16816(sc[0], qa[ks], kb[ks][0], kb[ks][1]);
-            mma_16816(sc[1], qa[ks], kb[ks][2], kb[ks][3]);
-            mma_16816(sd[0], qa[ks + 1], kb[ks + 1][0], kb[ks + 1][1]);
-            mma_16816(sd[1], qa[ks + 1], kb[ks + 1][2], kb[ks + 1][3]);
-          }
+          // ---- S = Q K^T over the step's 16 keys ----------------------------------------
+          // even and odd k-steps accumulate separately: two independent MMA chains per tile
+          float sc[2][4], sd[2][4];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
-        }
-        // ---- mask + online softmax (rows gr and gr + 8) ----------------------------------
-        bool vk[2][2];
-        bool any_invalid = false;
+            for (int e = 0; e < 4; ++e) sc[nt][e] = sd[nt][e] = 0.f;
+          {
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int key = kbase + nt * 8 + tq * 2 + e;
-            vk[nt][e] = key >= kv_begin && key < kv_end;
-            any_invalid |= !vk[nt][e];
-          }
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x = vk[nt][e & 1] ? sc[nt][e] * sl2 : -INFINITY;
-            sc[nt][e] = x;
-            mx[e >> 1] = fmaxf(mx[e >> 1], x);
-          }
-        // lazily moved maximum: the reference only moves when a stage exceeds it by more
-        // than 8 (log2 units), so O is rarely rescaled; the final division is unaffected
-        float alpha[2] = {1.f, 1.f}, muse[2];
-        bool moved = false;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
-          mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-          if (mx[h] > m_run[h] + 8.f) {
-            alpha[h] = m_run[h] == -INFINITY ? 0.f : fast_exp2(m_run[h] - mx[h]);
-            m_run[h] = mx[h];
-            moved = true;
-          }
-          muse[h] = m_run[h] == -INFINITY ? 0.f : m_run[h];
-        }
-        float rs[2] = {0.f, 0.f};
-        uint32_t pa_[4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const float p0 = fast_exp2(sc[nt][0] - muse[0]);
-          const float p1 = fast_exp2(sc[nt][1] - muse[0]);
-          const float p2 = fast_exp2(sc[nt][2] - muse[1]);
-          const float p3 = fast_exp2(sc[nt][3] - muse[1]);
-          rs[0] += p0 + p1;
-          rs[1] += p2 + p3;
-          pa_[nt * 2 + 0] = pack_bf16(p0, p1);
-          pa_[nt * 2 + 1] = pack_bf16(p2, p3);
-        }
-        l_run[0] = l_run[0] * alpha[0] + rs[0];
-        l_run[1] = l_run[1] * alpha[1] + rs[1];
-        if (__any_sync(0xffffffffu, moved)) {
-#pragma unroll
-          for (int j = 0; j < kD / 8; ++j) {
-            o[j][0] *= alpha[0];
-            o[j][1] *= alpha[0];
-            o[j][2] *= alpha[1];
-            o[j][3] *= alpha[1];
-          }
-        }
-        // ---- O += P V ---------------------------------------------------------------
-        const uint32_t aP[4] = {pa_[0], pa_[1], pa_[2], pa_[3]};
-        // keys of this lane inside the B fragments: 2tq, 2tq+1 (b0) and 8+2tq, 8+2tq+1 (b1)
-        const uint32_t m_lo = (vk[0][0] ? 0x0000FFFFu : 0u) | (vk[0][1] ? 0xFFFF0000u : 0u);
-        const uint32_t m_hi = (vk[1][0] ? 0x0000FFFFu : 0u) | (vk[1][1] ? 0xFFFF0000u : 0u);
-        {
-#pragma unroll
-          for (int j = 0; j < kD / 8; j += 2) {
-            uint32_t b0 = vb[j >> 1][0], b1 = vb[j >> 1][1], b2 = vb[j >> 1][2], b3 = vb[j >> 1][3];
-            if (any_invalid) {   // stale or unused rows may hold non-finite values
-              b0 &= m_lo;
-              b1 &= m_hi;
-              b2 &= m_lo;
-              b3 &= m_hi;
+            for (int ks = 0; ks < kD / 16; ks += 2) {
+              mma_16816(sc[0], qa[ks], kb[ks][0], kb[ks][1]);
+              mma_16816(sc[1], qa[ks], kb[ks][2], kb[ks][3]);
+              mma_16816(sd[0], qa[ks + 1], kb[ks + 1][0], kb[ks + 1][1]);
+              mma_16816(sd[1], qa[ks + 1], kb[ks + 1][2], kb[ks + 1][3]);
             }
-            mma_16816(o[j], aP, b0, b1);
-            mma_16816(o[j + 1], aP, b2, b3);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) sc[nt][e] += sd[nt][e];
+          }
+          // ---- mask + online softmax (rows gr and gr + 8) --------------------------------
+          // V rows outside the split may be stale or unused pool rows: zeroed for the MMA
+          bool vk[2][2];
+          bool any_invalid = false;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int key = kbase + nt * 8 + tq * 2 + e;
+              vk[nt][e] = key >= kv_begin && key < kv_end;
+              any_invalid |= !vk[nt][e];
+            }
+          float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int r = e >> 1;
+              const int key = kbase + nt * 8 + tq * 2 + (e & 1);
+              const float x = key >= klo[r] && key < khi[r] ? sc[nt][e] * sl2 : -INFINITY;
+              sc[nt][e] = x;
+              mx[r] = fmaxf(mx[r], x);
+            }
+          // lazily moved maximum: the reference only moves when a step exceeds it by more
+          // than 8 (log2 units), so O is rarely rescaled; the final division is unaffected
+          float alpha[2] = {1.f, 1.f}, muse[2];
+          bool moved = false;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+            if (mx[h] > m_run[h] + 8.f) {
+              alpha[h] = m_run[h] == -INFINITY ? 0.f : fast_exp2(m_run[h] - mx[h]);
+              m_run[h] = mx[h];
+              moved = true;
+            }
+            muse[h] = m_run[h] == -INFINITY ? 0.f : m_run[h];
+          }
+          float rs[2] = {0.f, 0.f};
+          uint32_t pa_[4];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt) {
+            const float p0 = fast_exp2(sc[nt][0] - muse[0]);
+            const float p1 = fast_exp2(sc[nt][1] - muse[0]);
+            const float p2 = fast_exp2(sc[nt][2] - muse[1]);
+            const float p3 = fast_exp2(sc[nt][3] - muse[1]);
+            rs[0] += p0 + p1;
+            rs[1] += p2 + p3;
+            pa_[nt * 2 + 0] = pack_bf16(p0, p1);
+            pa_[nt * 2 + 1] = pack_bf16(p2, p3);
+          }
+          l_run[0] = l_run[0] * alpha[0] + rs[0];
+          l_run[1] = l_run[1] * alpha[1] + rs[1];
+          if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+            for (int j = 0; j < kD / 8; ++j) {
+              o[j][0] *= alpha[0];
+              o[j][1] *= alpha[0];
+              o[j][2] *= alpha[1];
+              o[j][3] *= alpha[1];
+            }
+          }
+          // ---- O += P V -------------------------------------------------------------
+          const uint32_t aP[4] = {pa_[0], pa_[1], pa_[2], pa_[3]};
+          // keys of this lane inside the B fragments: 2tq, 2tq+1 (b0) and 8+2tq, 8+2tq+1 (b1)
+          const uint32_t m_lo = (vk[0][0] ? 0x0000FFFFu : 0u) | (vk[0][1] ? 0xFFFF0000u : 0u);
+          const uint32_t m_hi = (vk[1][0] ? 0x0000FFFFu : 0u) | (vk[1][1] ? 0xFFFF0000u : 0u);
+          {
+#pragma unroll
+            for (int j = 0; j < kD / 8; j += 2) {
+              uint32_t b0 = vb[j >> 1][0], b1 = vb[j >> 1][1], b2 = vb[j >> 1][2],
+                       b3 = vb[j >> 1][3];
+              if (any_invalid) {
+                b0 &= m_lo;
+                b1 &= m_hi;
+                b2 &= m_lo;
+                b3 &= m_hi;
+              }
+              mma_16816(o[j], aP, b0, b1);
+              mma_16816(o[j + 1], aP, b2, b3);
+            }
           }
         }
       }
       if (!ok) break;
 
-      // ---- combine the four warps -------------------------------------------------------
+      // ---- combine the key slices of each row ---------------------------------------------
+      // red_o [kg][M][128] fp32 in the item's last stage, which no warp reads any more once
+      // all have passed the first barrier; the stage is released after the last one.
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
         l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
       }
+      const bool have_stage = n_stages > 0;
+      const int last_slot = have_stage ? (sg - 1) % kStages : 0;
+      float* red_o = reinterpret_cast<float*>(tiles + last_slot * kStageBytes);
+      if (have_stage) {
+        named_bar(1, kConsumerWarps * 32);   // every warp is done with the last stage's K/V
+        const int r0 = rb * 16 + gr;
 #pragma unroll
-      for (int j = 0; j < kD / 8; ++j) {
-        const int col = j * 8 + tq * 2;
-        if (gr < G) {
-          float* r0 = red_o + (warp * G + gr) * kD + col;
-          r0[0] = o[j][0];
-          r0[1] = o[j][1];
+        for (int j = 0; j < kD / 8; ++j) {
+          const int col = j * 8 + tq * 2;
+          if (r0 < M) {
+            float* p0 = red_o + (kq * M + r0) * kD + col;
+            p0[0] = o[j][0];
+            p0[1] = o[j][1];
+          }
+          if (r0 + 8 < M) {
+            float* p1 = red_o + (kq * M + r0 + 8) * kD + col;
+            p1[0] = o[j][2];
+            p1[1] = o[j][3];
+          }
         }
-        if (gr + 8 < G) {
-          float* r1 = red_o + (warp * G + gr + 8) * kD + col;
-          r1[0] = o[j][2];
-          r1[1] = o[j][3];
-        }
-      }
-      if (tq == 0) {
-        if (gr < G) {
-          sm->red_m[warp][gr] = m_run[0];
-          sm->red_l[warp][gr] = l_run[0];
-        }
-        if (gr + 8 < G) {
-          sm->red_m[warp][gr + 8] = m_run[1];
-          sm->red_l[warp][gr + 8] = l_run[1];
+        if (tq == 0) {
+          if (r0 < M) {
+            sm->red_m[kq * M + r0] = m_run[0];
+            sm->red_l[kq * M + r0] = l_run[0];
+          }
+          if (r0 + 8 < M) {
+            sm->red_m[kq * M + r0 + 8] = m_run[1];
+            sm->red_l[kq * M + r0 + 8] = l_run[1];
+          }
         }
       }
       named_bar(1, kConsumerWarps * 32);
       const int d = threadIdx.x;   // 0..127: one output column
       const int n_split = a.split_offset[b + 1] - a.split_offset[b];
-      for (int h = 0; h < G; ++h) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm->red_m[w][h]);
-        const float Mu = M == -INFINITY ? 0.f : M;
+      const int live_rows = nq <= 0 ? 0 : (nq * G < M ? nq * G : M);
+      for (int m = 0; m < live_rows; ++m) {
+        float Mx = -INFINITY;
         float Lsum = 0.f, acc = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float f = fast_exp2(sm->red_m[w][h] - Mu);
-          Lsum += f * sm->red_l[w][h];
-          acc += f * red_o[(w * G + h) * kD + d];
+        if (have_stage) {
+          for (int w = 0; w < kg; ++w) Mx = fmaxf(Mx, sm->red_m[w * M + m]);
+          const float Mu = Mx == -INFINITY ? 0.f : Mx;
+          for (int w = 0; w < kg; ++w) {
+            const float f = fast_exp2(sm->red_m[w * M + m] - Mu);
+            Lsum += f * sm->red_l[w * M + m];
+            acc += f * red_o[(w * M + m) * kD + d];
+          }
+          Mx = Mu;
         }
         const float on = Lsum > 0.f ? acc / Lsum : 0.f;
-        const float lse_nat = Lsum > 0.f ? (Mu + fast_log2(Lsum)) * kLn2 : -INFINITY;
+        const float lse_nat = Lsum > 0.f ? (Mx + fast_log2(Lsum)) * kLn2 : -INFINITY;
         if (n_split == 1) {
-          const long long orow = static_cast<long long>(b) * a.Hq + g * G + h;
+          const int qrow = q_row0 + m / G;
+          if (qrow < 0 || qrow >= a.q_rows) continue;
+          const long long orow = static_cast<long long>(qrow) * a.Hq + g * G + m % G;
           a.out[orow * kD + d] = __float2bfloat16_rn(on * a.out_scale);
           if (a.lse && d == 0) a.lse[orow] = lse_nat;
         } else {
-          const long long prow = static_cast<long long>(item) * G + h;
+          const long long prow = static_cast<long long>(item) * M + m;
           a.part_o[prow * kD + d] = on;
           if (d == 0) a.part_lse[prow] = lse_nat;
         }
@@ -494,25 +555,25 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         ++jcount;
       }
-      named_bar(1, kConsumerWarps * 32);   // the combine buffers are free again
+      named_bar(1, kConsumerWarps * 32);   // the combine is read: the stage goes back
+      if (have_stage && lane == 0) mbar_arrive(&sm->empty[last_slot]);
     }
   }
 }
 
 int g_num_sms = 0;
 
-}  // namespace
-
-int launch_decode(const DecodeLaunch& a, cudaStream_t st) {
+template <int NRB, bool ROWMASK>
+int launch_decode_t(const DecodeLaunch& a, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_bytes(kMaxG)) != cudaSuccess)
+    if (cudaFuncSetAttribute(decode_split_kernel<NRB, ROWMASK>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes(kMaxRows)) != cudaSuccess)
       return -1;
     attr_set = true;
   }
-  const int G = a.Hq / a.Hkv;
-  const int smem = smem_bytes(G);
+  const int smem = smem_bytes(a.rows);
   const int per_sm = 2 * (smem + 1024) <= 228 * 1024 ? 2 : 1;
   if (g_num_sms == 0) {
     int dev = 0;
@@ -524,11 +585,29 @@ int launch_decode(const DecodeLaunch& a, cudaStream_t st) {
     const int grid = a.capacity < per_sm * g_num_sms ? a.capacity : per_sm * g_num_sms;
     void* tok;
     timer_begin(st, &tok);
-    decode_split_kernel<<<grid, kThreads, smem, st>>>(*a.kmap, *a.vmap, *a.qmap, a);
+    decode_split_kernel<NRB, ROWMASK><<<grid, kThreads, smem, st>>>(*a.kmap, *a.vmap, *a.qmap, a);
     timer_end(st, tok);
     count_launches(1);
   }
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
+int launch_decode(const DecodeLaunch& a, cudaStream_t st) {
+  if (a.rows < 1 || a.rows > kMaxRows || (a.nrb != 1 && a.nrb != 2 && a.nrb != 4) ||
+      a.rows > 16 * a.nrb)
+    return -1;
+  const int G = a.Hq / a.Hkv;
+  const bool rowmask = a.causal && a.rows > G;   // several queries per item
+  switch (a.nrb * 2 + (rowmask ? 1 : 0)) {
+    case 2: return launch_decode_t<1, false>(a, st);
+    case 3: return launch_decode_t<1, true>(a, st);
+    case 4: return launch_decode_t<2, false>(a, st);
+    case 5: return launch_decode_t<2, true>(a, st);
+    case 8: return launch_decode_t<4, false>(a, st);
+    default: return launch_decode_t<4, true>(a, st);
+  }
 }
 
 }  // namespace pa

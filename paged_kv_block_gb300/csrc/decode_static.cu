@@ -25,7 +25,8 @@ void* g_scratch_ptr[kMaxDevices] = {};
 extern "C" int paged_decode_run_static(const paged_decode_params* params, const void* query,
                                        const void* k, const void* v, const int32_t* kv_indptr,
                                        const int32_t* kv_indices, const int32_t* seq_lens,
-                                       void* out, float* lse, void* stream) {
+                                       const int32_t* qo_indptr, void* out, float* lse,
+                                       void* stream) {
   const size_t need = paged_decode_workspace_size(params);
   if (need == 0) return PAGED_ATTN_ERR_INVALID_ARGUMENT;
   if (need > kScratchBytes) return PAGED_ATTN_ERR_WORKSPACE;   // over the fixed maximum
@@ -47,6 +48,6 @@ extern "C" int paged_decode_run_static(const paged_decode_params* params, const 
   }
   // The regular decode path clears the status word itself and overwrites every other part
   // of the scratch it reads, so stale contents from an earlier call do not leak in.
-  return paged_decode_run(params, query, k, v, kv_indptr, kv_indices, seq_lens, out, lse,
-                          scratch, kScratchBytes, stream);
+  return paged_decode_run(params, query, k, v, kv_indptr, kv_indices, seq_lens, qo_indptr, out,
+                          lse, scratch, kScratchBytes, stream);
 }

@@ -29,6 +29,15 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 inline long long ceil_div_ll(long long a, long long b) { return (a + b - 1) / b; }
 
+// Keys per TMA page piece.  A piece is a run of consecutive keys inside one page, and the
+// pieces of a `span`-key stage or sub-chunk tile it in order (span is a power of two).  A
+// power-of-two page size gives min(page_size, span); any other multiple of 8 gives 8-key
+// pieces, which never straddle a page boundary because page boundaries are multiples of 8.
+__host__ __device__ inline int page_piece_rows(int page_size, int span) {
+  if ((page_size & (page_size - 1)) != 0) return 8;
+  return page_size < span ? page_size : span;
+}
+
 // Tokens per Q sub-tile: floor(128 / G); a CTA holds two sub-tiles.
 inline int sub_tile_tokens(int G) { return kMTileRows / G; }
 inline int cta_tile_tokens(int G) { return 2 * sub_tile_tokens(G); }
@@ -37,7 +46,9 @@ inline int cta_tile_tokens(int G) { return 2 * sub_tile_tokens(G); }
 // All write the status word on capacity problems; none synchronises the host.
 void launch_bsr_tiles(const int* block_indptr, int B, int Hkv, int Sq, int qbs, int tile_tokens,
                       TileRec* tmp, cudaStream_t st);
-void launch_prefill_tiles(const int* qo_indptr, const int* seq_lens, int B, int Hkv,
+// Request b has qo_indptr[b + 1] - qo_indptr[b] queries at rows from qo_indptr[b], or
+// (qo_indptr == nullptr) q_len queries at rows from b * q_len.
+void launch_prefill_tiles(const int* qo_indptr, int q_len, const int* seq_lens, int B, int Hkv,
                           int tile_tokens, int causal, int window_left, int capacity,
                           int* tile_offsets, int* n_tiles, TileRec* tmp, uint32_t* status,
                           cudaStream_t st);
@@ -51,9 +62,12 @@ void launch_bitmap_plan(const uint8_t* sel, const int* lo, const int* hi, const 
                         const int* blast, int T, int NB, long long capacity, int* indptr,
                         int* indices, uint32_t* status, cudaStream_t st);
 
-// Split-KV work list, and zeroed work / merge counters (B * Hkv + 1 ints).
-void launch_decode_plan(const int* seq_lens, int B, int Hkv, int chunk, int window_left,
-                        int max_splits, int* split_offset, SplitItem* items, int* counters,
+// Split-KV work list, and zeroed work / merge counters (B * Hkv + 1 ints).  Request b has
+// qo_indptr[b + 1] - qo_indptr[b] queries (qo_indptr != nullptr) or q_len; packed offsets
+// that break their contract (start 0, steps in [1, max_q], end total_q) set kErrMetadata.
+void launch_decode_plan(const int* seq_lens, const int* qo_indptr, int q_len, int max_q,
+                        int total_q, int B, int Hkv, int chunk, int window_left, int max_splits,
+                        int* split_offset, SplitItem* items, int* counters, uint32_t* status,
                         cudaStream_t st);
 
 // Keys per sub-chunk of a 128-key KV tile: the largest of 128, 64 or kv_block_size that
@@ -69,19 +83,25 @@ inline int attn_sub_chunk(int kv_block_size, bool block_sparse) {
 struct DecodeLaunch {
   const CUtensorMap* kmap;   // host copies, passed by value to the kernel
   const CUtensorMap* vmap;
-  const CUtensorMap* qmap;   // query rows [B * Hq, D], box 64 x G
+  const CUtensorMap* qmap;   // query [q_rows, Hq, D], box 64 x G heads x rows / G queries
   int* work_counter;         // next work item (zeroed by the planner)
   int* counters;             // finished splits per (request, KV head) (zeroed by the planner)
-  const __nv_bfloat16* q;    // [B, Hq, D]
+  const int* qo_indptr;      // packed queries: request b owns query rows qo_indptr[b]..;
+                             // nullptr: q_len queries per request at rows b * q_len..
+  int q_len;
+  int q_rows;                // rows of query / out: writes outside [0, q_rows) are skipped
+  int rows;                  // M = G x queries per item (<= 64): rows of one work item
+  int nrb;                   // 16-row blocks of an item: 1 (M <= 16), 2 (<= 32) or 4
+  int causal;                // keys after a query's position are masked
   const int* kv_indptr;
   const int* kv_indices;
   const int* seq_lens;
   const int* split_offset;
   const SplitItem* items;
-  float* part_o;             // [items, G, D]
-  float* part_lse;           // [items, G]
-  __nv_bfloat16* out;        // [B, Hq, D]
-  float* lse;                // [B, Hq] or nullptr
+  float* part_o;             // [items, M, D]
+  float* part_lse;           // [items, M]
+  __nv_bfloat16* out;        // [q_rows, Hq, D]
+  float* lse;                // [q_rows, Hq] or nullptr
   uint32_t* status;
   int B, Hq, Hkv, D, page_size, page_rows, k_head_off, v_head_off, num_pages;
   int capacity;              // launched work items

@@ -69,8 +69,8 @@ __global__ void bsr_tiles_kernel(const int* __restrict__ block_indptr, int B, in
 }
 
 // ---- packed-Q prefill tiles --------------------------------------------------------------
-__global__ void prefill_count_kernel(const int* __restrict__ qo, int B, int Hkv, int tt,
-                                     int capacity, int* __restrict__ off, int* n_tiles,
+__global__ void prefill_count_kernel(const int* __restrict__ qo, int q_len, int B, int Hkv,
+                                     int tt, int capacity, int* __restrict__ off, int* n_tiles,
                                      uint32_t* status) {
   __shared__ int warp_sums[32];
   int carry = 0;
@@ -78,7 +78,7 @@ __global__ void prefill_count_kernel(const int* __restrict__ qo, int B, int Hkv,
     const int b = base + threadIdx.x;
     int c = 0;
     if (b < B) {
-      const int nq = qo[b + 1] - qo[b];
+      const int nq = qo ? qo[b + 1] - qo[b] : q_len;
       c = nq > 0 ? (nq + tt - 1) / tt : 0;
     }
     int total;
@@ -97,11 +97,13 @@ __global__ void prefill_count_kernel(const int* __restrict__ qo, int B, int Hkv,
   }
 }
 
-__global__ void prefill_fill_kernel(const int* __restrict__ qo, const int* __restrict__ lens,
-                                    int Hkv, int tt, int causal, int window_left, int capacity,
-                                    const int* __restrict__ off, TileRec* __restrict__ tmp) {
+__global__ void prefill_fill_kernel(const int* __restrict__ qo, int q_len,
+                                    const int* __restrict__ lens, int Hkv, int tt, int causal,
+                                    int window_left, int capacity, const int* __restrict__ off,
+                                    TileRec* __restrict__ tmp) {
   const int b = blockIdx.x;
-  const int nq = qo[b + 1] - qo[b];
+  const int nq = qo ? qo[b + 1] - qo[b] : q_len;
+  const int row0 = qo ? qo[b] : b * q_len;
   const int L = lens[b];
   const int nt = off[b + 1] - off[b];
   for (int idx = threadIdx.x; idx < Hkv * nt; idx += blockDim.x) {
@@ -125,7 +127,7 @@ __global__ void prefill_fill_kernel(const int* __restrict__ qo, const int* __res
       t.kv_begin = static_cast<int>(lo / kKvTile);
       t.kv_end = static_cast<int>((hi + kKvTile - 1) / kKvTile);
     }
-    t.q_row0 = qo[b] + tok0;
+    t.q_row0 = row0 + tok0;
     t.pad = 0;
     tmp[pos] = t;
   }
@@ -294,27 +296,34 @@ __global__ void counts_to_indptr_kernel(const int* __restrict__ counts, int T, l
 }
 
 // ---- decode split planner -----------------------------------------------------------------
-__device__ __forceinline__ void decode_split_range(int L, int chunk, int window_left, int& lo,
-                                                   int& s0, int& n) {
+__device__ __forceinline__ void decode_split_range(int L, int nq, int chunk, int window_left,
+                                                   int& lo, int& s0, int& n) {
   if (L < 0) L = 0;
-  lo = window_left >= 0 ? max(0, L - 1 - window_left) : 0;
+  // the earliest query sits at L - nq and keeps keys from L - nq - window_left on
+  const long long first = static_cast<long long>(L) - nq - window_left;
+  lo = window_left >= 0 ? static_cast<int>(first > 0 ? first : 0) : 0;
   s0 = lo / chunk;
   const int s1 = max((L + chunk - 1) / chunk, s0 + 1);
   n = s1 - s0;
 }
 
 // One CTA: split counts, their exclusive scan, the work items, and zeroed counters.
-__global__ void decode_plan_kernel(const int* __restrict__ lens, int B, int Hkv, int chunk,
+__global__ void decode_plan_kernel(const int* __restrict__ lens, const int* __restrict__ qo,
+                                   int q_len, int max_q, int total_q, int B, int Hkv, int chunk,
                                    int window_left, int max_splits, int* __restrict__ off,
-                                   SplitItem* __restrict__ items, int* __restrict__ counters) {
+                                   SplitItem* __restrict__ items, int* __restrict__ counters,
+                                   uint32_t* status) {
   __shared__ int warp_sums[32];
   int carry = 0;
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
     int n = 0;
     if (b < B) {
+      const int nq = qo ? qo[b + 1] - qo[b] : q_len;
+      if (qo && (nq < 1 || nq > max_q || (b == 0 && qo[0] != 0) || (b == B - 1 && qo[B] != total_q)))
+        report_error(status, kErrMetadata);
       int lo, s0;
-      decode_split_range(lens[b], chunk, window_left, lo, s0, n);
+      decode_split_range(lens[b], nq, chunk, window_left, lo, s0, n);
       n = min(n, max_splits);
     }
     int total;
@@ -329,8 +338,9 @@ __global__ void decode_plan_kernel(const int* __restrict__ lens, int B, int Hkv,
   const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   for (int b = threadIdx.x >> 5; b < B; b += nw) {
     int L = lens[b];
+    const int nq = qo ? qo[b + 1] - qo[b] : q_len;
     int lo, s0, n_all;
-    decode_split_range(L, chunk, window_left, lo, s0, n_all);
+    decode_split_range(L, nq, chunk, window_left, lo, s0, n_all);
     if (L < 0) L = 0;
     const int n = off[b + 1] - off[b];
     for (int idx = lane; idx < Hkv * n; idx += 32) {
@@ -358,15 +368,15 @@ void launch_bsr_tiles(const int* block_indptr, int B, int Hkv, int Sq, int qbs, 
   count_launches(1);
 }
 
-void launch_prefill_tiles(const int* qo_indptr, const int* seq_lens, int B, int Hkv,
+void launch_prefill_tiles(const int* qo_indptr, int q_len, const int* seq_lens, int B, int Hkv,
                           int tile_tokens, int causal, int window_left, int capacity,
                           int* tile_offsets, int* n_tiles, TileRec* tmp, uint32_t* status,
                           cudaStream_t st) {
-  prefill_count_kernel<<<1, 1024, 0, st>>>(qo_indptr, B, Hkv, tile_tokens, capacity,
+  prefill_count_kernel<<<1, 1024, 0, st>>>(qo_indptr, q_len, B, Hkv, tile_tokens, capacity,
                                            tile_offsets, n_tiles, status);
   count_launches(1);
   if (B > 0) {
-    prefill_fill_kernel<<<B, 256, 0, st>>>(qo_indptr, seq_lens, Hkv, tile_tokens, causal,
+    prefill_fill_kernel<<<B, 256, 0, st>>>(qo_indptr, q_len, seq_lens, Hkv, tile_tokens, causal,
                                            window_left, capacity, tile_offsets, tmp);
     count_launches(1);
   }
@@ -404,11 +414,13 @@ void launch_bitmap_plan(const uint8_t* sel, const int* lo, const int* hi, const 
   count_launches(3);
 }
 
-void launch_decode_plan(const int* seq_lens, int B, int Hkv, int chunk, int window_left,
-                        int max_splits, int* split_offset, SplitItem* items, int* counters,
+void launch_decode_plan(const int* seq_lens, const int* qo_indptr, int q_len, int max_q,
+                        int total_q, int B, int Hkv, int chunk, int window_left, int max_splits,
+                        int* split_offset, SplitItem* items, int* counters, uint32_t* status,
                         cudaStream_t st) {
-  decode_plan_kernel<<<1, 1024, 0, st>>>(seq_lens, B, Hkv, chunk, window_left, max_splits,
-                                         split_offset, items, counters);
+  decode_plan_kernel<<<1, 1024, 0, st>>>(seq_lens, qo_indptr, q_len, max_q, total_q, B, Hkv,
+                                         chunk, window_left, max_splits, split_offset, items,
+                                         counters, status);
   count_launches(1);
 }
 

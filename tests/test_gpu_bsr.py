@@ -74,6 +74,9 @@ CASES = [
     (2, 50, 4, 4, [80, 60], 16, 16, 64, False, "empty", {}, 0.0, "dense"),
     (1, 256, 64, 8, [700], 64, 128, 64, False, "sink_recent_random",
      {"n_recent": 3, "n_random": 2}, 0.01, "causal"),
+    # page sizes that are not powers of two: 8-key pieces that never straddle a page
+    (2, 40, 8, 2, [100, 77], 24, 16, 64, False, "random", {"p": 0.6}, 0.0, "causal"),
+    (1, 30, 4, 1, [150], 40, 8, 8, True, "random", {"p": 0.5}, 0.1, "dense"),
 ]
 
 

@@ -48,5 +48,5 @@ def test_static_scratch_rejects_problems_over_its_size():
                               bmm2_scale=1.0, split_chunk=128)
     assert pkb.paged_decode_workspace_size(params) > (32 << 20)
     rc = pkb.lib().paged_decode_run_static(params, None, None, None, None, None, None, None,
-                                           None, None)
+                                           None, None, None)
     assert rc == pkb.ERR_WORKSPACE
