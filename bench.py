@@ -212,6 +212,8 @@ def qsa_pairs(p):
 def make_workload(name):
     if name == "decode_b64":
         return W.decode_b64()
+    if name == "decode_b64_sq4":
+        return W.decode_b64_sq4()
     if name == "tiny_bsr":
         return W.tiny_bsr()
     if name == "prefill_b16":
@@ -227,11 +229,14 @@ def make_workload(name):
 
 def describe(name, p):
     if p["form"] == "decode":
-        return {"workload": name, "batch": int(p["q"].shape[0]), "num_qo_heads": int(p["q"].shape[1]),
-                "num_kv_heads": int(p["kv_cache"].shape[2]), "head_dim": int(p["q"].shape[2]),
-                "page_size": int(p["page_size"]), "seq_lens": "U[512,8192]",
-                "total_kv_tokens": int(p["seq_lens"].sum()), "cache": "combined [P,2,Hkv,ps,D]",
-                "mask": p["mask_type"], "split_kv": True}
+        d = {"workload": name, "batch": int(p["q"].shape[0]), "num_qo_heads": int(p["q"].shape[-2]),
+             "num_kv_heads": int(p["kv_cache"].shape[2]), "head_dim": int(p["q"].shape[-1]),
+             "page_size": int(p["page_size"]), "seq_lens": "U[512,8192]",
+             "total_kv_tokens": int(p["seq_lens"].sum()), "cache": "combined [P,2,Hkv,ps,D]",
+             "mask": p["mask_type"], "split_kv": True}
+        if p["seq_len_q"] > 1:
+            d["seq_len_q"] = int(p["seq_len_q"])
+        return d
     if p["form"] == "bsr":
         return {"workload": name, "batch": int(p["q"].shape[0]), "q_len": int(p["q"].shape[1]),
                 "num_qo_heads": int(p["q"].shape[2]), "page_size": int(p["page_size"]),
@@ -260,11 +265,13 @@ class Runner:
             self.params = pkb.decode_params(d["q"], d["kv_cache"], p["max_seq_len"],
                                             bmm1_scale=p["sm_scale"], bmm2_scale=p["bmm2_scale"],
                                             mask_type=p["mask_type"],
-                                            window_left=p["window_left"])
+                                            window_left=p["window_left"],
+                                            seq_len_q=p["seq_len_q"], qo_indptr=d["qo_indptr"],
+                                            max_seq_len_q=p["max_seq_len_q"])
             self.ws = torch.empty(pkb.paged_decode_workspace_size(self.params), dtype=torch.uint8,
                                   device=dev)
             self.out = torch.empty_like(d["q"])
-            self.lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
+            self.lse = torch.empty(d["q"].shape[:-1], dtype=torch.float32, device=dev)
         elif self.form == "bsr":
             cache = d["kv_cache"] if "kv_cache" in d else (d["k_cache"], d["v_cache"])
             self.k, self.v = (cache, None) if not isinstance(cache, tuple) else cache
@@ -302,7 +309,8 @@ class Runner:
 
     def inputs(self):
         """The step's input tensors (device), in a fixed order."""
-        names = {"decode": ["q", "kv_cache", "kv_indptr", "kv_indices", "seq_lens"],
+        names = {"decode": ["q", "kv_cache", "kv_indptr", "kv_indices", "seq_lens",
+                            "qo_indptr"],
                  "bsr": ["q", "k_cache", "v_cache", "kv_cache", "kv_indptr", "kv_indices",
                          "block_indptr", "block_indices", "seq_lens_kv", "kv_valid_bits"],
                  "prefill": ["q", "k_cache", "v_cache", "qo_indptr", "block_tables",
@@ -315,7 +323,8 @@ class Runner:
         d = self.d
         if self.form == "decode":
             pkb.paged_decode_run(self.params, d["q"], d["kv_cache"], None, d["kv_indptr"],
-                                 d["kv_indices"], d["seq_lens"], self.out, self.lse, self.ws)
+                                 d["kv_indices"], d["seq_lens"], self.out, self.lse, self.ws,
+                                 qo_indptr=d["qo_indptr"])
         elif self.form == "bsr":
             pkb.paged_attn_plan(self.params, self.meta, self.ws)
             pkb.paged_attn_run(self.params, self.meta, d["q"], self.k, self.v, self.out, None,
@@ -544,7 +553,8 @@ def main():
         line["cpu_baseline"] = cpu_baseline_decode(p)
     if not args.no_extra and rank == 0:
         extra = {}
-        for name in ("tiny_bsr", "prefill_b16", "prefill_b16_w1023", "long_bsr", "qsa_t32k"):
+        for name in ("decode_b64_sq4", "tiny_bsr", "prefill_b16", "prefill_b16_w1023",
+                     "long_bsr", "qsa_t32k"):
             if name == args.workload:
                 continue
             try:
@@ -554,9 +564,18 @@ def main():
                 rc, raw = rr.status()
                 if rc != pkb.OK:
                     raise RuntimeError(f"device status {raw:#x}")
+                steps = max(3, min(args.steps, 20))
+                if q["form"] == "decode":
+                    nb = decode_kv_bytes(q)
+                    extra[name] = {"gbs_step": nb / (reg / steps * 1e-3) / 1e9,
+                                   "gbs_kernel": nb / (kms * 1e-3) / 1e9,
+                                   "frac_hbm_peak": nb / (kms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                                   "ms_step": reg / steps, "ms_kernel": kms, "kv_bytes": nb}
+                    del rr
+                    torch.cuda.empty_cache()
+                    continue
                 n = {"bsr": bsr_pairs, "prefill": prefill_pairs, "qsa": qsa_pairs}[q["form"]](q)
                 flops = 4 * q["q"].shape[-1] * n
-                steps = max(3, min(args.steps, 20))
                 extra[name] = {"tflops_step": flops / (reg / steps * 1e-3) / 1e12,
                                "tflops_kernel": flops / (kms * 1e-3) / 1e12,
                                "frac_bf16_peak": flops / (kms * 1e-3) / 1e12 / pk["bf16_tflops"],

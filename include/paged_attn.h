@@ -267,8 +267,10 @@ int paged_decode_run_static(const paged_decode_params* params, const void* query
  *   tiles:   TileRec {b, g, tok0, ntok, kv_begin, kv_end, q_row0, 0} (8 x int32) in launch
  *            order; BSR: tiles_capacity records; prefill: int32 count at count_offset
  *   bitmap:  int32 indptr [T + 1] and int32 block ids
- *   decode:  int32 split_offset [B + 1] and items {b, g, kv_begin, kv_end} (4 x int32);
- *            the live item count is num_kv_heads * split_offset[B] */
+ *   decode:  int32 split_offset [B + 1], items {b, g, kv_begin, kv_end} (4 x int32) and
+ *            the int32 claim order of the items (by size class min(7, 8 x keys / split_chunk),
+ *            largest first, list order within a class); the live item count is
+ *            num_kv_heads * split_offset[B] */
 typedef struct paged_attn_plan_layout {
   size_t status_offset;
   size_t tiles_offset;
@@ -282,6 +284,7 @@ typedef struct paged_attn_plan_layout {
   int64_t items_capacity;
   int split_chunk;
   int tile_tokens;
+  size_t order_offset;   /* decode: int32 claim order of the split items */
 } paged_attn_plan_layout;
 
 int paged_attn_plan_layout_of(const paged_attn_params* params, paged_attn_plan_layout* out);

@@ -131,6 +131,20 @@ def plan_decode(seq_lens, Hkv, chunk, window_left=-1, q_lens=None):
     return split_offset.astype(np.int32), items.astype(np.int32)
 
 
+ORDER_CLASSES = 8  # size classes of the split-KV claim order
+
+
+def decode_work_order(items, chunk):
+    """Order in which the split-KV work items are claimed: by size class
+    min(7, 8 * (kv_end - kv_begin) // chunk), largest class first; items of one class keep
+    their list order.  The longest splits start first and the short tails of the requests
+    fill the end of the launch."""
+    items = np.asarray(items, dtype=np.int64).reshape(-1, 4)
+    size = items[:, 3] - items[:, 2]
+    cls = np.clip((ORDER_CLASSES * size) // chunk, 0, ORDER_CLASSES - 1)
+    return np.array(sorted(range(len(items)), key=lambda i: (-int(cls[i]), i)), dtype=np.int32)
+
+
 def plan_bitmap(sel_blocks, lo, hi, block_first, block_last):
     """Per-query CSR of selected global block IDs (ascending): block g is listed for query
     t iff sel_blocks[t, g] != 0 and [block_first[g], block_last[g]] meets [lo[t], hi[t]]."""

@@ -74,7 +74,8 @@ class PlanLayout(C.Structure):
                 ("indptr_offset", C.c_size_t), ("indices_offset", C.c_size_t),
                 ("indices_capacity", C.c_int64), ("split_offset_offset", C.c_size_t),
                 ("items_offset", C.c_size_t), ("items_capacity", C.c_int64),
-                ("split_chunk", C.c_int), ("tile_tokens", C.c_int)]
+                ("split_chunk", C.c_int), ("tile_tokens", C.c_int),
+                ("order_offset", C.c_size_t)]
 
 
 _LIB = None

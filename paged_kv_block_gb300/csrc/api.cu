@@ -174,7 +174,7 @@ PrefillLayout prefill_layout(const paged_prefill_params* p) {
 constexpr int kDecodeMaxRows = 64;
 
 struct DecodeLayout {
-  size_t status, split_off, counters, items, part_lse, part_o;   // split-KV route
+  size_t status, split_off, counters, items, order, part_lse, part_o;   // split-KV route
   size_t n_tiles, tile_off, tmp, sorted, hist, offs;             // tile route
   size_t total;
   int capacity, chunk, max_splits;
@@ -242,6 +242,7 @@ DecodeLayout decode_layout(const paged_decode_params* p) {
     s.split_off = l.take(sizeof(int) * static_cast<size_t>(p->batch + 1));
     s.counters = l.take(sizeof(int) * (static_cast<size_t>(p->batch) * p->num_kv_heads + 1));
     s.items = l.take(sizeof(SplitItem) * static_cast<size_t>(s.capacity > 0 ? s.capacity : 1));
+    s.order = l.take(sizeof(int) * static_cast<size_t>(s.capacity > 0 ? s.capacity : 1));
     s.part_lse = l.take(sizeof(float) * static_cast<size_t>(s.capacity) * s.rows + 4);
     s.part_o = l.take(sizeof(float) * static_cast<size_t>(s.capacity) * s.rows * p->head_dim + 4);
   } else {
@@ -704,8 +705,9 @@ int paged_decode_run(const paged_decode_params* p, const void* query, const void
   SplitItem* items = at<SplitItem>(ws, s.items);
   int* counters = at<int>(ws, s.counters);
   const int q_len = qo_indptr ? 0 : s.q_per_item;
+  int* order = at<int>(ws, s.order);
   launch_decode_plan(seq_lens, qo_indptr, q_len, s.q_per_item, s.q_rows, p->batch, Hkv, s.chunk,
-                     p->window_left, s.max_splits, split_off, items, counters, status, st);
+                     p->window_left, s.max_splits, split_off, items, order, counters, status, st);
   const int R = page_piece_rows(ps, 64);
   const long long pool_rows = static_cast<long long>(p->num_pages) * (p->combined_cache ? 2 : 1) *
                               Hkv * ps;
@@ -733,6 +735,7 @@ int paged_decode_run(const paged_decode_params* p, const void* query, const void
   a.seq_lens = seq_lens;
   a.split_offset = split_off;
   a.items = items;
+  a.order = order;
   a.part_o = at<float>(ws, s.part_o);
   a.part_lse = at<float>(ws, s.part_lse);
   a.out = static_cast<__nv_bfloat16*>(out);
@@ -798,6 +801,7 @@ int paged_decode_plan_layout_of(const paged_decode_params* p, paged_attn_plan_la
     o->split_offset_offset = s.split_off;
     o->items_offset = s.items;
     o->items_capacity = s.capacity;
+    o->order_offset = s.order;
     o->split_chunk = s.chunk;
   }
   return PAGED_ATTN_OK;

@@ -70,6 +70,104 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
   return row * 128u + (((chunk ^ (row & 7u)) & 7u) << 4);
 }
 
+// Merge of the split partials of rows m0 .. m0 + 7 (those below live_rows) of one (request,
+// KV head), by one warp: lane l owns columns 4l .. 4l + 3.  The merge sits on the critical
+// path at the end of a launch, so it is written for few dependent L2 round trips: lane j
+// loads split s0 + j's LSE of all 8 rows at once, and the partial rows of two splits are
+// loaded together (16 loads in flight) before they are accumulated.  Every live row of
+// every split has a partial (an empty split writes O = 0 and LSE = -inf), so no load is
+// conditional on the data.
+constexpr int kMergeRows = 8;
+__device__ __forceinline__ void merge_rows(const DecodeLaunch& a, long long base, int n_split, int M,
+                                        int G, int m0, int live_rows, int q_row0, int g,
+                                        int lane) {
+  const int nr = live_rows - m0 < kMergeRows ? live_rows - m0 : kMergeRows;
+  float Mx[kMergeRows], wsum[kMergeRows];
+  float4 acc[kMergeRows];
+#pragma unroll
+  for (int r = 0; r < kMergeRows; ++r) {
+    Mx[r] = -INFINITY;
+    wsum[r] = 0.f;
+    acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  // row maxima over all splits (one pass of loads when n_split <= 32)
+  float lse_own[kMergeRows];
+  for (int s0 = 0; s0 < n_split; s0 += 32) {
+    const int s = s0 + lane;
+#pragma unroll
+    for (int r = 0; r < kMergeRows; ++r) {
+      lse_own[r] = (s < n_split && r < nr) ? __ldcg(a.part_lse + (base + s) * M + m0 + r)
+                                           : -INFINITY;
+      Mx[r] = fmaxf(Mx[r], lse_own[r]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kMergeRows; ++r) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Mx[r] = fmaxf(Mx[r], __shfl_xor_sync(0xffffffffu, Mx[r], o));
+    if (Mx[r] == -INFINITY) Mx[r] = 0.f;
+  }
+  for (int s0 = 0; s0 < n_split; s0 += 32) {
+    const int s = s0 + lane;
+    float wl[kMergeRows];
+#pragma unroll
+    for (int r = 0; r < kMergeRows; ++r) {
+      // the LSEs of the last group of 32 splits are still in registers
+      const float l = (s0 + 32 >= n_split) ? lse_own[r]
+                      : ((s < n_split && r < nr) ? __ldcg(a.part_lse + (base + s) * M + m0 + r)
+                                                 : -INFINITY);
+      wl[r] = __expf(l - Mx[r]);
+      wsum[r] += wl[r];
+    }
+    const int ns = n_split - s0 < 32 ? n_split - s0 : 32;
+    for (int j = 0; j < ns; j += 2) {
+      const bool two = j + 1 < ns;
+      const float* po0 = a.part_o + ((base + s0 + j) * M + m0) * kD;
+      const float* po1 = po0 + static_cast<long long>(M) * kD;
+      float4 v0[kMergeRows], v1[kMergeRows];
+#pragma unroll
+      for (int r = 0; r < kMergeRows; ++r) {
+        if (r < nr) {
+          v0[r] = __ldcg(reinterpret_cast<const float4*>(po0 + r * kD) + lane);
+          if (two) v1[r] = __ldcg(reinterpret_cast<const float4*>(po1 + r * kD) + lane);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kMergeRows; ++r) {
+        const float w0 = __shfl_sync(0xffffffffu, wl[r], j);
+        const float w1 = __shfl_sync(0xffffffffu, wl[r], two ? j + 1 : j);
+        if (r < nr) {
+          acc[r].x += w0 * v0[r].x;
+          acc[r].y += w0 * v0[r].y;
+          acc[r].z += w0 * v0[r].z;
+          acc[r].w += w0 * v0[r].w;
+          if (two) {
+            acc[r].x += w1 * v1[r].x;
+            acc[r].y += w1 * v1[r].y;
+            acc[r].z += w1 * v1[r].z;
+            acc[r].w += w1 * v1[r].w;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kMergeRows; ++r) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum[r] += __shfl_xor_sync(0xffffffffu, wsum[r], o);
+    if (r >= nr) continue;
+    const int m = m0 + r;
+    const int qrow = q_row0 + m / G;
+    if (qrow < 0 || qrow >= a.q_rows) continue;
+    const float sc = wsum[r] > 0.f ? a.out_scale / wsum[r] : 0.f;
+    const long long orow = static_cast<long long>(qrow) * a.Hq + g * G + m % G;
+    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(a.out + orow * kD) + lane * 2;
+    dst[0] = __floats2bfloat162_rn(acc[r].x * sc, acc[r].y * sc);
+    dst[1] = __floats2bfloat162_rn(acc[r].z * sc, acc[r].w * sc);
+    if (a.lse && lane == 0) a.lse[orow] = wsum[r] > 0.f ? Mx[r] + __logf(wsum[r]) : -INFINITY;
+  }
+}
+
 // NRB: 16-row blocks per item (1, 2 or 4).  ROWMASK: rows differ in their visible keys
 // (causal mask with several queries per item); otherwise every row sees the whole split.
 template <int NRB, bool ROWMASK>
@@ -136,6 +234,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         }
         break;
       }
+      item = __ldg(a.order + item);
       const SplitItem it = a.items[item];
       if (lane == 0) {
         sm->item_id[islot] = item;
@@ -213,36 +312,8 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
         const int nq = a.qo_indptr ? a.qo_indptr[b + 1] - a.qo_indptr[b] : a.q_len;
         const int q_row0 = a.qo_indptr ? a.qo_indptr[b] : b * a.q_len;
         const int live_rows = nq <= 0 ? 0 : (nq * G < M ? nq * G : M);
-        for (int m = 0; m < live_rows; ++m) {
-          float Mx = -INFINITY;
-          for (int s = lane; s < n_split; s += 32)
-            Mx = fmaxf(Mx, __ldcg(a.part_lse + (base + s) * M + m));
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
-          const float Mu = Mx == -INFINITY ? 0.f : Mx;
-          float wsum = 0.f;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int s = 0; s < n_split; ++s) {
-            const float wgt = __expf(__ldcg(a.part_lse + (base + s) * M + m) - Mu);
-            wsum += wgt;
-            if (wgt > 0.f) {
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                                   a.part_o + ((base + s) * M + m) * kD) + lane);
-              acc.x += wgt * v.x;
-              acc.y += wgt * v.y;
-              acc.z += wgt * v.z;
-              acc.w += wgt * v.w;
-            }
-          }
-          const float sc = wsum > 0.f ? a.out_scale / wsum : 0.f;
-          const int qrow = q_row0 + m / G;
-          if (qrow < 0 || qrow >= a.q_rows) continue;
-          const long long orow = static_cast<long long>(qrow) * a.Hq + g * G + m % G;
-          __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(a.out + orow * kD) + lane * 2;
-          dst[0] = __floats2bfloat162_rn(acc.x * sc, acc.y * sc);
-          dst[1] = __floats2bfloat162_rn(acc.z * sc, acc.w * sc);
-          if (a.lse && lane == 0) a.lse[orow] = wsum > 0.f ? Mu + __logf(wsum) : -INFINITY;
-        }
+        for (int m0 = 0; m0 < live_rows; m0 += kMergeRows)
+          merge_rows(a, base, n_split, M, G, m0, live_rows, q_row0, g, lane);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm->merge_empty[js]);

@@ -62,13 +62,14 @@ void launch_bitmap_plan(const uint8_t* sel, const int* lo, const int* hi, const 
                         const int* blast, int T, int NB, long long capacity, int* indptr,
                         int* indices, uint32_t* status, cudaStream_t st);
 
-// Split-KV work list, and zeroed work / merge counters (B * Hkv + 1 ints).  Request b has
+// Split-KV work list, its claim order (items by size class, largest first; stable), and
+// zeroed work / merge counters (B * Hkv + 1 ints).  Request b has
 // qo_indptr[b + 1] - qo_indptr[b] queries (qo_indptr != nullptr) or q_len; packed offsets
 // that break their contract (start 0, steps in [1, max_q], end total_q) set kErrMetadata.
 void launch_decode_plan(const int* seq_lens, const int* qo_indptr, int q_len, int max_q,
                         int total_q, int B, int Hkv, int chunk, int window_left, int max_splits,
-                        int* split_offset, SplitItem* items, int* counters, uint32_t* status,
-                        cudaStream_t st);
+                        int* split_offset, SplitItem* items, int* order, int* counters,
+                        uint32_t* status, cudaStream_t st);
 
 // Keys per sub-chunk of a 128-key KV tile: the largest of 128, 64 or kv_block_size that
 // divides kv_block_size (dense tiles use 128).
@@ -98,6 +99,7 @@ struct DecodeLaunch {
   const int* seq_lens;
   const int* split_offset;
   const SplitItem* items;
+  const int* order;          // claim order: the k-th claimed item is items[order[k]]
   float* part_o;             // [items, M, D]
   float* part_lse;           // [items, M]
   __nv_bfloat16* out;        // [q_rows, Hq, D]

@@ -307,12 +307,15 @@ __device__ __forceinline__ void decode_split_range(int L, int nq, int chunk, int
   n = s1 - s0;
 }
 
-// One CTA: split counts, their exclusive scan, the work items, and zeroed counters.
+constexpr int kOrderClasses = 8;   // size classes of the claim order
+
+// One CTA: split counts, their exclusive scan, the work items, their claim order and zeroed
+// counters.
 __global__ void decode_plan_kernel(const int* __restrict__ lens, const int* __restrict__ qo,
                                    int q_len, int max_q, int total_q, int B, int Hkv, int chunk,
                                    int window_left, int max_splits, int* __restrict__ off,
-                                   SplitItem* __restrict__ items, int* __restrict__ counters,
-                                   uint32_t* status) {
+                                   SplitItem* __restrict__ items, int* __restrict__ order,
+                                   int* __restrict__ counters, uint32_t* status) {
   __shared__ int warp_sums[32];
   int carry = 0;
   for (int base = 0; base < B; base += blockDim.x) {
@@ -353,6 +356,50 @@ __global__ void decode_plan_kernel(const int* __restrict__ lens, const int* __re
       it.kv_end = static_cast<int>(min((s + 1) * chunk, static_cast<long long>(L)));
       items[static_cast<long long>(Hkv) * off[b] + idx] = it;
     }
+  }
+  __syncthreads();
+  // Claim order: items by size class min(7, 8 * size / chunk), largest first, list order
+  // within a class.  Thread t ranks a contiguous run of items: class counts in registers,
+  // one block scan per class, then the positions.  The class of a size is the number of
+  // thresholds ceil(c * chunk / 8), c = 1..7, it reaches.
+  const int n_items = Hkv * off[B];
+  const int per = (n_items + blockDim.x - 1) / blockDim.x;
+  const int i0 = min(n_items, static_cast<int>(threadIdx.x) * per);
+  const int i1 = min(n_items, i0 + per);
+  int thr[kOrderClasses];
+#pragma unroll
+  for (int c = 1; c < kOrderClasses; ++c)
+    thr[c] = static_cast<int>((static_cast<long long>(c) * chunk + kOrderClasses - 1) / kOrderClasses);
+  auto cls = [&](int i) {
+    const int z = items[i].kv_end - items[i].kv_begin;
+    int c = 0;
+#pragma unroll
+    for (int k = 1; k < kOrderClasses; ++k) c += z >= thr[k];
+    return c;
+  };
+  int cnt[kOrderClasses];
+#pragma unroll
+  for (int c = 0; c < kOrderClasses; ++c) cnt[c] = 0;
+  for (int i = i0; i < i1; ++i) {
+    const int ci = cls(i);
+#pragma unroll
+    for (int c = 0; c < kOrderClasses; ++c) cnt[c] += ci == c;
+  }
+  int pos[kOrderClasses];
+  int base = 0;
+#pragma unroll
+  for (int c = kOrderClasses - 1; c >= 0; --c) {
+    int total;
+    pos[c] = base + block_exclusive_scan(cnt[c], warp_sums, total);
+    base += total;
+  }
+  for (int i = i0; i < i1; ++i) {
+    const int ci = cls(i);
+    int p = 0;
+#pragma unroll
+    for (int c = 0; c < kOrderClasses; ++c)
+      if (ci == c) p = pos[c]++;
+    order[p] = i;
   }
 }
 
@@ -416,11 +463,11 @@ void launch_bitmap_plan(const uint8_t* sel, const int* lo, const int* hi, const 
 
 void launch_decode_plan(const int* seq_lens, const int* qo_indptr, int q_len, int max_q,
                         int total_q, int B, int Hkv, int chunk, int window_left, int max_splits,
-                        int* split_offset, SplitItem* items, int* counters, uint32_t* status,
-                        cudaStream_t st) {
+                        int* split_offset, SplitItem* items, int* order, int* counters,
+                        uint32_t* status, cudaStream_t st) {
   decode_plan_kernel<<<1, 1024, 0, st>>>(seq_lens, qo_indptr, q_len, max_q, total_q, B, Hkv,
                                          chunk, window_left, max_splits, split_offset, items,
-                                         counters, status);
+                                         order, counters, status);
   count_launches(1);
 }
 

@@ -398,6 +398,15 @@ def decode_b64(seed=1002):
     return make_decode_problem(seed, lens, Hq=32, Hkv=8, D=128, page_size=16, combined=True)
 
 
+def decode_b64_sq4(seed=1002, seq_len_q=4):
+    """Multi-query decode (speculative verification): the decode_b64 cache and lengths with
+    seq_len_q = 4 queries per request, query [64, 4, 32, 128], causal mask."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(512, 8192, size=64, endpoint=True)
+    return make_decode_problem(seed, lens, Hq=32, Hkv=8, D=128, page_size=16, combined=True,
+                               mask_type="causal", seq_len_q=seq_len_q)
+
+
 def prefill_b16(seed=1003, window_left=-1):
     """Dense causal packed-Q prefill: B=16, q_len U[128, 2048], prefix U[0, 2048],
     Hq=32, Hkv=8, D=128, separate HND pools ps=32, row-strided block_tables."""

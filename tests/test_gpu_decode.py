@@ -71,6 +71,8 @@ def test_decode_matches_oracle(case):
     assert np.array_equal(off, off_ref)
     items = read_ws(ws, lay.items_offset, 4 * Hkv * int(off[-1])).numpy().reshape(-1, 4)
     assert np.array_equal(items, items_ref)
+    order = read_ws(ws, lay.order_offset, len(items_ref)).numpy()
+    assert np.array_equal(order, PL.decode_work_order(items_ref, lay.split_chunk))
     if chunk:
         assert lay.split_chunk == chunk
 

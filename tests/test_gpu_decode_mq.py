@@ -62,6 +62,8 @@ def _check_plan(p, ws, params):
         assert np.array_equal(off, off_ref)
         items = read_ws(ws, lay.items_offset, 4 * Hkv * int(off[-1])).numpy().reshape(-1, 4)
         assert np.array_equal(items, items_ref)
+        order = read_ws(ws, lay.order_offset, len(items_ref)).numpy()
+        assert np.array_equal(order, PL.decode_work_order(items_ref, lay.split_chunk))
     else:                                            # tile route
         n = int(read_ws(ws, lay.count_offset, 1)[0])
         recs = read_ws(ws, lay.tiles_offset, 8 * n).numpy().reshape(-1, 8)

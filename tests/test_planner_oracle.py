@@ -98,6 +98,20 @@ def test_multi_query_decode_splits_cover_the_visible_union():
                     assert np.all(rows[:, 3] - rows[:, 2] <= chunk)
 
 
+def test_decode_work_order_is_a_stable_size_class_sort():
+    lens = [1, 700, 129, 4000, 333, 2049]
+    chunk = 512
+    _, items = PL.plan_decode(lens, 2, chunk)
+    order = PL.decode_work_order(items, chunk)
+    assert sorted(order.tolist()) == list(range(len(items)))
+    size = items[order, 3] - items[order, 2]
+    cls = np.minimum(7, 8 * size // chunk)
+    assert np.all(np.diff(cls) <= 0)                       # larger classes first
+    for c in np.unique(cls):
+        assert np.all(np.diff(order[cls == c]) > 0)       # list order inside a class
+    assert size[0] == chunk and size[-1] == min(items[:, 3] - items[:, 2])
+
+
 def test_decode_chunk_formula():
     # floor(64 * 8 * 64 / (16 * 152)) = 13 tiles of 128 keys
     assert PL.decode_split_chunk(64, 8, 8192, 152) == 1664
