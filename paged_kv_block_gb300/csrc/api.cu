@@ -694,7 +694,10 @@ int paged_decode_run(const paged_decode_params* p, const void* query, const void
   if (!ws || ws_bytes < s.total) return PAGED_ATTN_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* status = at<uint32_t>(ws, s.status);
-  if (cudaMemsetAsync(status, 0, 4 * sizeof(uint32_t), st) != cudaSuccess) return PAGED_ATTN_ERR_CUDA;
+  // the split route's planner clears the status word itself
+  if ((s.tiled || p->batch == 0 || s.q_rows == 0) &&
+      cudaMemsetAsync(status, 0, 4 * sizeof(uint32_t), st) != cudaSuccess)
+    return PAGED_ATTN_ERR_CUDA;
   if (p->batch == 0 || s.q_rows == 0) return PAGED_ATTN_OK;
   if (s.tiled)
     return decode_run_tiled(p, s, query, k, v, kv_indptr, kv_indices, seq_lens, qo_indptr, out,

@@ -40,6 +40,17 @@ __device__ __forceinline__ bool launch_aborted(const uint32_t* status) {
   return status && (*reinterpret_cast<const volatile uint32_t*>(status) & kErrTimeout);
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream serialization
+// may start while the previous kernel of its stream still runs: grid_dependency_wait()
+// returns once that kernel has completed and its writes are visible (at once when there is
+// no such dependency).  grid_launch_dependents() lets the next kernel start early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------------------

@@ -51,6 +51,7 @@ struct DecodeSmem {
   uint64_t merge_empty[kMergeSlots];
   int4 merge_job[kMergeSlots];   // (request, KV head, item, splits); request -1 ends the queue
   int abort_flag;
+  int skip;                // an earlier CTA recorded a timeout: this CTA does nothing
   float red_m[kMaxRows];   // per (key slice, row) maxima and sums of the combine
   float red_l[kMaxRows];
 };
@@ -183,8 +184,6 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
   uint8_t* qslots = tiles + kStages * kStageBytes;
   DecodeSmem* sm = reinterpret_cast<DecodeSmem*>(qslots + kItemSlots * 2 * qhalf);
 
-  if (launch_aborted(a.status)) return;
-  const int n_items = a.Hkv * a.split_offset[a.B];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -202,18 +201,23 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     sm->abort_flag = 0;
     fence_mbar_init();
   }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&qmap);
+  }
+  // everything below reads the plan, which the launch before this one writes
+  grid_dependency_wait();
+  if (threadIdx.x == 0) sm->skip = launch_aborted(a.status) ? 1 : 0;
   __syncthreads();
+  if (sm->skip) return;
+  const int n_items = a.Hkv * a.split_offset[a.B];
   volatile int* abort_flag = &sm->abort_flag;
 
   if (warp == kProducerWarp) {
     // ------------------------------ producer (whole warp) -----------------------------
     // Lane p handles page piece p of every stage (R keys of one page); the page ids of the
     // next stage are loaded while the current stage is issued.
-    if (lane == 0) {
-      tma_prefetch_desc(&kmap);
-      tma_prefetch_desc(&vmap);
-      tma_prefetch_desc(&qmap);
-    }
     const int ps = a.page_size;
     const int R = page_piece_rows(ps, kStageKeys);
     const int pieces = kStageKeys / R;                       // <= 8 (pieces of >= 8 keys)
@@ -656,7 +660,20 @@ int launch_decode_t(const DecodeLaunch& a, cudaStream_t st) {
     const int grid = a.capacity < per_sm * g_num_sms ? a.capacity : per_sm * g_num_sms;
     void* tok;
     timer_begin(st, &tok);
-    decode_split_kernel<NRB, ROWMASK><<<grid, kThreads, smem, st>>>(*a.kmap, *a.vmap, *a.qmap, a);
+    // programmatic dependent launch: the CTAs start their prologue while the planner runs
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_split_kernel<NRB, ROWMASK>, *a.kmap, *a.vmap, *a.qmap,
+                           a) != cudaSuccess)
+      return -1;
     timer_end(st, tok);
     count_launches(1);
   }

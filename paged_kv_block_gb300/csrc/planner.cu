@@ -317,6 +317,11 @@ __global__ void decode_plan_kernel(const int* __restrict__ lens, const int* __re
                                    SplitItem* __restrict__ items, int* __restrict__ order,
                                    int* __restrict__ counters, uint32_t* status) {
   __shared__ int warp_sums[32];
+  // the split kernel that follows may start its prologue now; it reads nothing of the plan
+  // before this kernel has completed
+  grid_launch_dependents();
+  if (threadIdx.x < 4) status[threadIdx.x] = 0;   // the status word of this run
+  __syncthreads();
   int carry = 0;
   for (int base = 0; base < B; base += blockDim.x) {
     const int b = base + threadIdx.x;
