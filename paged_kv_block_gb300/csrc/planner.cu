@@ -38,6 +38,45 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int& total) {
   return before + x - v;
 }
 
+// Exclusive block scan of N values per thread at once (N independent sums); total[k] is the
+// block total of value k.  ws: N * 32 ints of shared memory.
+template <int N>
+__device__ void block_exclusive_scan_n(const int (&v)[N], int (&ex)[N], int (&total)[N], int* ws) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int x[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    x[k] = v[k];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x[k], o);
+      if (lane >= o) x[k] += y;
+    }
+  }
+  if (lane == 31)
+#pragma unroll
+    for (int k = 0; k < N; ++k) ws[k * 32 + w] = x[k];
+  __syncthreads();
+  if (w == 0) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      int t = lane < nw ? ws[k * 32 + lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += y;
+      }
+      ws[k * 32 + lane] = t;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    ex[k] = (w > 0 ? ws[k * 32 + w - 1] : 0) + x[k] - v[k];
+    total[k] = ws[k * 32 + nw - 1];
+  }
+}
+
 // ---- block-sparse tiles ----------------------------------------------------------------
 // One thread per BSR row (b, g, r).  Tile (b, g, r, m) goes to natural index
 // (b * Hkv + g) * tiles_per_bg + r * ceil(qbs / tt) + m.
@@ -390,13 +429,14 @@ __global__ void decode_plan_kernel(const int* __restrict__ lens, const int* __re
 #pragma unroll
     for (int c = 0; c < kOrderClasses; ++c) cnt[c] += ci == c;
   }
-  int pos[kOrderClasses];
+  __shared__ int class_sums[kOrderClasses * 32];
+  int pos[kOrderClasses], tot[kOrderClasses];
+  block_exclusive_scan_n<kOrderClasses>(cnt, pos, tot, class_sums);
   int base = 0;
 #pragma unroll
   for (int c = kOrderClasses - 1; c >= 0; --c) {
-    int total;
-    pos[c] = base + block_exclusive_scan(cnt[c], warp_sums, total);
-    base += total;
+    pos[c] += base;
+    base += tot[c];
   }
   for (int i = i0; i < i1; ++i) {
     const int ci = cls(i);
