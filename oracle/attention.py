@@ -383,6 +383,44 @@ def qsa_forward(q, k, v, sel_blocks, lo, hi, blk_base, tok_base, block_first, bl
     return out, lse
 
 
+def qsa_indexed_forward(q, k, v, sel_indices, lo, hi, block_first, block_last, scale=0.0625,
+                        block_size=4, rows=None):
+    """Indexed form of [QSA] (the notes name qsa_indexed_forward for callers that already hold
+    each query's selected block indices).  Row t of sel_indices [T, K] lists global block ids;
+    entries outside [0, NB) are unused.  Query token t sees key token j iff lo[t] <= j <= hi[t]
+    and j lies in the span [block_first[g], block_last[g]] of a listed block g (the listed
+    blocks of a row are distinct).  Returns the float64 output [T, Hq, D] and LSE [Hq, T]."""
+    if block_size != 4:
+        raise ValueError("block_size must be 4")
+    qf, kf, vf = f64(q), f64(k), f64(v)
+    T, Hq, D = qf.shape
+    Hkv = kf.shape[1]
+    G = Hq // Hkv
+    idx = sel_indices.numpy() if isinstance(sel_indices, torch.Tensor) else np.asarray(sel_indices)
+    first, last = i64(block_first), i64(block_last)
+    NB = first.size
+    lo_, hi_ = i64(lo), i64(hi)
+    ts = range(T) if rows is None else [int(t) for t in rows]
+    out = np.full((T, Hq, D), np.nan if rows is not None else 0.0)
+    lse = np.full((Hq, T), np.nan if rows is not None else -np.inf)
+    for t in ts:
+        spans = []
+        for g in idx[t]:
+            g = int(g)
+            if 0 <= g < NB:
+                a, e = max(first[g], lo_[t]), min(last[g], hi_[t])
+                if a <= e:
+                    spans.append(np.arange(a, e + 1))
+        j = np.sort(np.concatenate(spans)) if spans else np.zeros(0, np.int64)
+        vis = np.ones((1, j.size), bool)
+        for g in range(Hkv):
+            o, s = masked_softmax_attention(qf[t, None, g * G:(g + 1) * G], kf[j, g], vf[j, g],
+                                            vis, float(scale))
+            out[t, g * G:(g + 1) * G] = o[0]
+            lse[g * G:(g + 1) * G, t] = s[0]
+    return out, lse
+
+
 # ----------------------------------------------------------------------------------------
 # Work accounting: exact visible-pair counts (FLOPs = 4 * D * pairs).
 # ----------------------------------------------------------------------------------------
@@ -440,4 +478,18 @@ def qsa_visible_pairs(Hq, sel_blocks, lo, hi, block_first, block_last):
         a = np.maximum(first[g], lo_[t])
         e = np.minimum(last[g], hi_[t])
         total += int(np.maximum(e - a + 1, 0).sum())
+    return total * Hq
+
+
+def qsa_indexed_visible_pairs(Hq, sel_indices, lo, hi, block_first, block_last):
+    idx = sel_indices.numpy() if isinstance(sel_indices, torch.Tensor) else np.asarray(sel_indices)
+    lo_, hi_ = i64(lo), i64(hi)
+    first, last = i64(block_first), i64(block_last)
+    NB = first.size
+    total = 0
+    for t in range(lo_.size):
+        g = idx[t].astype(np.int64)
+        g = g[(g >= 0) & (g < NB)]
+        total += int(np.maximum(np.minimum(last[g], hi_[t]) - np.maximum(first[g], lo_[t]) + 1,
+                                0).sum())
     return total * Hq

@@ -161,3 +161,23 @@ def plan_bitmap(sel_blocks, lo, hi, block_first, block_last):
         indptr[t + 1] = indptr[t] + g.size
     indices = np.concatenate(parts) if parts else np.zeros(0, np.int64)
     return indptr.astype(np.int32), indices.astype(np.int32)
+
+
+def plan_indexed(sel_indices, lo, hi, block_first, block_last):
+    """Per-query CSR of the indexed form: row t keeps, in the caller's order, the entries g of
+    sel_indices[t] with 0 <= g < NB whose span [block_first[g], block_last[g]] meets
+    [lo[t], hi[t]]; every other entry is dropped."""
+    idx = sel_indices.numpy() if hasattr(sel_indices, "numpy") else np.asarray(sel_indices)
+    lo_, hi_ = i64(lo), i64(hi)
+    first, last = i64(block_first), i64(block_last)
+    NB = first.size
+    T = lo_.size
+    indptr = np.zeros(T + 1, dtype=np.int64)
+    parts = []
+    for t in range(T):
+        keep = [int(g) for g in idx[t]
+                if 0 <= int(g) < NB and max(first[g], lo_[t]) <= min(last[g], hi_[t])]
+        parts.append(np.array(keep, dtype=np.int64))
+        indptr[t + 1] = indptr[t] + len(keep)
+    indices = np.concatenate(parts) if parts else np.zeros(0, np.int64)
+    return indptr.astype(np.int32), indices.astype(np.int32)

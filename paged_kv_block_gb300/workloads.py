@@ -378,8 +378,39 @@ def make_qsa_problem(seed, seq_lens, Hq, Hkv, D, *, block_size=4, n_near=16, n_r
                 block_size=block_size)
 
 
+def make_qsa_indexed_problem(seed, seq_lens, Hq, Hkv, D, *, block_size=4, n_near=16,
+                             n_random=256, scale=None, extra_cols=0, junk=0.0):
+    """The selection of make_qsa_problem given as index rows (the indexed form):
+    sel_indices [T, K] int32, row t holding its selected global block ids and -1 for unused
+    entries, all in a seeded random order.  K = the largest row count + extra_cols.  A
+    fraction `junk` of the unused entries hold instead the id of a block past hi[t] (a
+    listed block with no visible key)."""
+    p = make_qsa_problem(seed, seq_lens, Hq, Hkv, D, block_size=block_size, n_near=n_near,
+                         n_random=n_random, scale=scale)
+    sel = p["sel_blocks"].numpy()
+    T, NB = sel.shape
+    rng = np.random.default_rng(seed + 7)
+    r, c = np.nonzero(sel)
+    counts = np.bincount(r, minlength=T)
+    K = max(1, int(counts.max(initial=0)) + int(extra_cols))
+    start = np.concatenate([[0], np.cumsum(counts)])
+    idx = np.full((T, K), -1, dtype=np.int32)
+    idx[r, np.arange(r.size) - start[r]] = c
+    if junk > 0:
+        hi_blk = p["hi"].numpy().astype(np.int64) // block_size
+        free = np.arange(K)[None, :] >= counts[:, None]
+        pick = free & (rng.random((T, K)) < junk)
+        cand = hi_blk[:, None] + 1 + rng.integers(0, 8, size=(T, K))
+        pick &= cand < NB
+        idx[pick] = cand[pick].astype(np.int32)
+    idx = np.take_along_axis(idx, np.argsort(rng.random((T, K)), axis=1), axis=1)
+    p = dict(p, form="qsa_indexed", sel_indices=torch.from_numpy(np.ascontiguousarray(idx)))
+    del p["sel_blocks"]
+    return p
+
+
 # ----------------------------------------------------------------------------------------
-# The five named workloads
+# The named workloads
 # ----------------------------------------------------------------------------------------
 
 def tiny_bsr(seed=1001):
@@ -430,3 +461,10 @@ def qsa_t32k(seed=1005, lens=(4096, 8192, 8192, 12288)):
     Hkv=2, D=256, block 4, 16 nearest + 256 random earlier blocks, scale 1/16."""
     return make_qsa_problem(seed, list(lens), Hq=24, Hkv=2, D=256, block_size=4, n_near=16,
                             n_random=256, scale=1.0 / 16)
+
+
+def qsa_t32k_indexed(seed=1005, lens=(4096, 8192, 8192, 12288)):
+    """qsa_t32k's selection as index rows (indexed form): sel_indices [32768, 272] int32, each
+    row's selected block ids in a seeded random order (rows with fewer blocks padded with -1)."""
+    return make_qsa_indexed_problem(seed, list(lens), Hq=24, Hkv=2, D=256, block_size=4,
+                                    n_near=16, n_random=256, scale=1.0 / 16)

@@ -198,3 +198,35 @@ def decode_bruteforce(prob):
                 O[row, h], LSE[row, h] = o, s
             row += 1
     return O.reshape(tuple(q.shape)), LSE.reshape(tuple(q.shape[:-1]))
+
+
+def qsa_indexed_visible(prob, t):
+    """Visible key tokens of query t in the indexed form: walk the keys in [lo, hi] and keep
+    those whose block (found by scanning the spans) is listed in row t."""
+    first = [int(x) for x in prob["block_first"]]
+    last = [int(x) for x in prob["block_last"]]
+    listed = set(int(g) for g in prob["sel_indices"][t])
+    out = []
+    for j in range(int(prob["lo"][t]), int(prob["hi"][t]) + 1):
+        for g in range(len(first)):
+            if first[g] <= j <= last[g]:
+                if g in listed:
+                    out.append(j)
+                break
+    return out
+
+
+def qsa_indexed_bruteforce(prob):
+    q, k, v = prob["q"], prob["k"], prob["v"]
+    T, Hq, D = q.shape
+    G = Hq // k.shape[1]
+    O = np.zeros((T, Hq, D))
+    LSE = np.zeros((Hq, T))
+    for t in range(T):
+        js = qsa_indexed_visible(prob, t)
+        for h in range(Hq):
+            keys = [_vec(k[j, h // G].float()) for j in js]
+            vals = [_vec(v[j, h // G].float()) for j in js]
+            o, s = _softmax_row(_vec(q[t, h].float()), keys, vals, prob["scale"])
+            O[t, h], LSE[h, t] = o, s
+    return O, LSE

@@ -127,6 +127,34 @@ def test_qsa_matches_bruteforce():
 # library special case: torch SDPA in float64 with an explicit mask
 # ----------------------------------------------------------------------------------------
 
+def _run_qsa_indexed(p, **kw):
+    return A.qsa_indexed_forward(p["q"], p["k"], p["v"], p["sel_indices"], p["lo"], p["hi"],
+                                 p["block_first"], p["block_last"], p["scale"], p["block_size"],
+                                 **kw)
+
+
+@pytest.mark.parametrize("extra,junk", [(0, 0.0), (3, 0.5)])
+def test_qsa_indexed_matches_bruteforce(extra, junk):
+    p = W.make_qsa_indexed_problem(37, [16, 12], Hq=2, Hkv=1, D=8, block_size=4, n_near=2,
+                                   n_random=2, extra_cols=extra, junk=junk)
+    o, s = _run_qsa_indexed(p)
+    ob, sb = BF.qsa_indexed_bruteforce(p)
+    _close(o, ob)
+    _close(s, sb)
+
+
+def test_qsa_indexed_equals_bitmap_form():
+    """The same selection as index rows (any order, padded, with listed blocks past hi) and
+    as a bitmap gives the same result."""
+    kw = dict(Hq=4, Hkv=2, D=16, block_size=4, n_near=3, n_random=4)
+    pi = W.make_qsa_indexed_problem(38, [24, 40], extra_cols=5, junk=0.3, **kw)
+    pb = W.make_qsa_problem(38, [24, 40], **kw)
+    o_i, s_i = _run_qsa_indexed(pi)
+    o_b, s_b = _run_qsa(pb)
+    _close(o_i, o_b, 1e-13)
+    _close(s_i, s_b, 1e-13)
+
+
 def test_prefill_matches_torch_sdpa():
     p = W.make_prefill_problem(11, q_lens=[7, 12], prefix_lens=[9, 3], Hq=6, Hkv=2, D=16,
                                page_size=8, mask_type="causal", window_left=5)

@@ -112,6 +112,21 @@ def test_decode_work_order_is_a_stable_size_class_sort():
     assert size[0] == chunk and size[-1] == min(items[:, 3] - items[:, 2])
 
 
+def test_indexed_csr_keeps_caller_order_and_drops_what_cannot_be_seen():
+    p = W.make_qsa_indexed_problem(5, [16, 24], Hq=2, Hkv=1, D=8, block_size=4, n_near=2,
+                                   n_random=3, extra_cols=4, junk=0.5)
+    idx = p["sel_indices"].numpy().copy()
+    NB = p["block_first"].numel()
+    idx[3, 0] = NB + 5                           # out of range: dropped
+    indptr, indices = PL.plan_indexed(idx, p["lo"], p["hi"], p["block_first"], p["block_last"])
+    for t in range(idx.shape[0]):
+        row = indices[indptr[t]:indptr[t + 1]].tolist()
+        seen = BF.qsa_indexed_visible(dict(p, sel_indices=idx), t)
+        # exactly the listed blocks that hold a visible key, in the order listed
+        want = [int(g) for g in idx[t] if 0 <= g < NB and any(4 * g <= j <= 4 * g + 3 for j in seen)]
+        assert row == want
+
+
 def test_decode_chunk_formula():
     # floor(64 * 8 * 64 / (16 * 152)) = 13 tiles of 128 keys
     assert PL.decode_split_chunk(64, 8, 8192, 152) == 1664
