@@ -205,6 +205,18 @@ def qsa_pairs(p):
         p["q"].shape[1]
 
 
+def qsa_indexed_pairs(p):
+    idx = p["sel_indices"].numpy()
+    NB = p["block_first"].numel()
+    t, c = np.nonzero((idx >= 0) & (idx < NB))
+    g = idx[t, c].astype(np.int64)
+    lo, hi = p["lo"].numpy()[t].astype(np.int64), p["hi"].numpy()[t].astype(np.int64)
+    first = p["block_first"].numpy()[g].astype(np.int64)
+    last = p["block_last"].numpy()[g].astype(np.int64)
+    return int(np.maximum(np.minimum(last, hi) - np.maximum(first, lo) + 1, 0).sum()) * \
+        p["q"].shape[1]
+
+
 # ----------------------------------------------------------------------------------------
 # one workload on the GPU
 # ----------------------------------------------------------------------------------------
@@ -224,6 +236,8 @@ def make_workload(name):
         return W.long_bsr()
     if name == "qsa_t32k":
         return W.qsa_t32k()
+    if name == "qsa_t32k_indexed":
+        return W.qsa_t32k_indexed()
     raise ValueError(name)
 
 
@@ -248,8 +262,11 @@ def describe(name, p):
                 "total_q": int(p["q"].shape[0]), "num_qo_heads": int(p["q"].shape[1]),
                 "page_size": int(p["page_size"]), "mask": p["mask_type"],
                 "window_left": p["window_left"]}
-    return {"workload": name, "tokens": int(p["q"].shape[0]), "num_qo_heads": int(p["q"].shape[1]),
-            "head_dim": int(p["q"].shape[2]), "num_blocks": int(p["sel_blocks"].shape[1])}
+    d = {"workload": name, "tokens": int(p["q"].shape[0]), "num_qo_heads": int(p["q"].shape[1]),
+         "head_dim": int(p["q"].shape[2]), "num_blocks": int(p["block_first"].numel())}
+    if p["form"] == "qsa_indexed":
+        d["index_width"] = int(p["sel_indices"].shape[1])
+    return d
 
 
 class Runner:
@@ -296,10 +313,16 @@ class Runner:
             self.out = torch.empty_like(d["q"])
             self.lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
         else:
-            self.params = pkb.qsa_params(d["q"], d["k"], d["sel_blocks"].shape[1],
-                                         scale=p["scale"])
-            self.meta = pkb.qsa_meta(d["sel_blocks"], d["lo"], d["hi"], d["blk_base"],
-                                     d["tok_base"], d["block_first"], d["block_last"])
+            if self.form == "qsa_indexed":
+                self.params = pkb.qsa_indexed_params(d["q"], d["k"], d["block_first"].numel(),
+                                                     d["sel_indices"].shape[1], scale=p["scale"])
+                self.meta = pkb.qsa_indexed_meta(d["sel_indices"], d["lo"], d["hi"],
+                                                 d["block_first"], d["block_last"])
+            else:
+                self.params = pkb.qsa_params(d["q"], d["k"], d["sel_blocks"].shape[1],
+                                             scale=p["scale"])
+                self.meta = pkb.qsa_meta(d["sel_blocks"], d["lo"], d["hi"], d["blk_base"],
+                                         d["tok_base"], d["block_first"], d["block_last"])
             self.ws = torch.empty(pkb.paged_attn_workspace_size(self.params), dtype=torch.uint8,
                                   device=dev)
             self.out = torch.empty_like(d["q"])
@@ -316,7 +339,9 @@ class Runner:
                  "prefill": ["q", "k_cache", "v_cache", "qo_indptr", "block_tables",
                              "seq_lens_kv"],
                  "qsa": ["q", "k", "v", "sel_blocks", "lo", "hi", "blk_base", "tok_base",
-                         "block_first", "block_last"]}[self.form]
+                         "block_first", "block_last"],
+                 "qsa_indexed": ["q", "k", "v", "sel_indices", "lo", "hi", "block_first",
+                                 "block_last"]}[self.form]
         return [(n, self.d[n]) for n in names if isinstance(self.d.get(n), torch.Tensor)]
 
     def step(self):
@@ -531,10 +556,11 @@ def main():
         kernel, bound, peak = "decode_split_kernel", "hbm", pk["hbm_gbs"]
     else:
         nbytes = None
-        units = {"bsr": bsr_pairs, "prefill": prefill_pairs, "qsa": qsa_pairs}[p["form"]](p)
+        units = {"bsr": bsr_pairs, "prefill": prefill_pairs, "qsa": qsa_pairs,
+                 "qsa_indexed": qsa_indexed_pairs}[p["form"]](p)
         units *= 4 * p["q"].shape[-1]
         unit, scale = "TFLOP/s", 1e12
-        kernel = "qsa_kernel" if p["form"] == "qsa" else "attn_tc_kernel"
+        kernel = "qsa_kernel" if p["form"] in ("qsa", "qsa_indexed") else "attn_tc_kernel"
         bound, peak = "tensor", pk["bf16_tflops"]
     value = units * world / (ms_step * 1e-3) / scale
     achieved = units / (kernel_ms * 1e-3) / scale
@@ -565,7 +591,7 @@ def main():
     if not args.no_extra and rank == 0:
         extra = {}
         for name in ("decode_b64_sq4", "tiny_bsr", "prefill_b16", "prefill_b16_w1023",
-                     "long_bsr", "qsa_t32k"):
+                     "long_bsr", "qsa_t32k", "qsa_t32k_indexed"):
             if name == args.workload:
                 continue
             try:
@@ -585,7 +611,8 @@ def main():
                     del rr
                     torch.cuda.empty_cache()
                     continue
-                n = {"bsr": bsr_pairs, "prefill": prefill_pairs, "qsa": qsa_pairs}[q["form"]](q)
+                n = {"bsr": bsr_pairs, "prefill": prefill_pairs, "qsa": qsa_pairs,
+                     "qsa_indexed": qsa_indexed_pairs}[q["form"]](q)
                 flops = 4 * q["q"].shape[-1] * n
                 extra[name] = {"tflops_step": flops / (reg / steps * 1e-3) / 1e12,
                                "tflops_kernel": flops / (kms * 1e-3) / 1e12,

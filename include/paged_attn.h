@@ -64,6 +64,8 @@ extern "C" {
 
 #define PAGED_ATTN_FORM_BSR 0    /* [BSA]: BSR rows per (request, KV head, query block) */
 #define PAGED_ATTN_FORM_BITMAP 1 /* [QSA]: uint8 block bitmap per packed query token    */
+#define PAGED_ATTN_FORM_INDEXED 2 /* [QSA] notes (qsa_indexed_forward): each packed query
+                                    token's selected global block ids as an index row  */
 
 /* Static description of a sparse launch (everything the plan's size depends on).
  * [BSA] signature and parameters; [QSA] signature and parameters. */
@@ -84,12 +86,14 @@ typedef struct paged_attn_params {
   int max_seq_len_kv;    /* static bound on seq_lens_kv, used for planning ([BSA])        */
   int mask_type;         /* PAGED_ATTN_MASK_DENSE or _CAUSAL, inside each block          */
   int has_valid_bits;    /* 1: kv_valid_bits_dev is given                                */
-  /* BITMAP only */
-  int num_blocks;        /* NB: columns of sel_blocks                                    */
+  /* BITMAP and INDEXED */
+  int num_blocks;        /* NB: columns of sel_blocks; blocks in block_first/last        */
   int block_size;        /* tokens per block: must be 4 ([QSA] block_size)               */
   int max_blocks_per_query; /* plan capacity: selected blocks per query on average over
-                               the launch (0 = NB)                                       */
+                               the launch (0 = NB for BITMAP, index_width for INDEXED)   */
   float sm_scale;        /* softmax scale; <= 0 selects 1/sqrt(D) ([BSA] sm_scale)        */
+  /* INDEXED only */
+  int index_width;       /* K: entries per index row of sel_indices                      */
 } paged_attn_params;
 
 /* Device metadata of a sparse launch.  Unused pointers may be NULL.  Layouts follow the
@@ -112,6 +116,12 @@ typedef struct paged_attn_meta {
   const int32_t* tok_base_dev;       /* [T] first token of the query's sequence           */
   const int32_t* block_first_dev;    /* [NB] inclusive token span of each block, in       */
   const int32_t* block_last_dev;     /* [NB] increasing order                              */
+  /* INDEXED (the [QSA] notes' indexed entry point; the pages give no signature): lo, hi,
+   * block_first and block_last as above, plus */
+  const int32_t* sel_indices_dev;    /* [T, K]: row t lists the global block ids query t
+                                        selects, distinct, in any order; negative entries
+                                        are unused; ids >= NB break the contract (dropped,
+                                        metadata status bit)                              */
 } paged_attn_meta;
 
 /* Workspace bytes needed by paged_attn_plan + paged_attn_run for these static params
@@ -136,12 +146,14 @@ int paged_attn_validate_bsr(const paged_attn_params* params, const int32_t* kv_i
  *   BSR:    a list of M-tiles (<= 256 rows of (token, head-in-group)), each with the
  *           block_indices slice of its BSR row, sorted by block count (largest first).
  *   BITMAP: a per-query CSR of selected global block ids meeting [lo, hi] (ascending).
+ *   INDEXED: the same CSR from the index rows: each row's ids in [0, NB) whose span meets
+ *           [lo, hi], in the row's order (no [T, NB] scan).
  * Reads only the metadata; writes only the workspace.  Clears the status word. */
 int paged_attn_plan(const paged_attn_params* params, const paged_attn_meta* meta,
                     void* workspace_dev, size_t workspace_bytes, void* stream);
 
 /* Run the planned launch.
- *   q_dev:   BSR [B, Sq, Hq, D]; BITMAP [T, Hq, D]                                ([BSA] q)
+ *   q_dev:   BSR [B, Sq, Hq, D]; BITMAP and INDEXED [T, Hq, D]                    ([BSA] q)
  *   k_dev:   BSR: K pool [P, Hkv, ps, D] or the combined cache [P, 2, Hkv, ps, D];
  *            BITMAP: k [T, Hkv, D]
  *   v_dev:   BSR: V pool [P, Hkv, ps, D] (NULL with a combined cache); BITMAP: v [T, Hkv, D]

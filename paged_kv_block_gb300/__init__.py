@@ -21,7 +21,7 @@ import torch
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libpagedattn.so")
 
-FORM_BSR, FORM_BITMAP = 0, 1
+FORM_BSR, FORM_BITMAP, FORM_INDEXED = 0, 1, 2
 MASK = {"dense": 0, "causal": 1}
 
 OK = 0
@@ -41,14 +41,16 @@ class AttnParams(C.Structure):
                 ("q_block_size", C.c_int), ("kv_block_size", C.c_int),
                 ("max_seq_len_kv", C.c_int), ("mask_type", C.c_int), ("has_valid_bits", C.c_int),
                 ("num_blocks", C.c_int), ("block_size", C.c_int),
-                ("max_blocks_per_query", C.c_int), ("sm_scale", C.c_float)]
+                ("max_blocks_per_query", C.c_int), ("sm_scale", C.c_float),
+                ("index_width", C.c_int)]
 
 
 class AttnMeta(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in (
         "kv_indptr_dev", "kv_indices_dev", "block_indptr_dev", "block_indices_dev",
         "seq_lens_kv_dev", "kv_valid_bits_dev", "sel_blocks_dev", "lo_dev", "hi_dev",
-        "blk_base_dev", "tok_base_dev", "block_first_dev", "block_last_dev")]
+        "blk_base_dev", "tok_base_dev", "block_first_dev", "block_last_dev",
+        "sel_indices_dev")]
 
 
 class PrefillParams(C.Structure):
@@ -464,6 +466,46 @@ def qsa_forward(q, k, v, sel_blocks, lo, hi, blk_base, tok_base, block_first, bl
     params = qsa_params(q, k, sel_blocks.shape[1], scale=scale, block_size=block_size,
                         max_blocks_per_query=max_blocks_per_query)
     meta = qsa_meta(sel_blocks, lo, hi, blk_base, tok_base, block_first, block_last)
+    out = torch.empty_like(q)
+    out_fp32 = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    lse = torch.empty(Hq, T, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = _workspace(paged_attn_workspace_size(params), q.device)
+    paged_attn_plan(params, meta, workspace, stream)
+    paged_attn_run(params, meta, q, k, v, out, out_fp32, lse, workspace, stream)
+    return out, out_fp32, lse
+
+
+def qsa_indexed_params(q, k, num_blocks, index_width, *, scale=0.0625, block_size=4,
+                       max_blocks_per_query=0) -> AttnParams:
+    p = qsa_params(q, k, num_blocks, scale=scale, block_size=block_size,
+                   max_blocks_per_query=max_blocks_per_query)
+    p.form = FORM_INDEXED
+    p.index_width = int(index_width)
+    return p
+
+
+def qsa_indexed_meta(sel_indices, lo, hi, block_first, block_last) -> AttnMeta:
+    m = AttnMeta()
+    m.sel_indices_dev = _dev(sel_indices, "sel_indices")
+    m.lo_dev, m.hi_dev = _dev(lo, "lo"), _dev(hi, "hi")
+    m.block_first_dev = _dev(block_first, "block_first")
+    m.block_last_dev = _dev(block_last, "block_last")
+    return m
+
+
+def qsa_indexed_forward(q, k, v, sel_indices, lo, hi, block_first, block_last, scale=0.0625,
+                        block_size=4, *, max_blocks_per_query=0, workspace=None, stream=None):
+    """Per-query block sparse attention from index rows sel_indices [T, K] int32 (each query
+    token's selected global block ids; negative entries unused): the indexed entry point the
+    [QSA] notes recommend when the indices already exist.  Returns (out bf16, out_fp32,
+    lse [Hq, T])."""
+    if not math.isfinite(scale):
+        raise ValueError("scale must be finite")
+    T, Hq, D = q.shape
+    params = qsa_indexed_params(q, k, block_first.numel(), sel_indices.shape[1], scale=scale,
+                                block_size=block_size, max_blocks_per_query=max_blocks_per_query)
+    meta = qsa_indexed_meta(sel_indices, lo, hi, block_first, block_last)
     out = torch.empty_like(q)
     out_fp32 = torch.empty(q.shape, dtype=torch.float32, device=q.device)
     lse = torch.empty(Hq, T, dtype=torch.float32, device=q.device)

@@ -80,8 +80,9 @@ bool sparse_params_ok(const paged_attn_params* p) {
     if (static_cast<long long>(p->batch) * p->q_len >= (1LL << 31)) return false;
     return true;
   }
-  if (p->form == PAGED_ATTN_FORM_BITMAP) {
+  if (p->form == PAGED_ATTN_FORM_BITMAP || p->form == PAGED_ATTN_FORM_INDEXED) {
     if (p->head_dim != 256 || p->block_size != 4 || p->num_blocks < 0) return false;
+    if (p->form == PAGED_ATTN_FORM_INDEXED && p->index_width <= 0) return false;
     return true;
   }
   return false;
@@ -113,7 +114,8 @@ SparseLayout sparse_layout(const paged_attn_params* p) {
     s.offs = l.take(ints * sizeof(int));
   } else {
     const long long T = p->q_len;
-    const long long mb = p->max_blocks_per_query > 0 ? p->max_blocks_per_query : p->num_blocks;
+    const long long mb = p->max_blocks_per_query > 0 ? p->max_blocks_per_query
+                         : (p->form == PAGED_ATTN_FORM_INDEXED ? p->index_width : p->num_blocks);
     s.bitmap_capacity = T * (mb > 0 ? mb : 1);
     s.indptr = l.take(sizeof(int) * static_cast<size_t>(T + 1));
     s.indices = l.take(sizeof(int) * static_cast<size_t>(s.bitmap_capacity));
@@ -510,6 +512,14 @@ int paged_attn_plan(const paged_attn_params* p, const paged_attn_meta* m, void* 
                      s.tile_tokens, tmp, st);
     launch_tile_sort(tmp, at<TileRec>(ws, s.sorted), nullptr, s.capacity, s.capacity, s.max_cost,
                      at<int>(ws, s.hist), at<int>(ws, s.offs), st);
+  } else if (p->form == PAGED_ATTN_FORM_INDEXED) {
+    if (!m->sel_indices_dev || !m->lo_dev || !m->hi_dev || !m->block_first_dev ||
+        !m->block_last_dev)
+      return PAGED_ATTN_ERR_INVALID_ARGUMENT;
+    launch_indexed_plan(m->sel_indices_dev, p->index_width, m->lo_dev, m->hi_dev,
+                        m->block_first_dev, m->block_last_dev, p->q_len, p->num_blocks,
+                        s.bitmap_capacity, at<int>(ws, s.indptr), at<int>(ws, s.indices), status,
+                        st);
   } else {
     if (!m->sel_blocks_dev || !m->lo_dev || !m->hi_dev || !m->block_first_dev || !m->block_last_dev)
       return PAGED_ATTN_ERR_INVALID_ARGUMENT;
@@ -530,7 +540,7 @@ int paged_attn_run(const paged_attn_params* p, const paged_attn_meta* m, const v
   uint32_t* status = at<uint32_t>(ws, s.status);
   const int D = p->head_dim;
   const float scale = p->sm_scale > 0.f ? p->sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
-  if (p->form == PAGED_ATTN_FORM_BITMAP) {
+  if (p->form == PAGED_ATTN_FORM_BITMAP || p->form == PAGED_ATTN_FORM_INDEXED) {
     if (!v) return PAGED_ATTN_ERR_INVALID_ARGUMENT;
     paged_attn_params pp = *p;
     pp.sm_scale = scale;

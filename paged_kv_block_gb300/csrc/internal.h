@@ -62,6 +62,12 @@ void launch_bitmap_plan(const uint8_t* sel, const int* lo, const int* hi, const 
                         const int* blast, int T, int NB, long long capacity, int* indptr,
                         int* indices, uint32_t* status, cudaStream_t st);
 
+// Indexed form: per-query CSR from index rows [T, K] (caller order; negative entries unused;
+// ids >= NB dropped and reported as kErrMetadata; ids whose span misses [lo, hi] dropped).
+void launch_indexed_plan(const int* idx, int K, const int* lo, const int* hi, const int* bfirst,
+                         const int* blast, int T, int NB, long long capacity, int* indptr,
+                         int* indices, uint32_t* status, cudaStream_t st);
+
 // Split-KV work list, its claim order (items by size class, largest first; stable), and
 // zeroed work / merge counters (B * Hkv + 1 ints).  Request b has
 // qo_indptr[b + 1] - qo_indptr[b] queries (qo_indptr != nullptr) or q_len; packed offsets

@@ -334,6 +334,48 @@ __global__ void counts_to_indptr_kernel(const int* __restrict__ counts, int T, l
   }
 }
 
+// ---- indexed per-query block plan --------------------------------------------------------
+// One warp per query token t: the K entries of row t are read 32 at a time (coalesced); an
+// entry g is kept when 0 <= g < NB and its span meets [lo[t], hi[t]], in the caller's order
+// (ballot compaction).  Entries >= NB break the contract: they are dropped and reported.
+// kFill = false writes the count of row t; kFill = true writes the ids from indptr[t] on.
+template <bool kFill>
+__global__ void indexed_scan_kernel(const int* __restrict__ idx, int K,
+                                    const int* __restrict__ lo, const int* __restrict__ hi,
+                                    const int* __restrict__ bfirst,
+                                    const int* __restrict__ blast, int T, int NB,
+                                    int* __restrict__ counts, const int* __restrict__ indptr,
+                                    int* __restrict__ indices, long long capacity,
+                                    uint32_t* status) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int l = lo[t], h = hi[t];
+  long long written = kFill ? indptr[t] : 0;
+  const long long rowbase = static_cast<long long>(t) * K;
+  bool bad = false;
+  for (int base = 0; base < K; base += 32) {
+    const int e = base + lane;
+    bool keep = false;
+    int g = -1;
+    if (e < K) {
+      g = idx[rowbase + e];
+      if (g >= NB) bad = true;
+      else if (g >= 0) keep = max(bfirst[g], l) <= min(blast[g], h);
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    if (kFill && keep) {
+      const long long at = written + __popc(m & ((1u << lane) - 1u));
+      if (at < capacity) indices[at] = g;
+    }
+    written += __popc(m);
+  }
+  if (!kFill) {
+    if (__any_sync(0xffffffffu, bad) && lane == 0) report_error(status, kErrMetadata);
+    if (lane == 0) counts[t] = static_cast<int>(written);
+  }
+}
+
 // ---- decode split planner -----------------------------------------------------------------
 __device__ __forceinline__ void decode_split_range(int L, int nq, int chunk, int window_left,
                                                    int& lo, int& s0, int& n) {
@@ -503,6 +545,20 @@ void launch_bitmap_plan(const uint8_t* sel, const int* lo, const int* hi, const 
   counts_to_indptr_kernel<<<1, 1024, 0, st>>>(indptr + 1, T, capacity, indptr, status);
   bitmap_scan_kernel<true><<<grid, 32 * warps_per_cta, 0, st>>>(
       sel, lo, hi, bfirst, blast, T, NB, nullptr, indptr, indices, capacity);
+  count_launches(3);
+}
+
+void launch_indexed_plan(const int* idx, int K, const int* lo, const int* hi, const int* bfirst,
+                         const int* blast, int T, int NB, long long capacity, int* indptr,
+                         int* indices, uint32_t* status, cudaStream_t st) {
+  if (T <= 0) return;
+  const int warps_per_cta = 8;
+  const int grid = ceil_div(T, warps_per_cta);
+  indexed_scan_kernel<false><<<grid, 32 * warps_per_cta, 0, st>>>(
+      idx, K, lo, hi, bfirst, blast, T, NB, indptr + 1, nullptr, nullptr, capacity, status);
+  counts_to_indptr_kernel<<<1, 1024, 0, st>>>(indptr + 1, T, capacity, indptr, status);
+  indexed_scan_kernel<true><<<grid, 32 * warps_per_cta, 0, st>>>(
+      idx, K, lo, hi, bfirst, blast, T, NB, nullptr, indptr, indices, capacity, status);
   count_launches(3);
 }
 
