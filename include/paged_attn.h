@@ -62,6 +62,12 @@ extern "C" {
 #define PAGED_ATTN_MASK_DENSE 0
 #define PAGED_ATTN_MASK_CAUSAL 1
 
+/* Output element types ([PRE] and [DEC] out_dtype).  Inputs are bf16; the normalised
+ * fp32 result is rounded to nearest-even into the output type. */
+#define PAGED_ATTN_DTYPE_BF16 0
+#define PAGED_ATTN_DTYPE_FP16 1
+#define PAGED_ATTN_DTYPE_FP32 2
+
 #define PAGED_ATTN_FORM_BSR 0    /* [BSA]: BSR rows per (request, KV head, query block) */
 #define PAGED_ATTN_FORM_BITMAP 1 /* [QSA]: uint8 block bitmap per packed query token    */
 #define PAGED_ATTN_FORM_INDEXED 2 /* [QSA] notes (qsa_indexed_forward): each packed query
@@ -178,6 +184,7 @@ typedef struct paged_prefill_params {
   int window_left;      /* -1 = no window; >= 0 needs the causal mask ([DEC] notes)       */
   float sm_scale;       /* <= 0 selects 1/sqrt(D) ([PRE] sm_scale)                         */
   float output_scale;   /* multiplies the normalised output ([PRE] output_scale)           */
+  int out_dtype;        /* PAGED_ATTN_DTYPE_* of out ([PRE] out_dtype; 0 = bf16)          */
 } paged_prefill_params;
 
 size_t paged_prefill_workspace_size(const paged_prefill_params* params);
@@ -186,7 +193,7 @@ size_t paged_prefill_workspace_size(const paged_prefill_params* params);
  *   q_dev [total_q, Hq, D]; k_cache_dev, v_cache_dev [P, Hkv, page_size, D] (HND);
  *   qo_indptr_dev [B + 1] (request b owns rows qo_indptr[b] : qo_indptr[b + 1]);
  *   block_tables_dev [B, C] row-strided physical page ids; seq_lens_kv_dev [B];
- *   out_dev [total_q, Hq, D] bf16; lse_dev [total_q, Hq] fp32 (optional).
+ *   out_dev [total_q, Hq, D] of out_dtype; lse_dev [total_q, Hq] fp32 (optional).
  * Every request needs len_q <= len_kv under the causal mask and ceil(len_kv / page_size)
  * <= C.  Table entries past a request's live pages are never read. */
 int paged_prefill_run(const paged_prefill_params* params, const void* q_dev,
@@ -218,6 +225,7 @@ typedef struct paged_decode_params {
                            query / out are [total_q, Hq, D], and every request has between
                            1 and max_seq_len_q queries (the static bound of [DEC])         */
   int total_q;          /* packed form: rows of query and out, = qo_indptr[B]              */
+  int out_dtype;        /* PAGED_ATTN_DTYPE_* of out ([DEC] out_dtype; 0 = bf16)          */
 } paged_decode_params;
 
 /* Workspace bytes for the decode plan and the fp32 split partials. */
@@ -237,7 +245,7 @@ int paged_decode_split_chunk(const paged_decode_params* params);
  *   qo_indptr[b] .. qo_indptr[b + 1]; the offsets start at 0, each step is between 1 and
  *   max_seq_len_q, and they end at total_q ([DEC] notes; a plan that sees them break
  *   this sets the metadata status bit and rows outside [0, total_q) are never written);
- *   out_dev: bf16 in the query's layout; lse_dev: fp32, one per output row and head
+ *   out_dev: out_dtype in the query's layout; lse_dev: fp32, one per output row and head
  *   (optional).
  * Under the causal mask every request needs nq <= len ([DEC] notes); a query before the
  * first key sees nothing and gets 0 / -inf.  A (request, KV head) unit of at most 64 rows

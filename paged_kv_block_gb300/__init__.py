@@ -23,6 +23,7 @@ LIB_PATH = os.path.join(HERE, "libpagedattn.so")
 
 FORM_BSR, FORM_BITMAP, FORM_INDEXED = 0, 1, 2
 MASK = {"dense": 0, "causal": 1}
+DTYPE = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 
 OK = 0
 ERR_INVALID_ARGUMENT = -1
@@ -58,7 +59,7 @@ class PrefillParams(C.Structure):
                 ("num_kv_heads", C.c_int), ("head_dim", C.c_int), ("page_size", C.c_int),
                 ("num_pages", C.c_int), ("max_pages_per_request", C.c_int),
                 ("mask_type", C.c_int), ("window_left", C.c_int), ("sm_scale", C.c_float),
-                ("output_scale", C.c_float)]
+                ("output_scale", C.c_float), ("out_dtype", C.c_int)]
 
 
 class DecodeParams(C.Structure):
@@ -67,7 +68,7 @@ class DecodeParams(C.Structure):
                 ("combined_cache", C.c_int), ("max_seq_len", C.c_int), ("mask_type", C.c_int),
                 ("window_left", C.c_int), ("bmm1_scale", C.c_float), ("bmm2_scale", C.c_float),
                 ("split_chunk", C.c_int), ("seq_len_q", C.c_int), ("max_seq_len_q", C.c_int),
-                ("total_q", C.c_int)]
+                ("total_q", C.c_int), ("out_dtype", C.c_int)]
 
 
 class PlanLayout(C.Structure):
@@ -350,31 +351,45 @@ def block_sparse_attention_with_paged_kv_cache(q, paged_kv_cache, paged_kv_indpt
     return out, lse
 
 
+def _out_dtype(out_dtype, out, q):
+    """[PRE]/[DEC] out_dtype: the given dtype, else out's dtype when out is given, else the
+    query's dtype."""
+    dt = out_dtype if out_dtype is not None else (out.dtype if out is not None else q.dtype)
+    if dt not in DTYPE:
+        raise ValueError(f"unsupported output dtype {dt}")
+    if out is not None and out.dtype != dt:
+        raise ValueError("out does not have out_dtype")
+    return dt
+
+
 def prefill_params(q, k_cache, block_tables, batch, *, mask_type="dense", window_left=-1,
-                   sm_scale=None, output_scale=1.0) -> PrefillParams:
+                   sm_scale=None, output_scale=1.0, out_dtype=torch.bfloat16) -> PrefillParams:
     total_q, Hq, D = q.shape
     P, Hkv, ps, _ = k_cache.shape
     return PrefillParams(batch=batch, total_q=total_q, num_qo_heads=Hq, num_kv_heads=Hkv,
                          head_dim=D, page_size=ps, num_pages=P,
                          max_pages_per_request=block_tables.shape[1],
                          mask_type=MASK[mask_type], window_left=int(window_left),
-                         sm_scale=float(sm_scale or 0.0), output_scale=float(output_scale))
+                         sm_scale=float(sm_scale or 0.0), output_scale=float(output_scale),
+                         out_dtype=DTYPE[out_dtype])
 
 
 def batch_prefill_with_paged_kv_cache(q, k_cache, v_cache, qo_indptr, block_tables, seq_lens_kv,
                                       *, page_size=32, kv_layout="HND", mask_type="dense",
                                       window_left=-1, sm_scale=None, output_scale=1.0,
-                                      out=None, lse=None, workspace=None, stream=None):
+                                      out_dtype=None, out=None, lse=None, workspace=None,
+                                      stream=None):
     """Plan + run one packed-Q prefill launch; returns (out, lse)."""
+    out_dtype = _out_dtype(out_dtype, out, q)
     if kv_layout != "HND":
         raise ValueError("only the HND layout is supported")
     if k_cache.shape[2] != page_size:
         raise ValueError("page_size does not match the pools")
     params = prefill_params(q, k_cache, block_tables, seq_lens_kv.numel(), mask_type=mask_type,
                             window_left=window_left, sm_scale=sm_scale,
-                            output_scale=output_scale)
+                            output_scale=output_scale, out_dtype=out_dtype)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     if workspace is None:
         workspace = _workspace(paged_prefill_workspace_size(params), q.device)
     paged_prefill_run(params, q, k_cache, v_cache, qo_indptr, block_tables, seq_lens_kv, out, lse,
@@ -384,7 +399,7 @@ def batch_prefill_with_paged_kv_cache(q, k_cache, v_cache, qo_indptr, block_tabl
 
 def decode_params(query, kv_cache, max_seq_len, *, bmm1_scale=None, bmm2_scale=1.0,
                   mask_type="dense", window_left=-1, split_chunk=0, seq_len_q=1,
-                  qo_indptr=None, max_seq_len_q=None) -> DecodeParams:
+                  qo_indptr=None, max_seq_len_q=None, out_dtype=torch.bfloat16) -> DecodeParams:
     """Static arguments of a decode call.  query is [B, Hq, D] (one query per request),
     [B, SQ, Hq, D] (seq_len_q = SQ > 1) or packed [total_q, Hq, D] with qo_indptr, whose
     static bound max_seq_len_q is then required."""
@@ -407,27 +422,28 @@ def decode_params(query, kv_cache, max_seq_len, *, bmm1_scale=None, bmm2_scale=1
                         mask_type=MASK[mask_type], window_left=int(window_left),
                         bmm1_scale=float(bmm1_scale or 0.0), bmm2_scale=float(bmm2_scale),
                         split_chunk=int(split_chunk), seq_len_q=int(sq), max_seq_len_q=max_sq,
-                        total_q=int(total_q))
+                        total_q=int(total_q), out_dtype=DTYPE[out_dtype])
 
 
 def batch_decode_with_paged_kv_cache(query, kv_cache, workspace_buffer, paged_kv_indptr,
                                      paged_kv_indices, seq_lens, max_seq_len, *, seq_len_q=1,
                                      qo_indptr=None, max_seq_len_q=None, bmm1_scale=None,
-                                     bmm2_scale=1.0, out=None, lse=None, mask_type="dense",
-                                     window_left=-1, kv_layout="HND", split_chunk=0,
-                                     stream=None):
+                                     bmm2_scale=1.0, out=None, out_dtype=None, lse=None,
+                                     mask_type="dense", window_left=-1, kv_layout="HND",
+                                     split_chunk=0, stream=None):
     """Decode with split-KV over a CSR page table; returns (out, lse).  One query per
     request ([B, Hq, D]), seq_len_q fixed queries ([B, SQ, Hq, D]) or packed queries
     ([total_q, Hq, D] with qo_indptr and its bound max_seq_len_q)."""
     if kv_layout != "HND":
         raise ValueError("only the HND layout is supported")
+    out_dtype = _out_dtype(out_dtype, out, query)
     params = decode_params(query, kv_cache, max_seq_len, bmm1_scale=bmm1_scale,
                            bmm2_scale=bmm2_scale, mask_type=mask_type, window_left=window_left,
                            split_chunk=split_chunk, seq_len_q=seq_len_q, qo_indptr=qo_indptr,
-                           max_seq_len_q=max_seq_len_q)
+                           max_seq_len_q=max_seq_len_q, out_dtype=out_dtype)
     k, v, *_ = _pools(kv_cache)
     if out is None:
-        out = torch.empty_like(query)
+        out = torch.empty(query.shape, dtype=out_dtype, device=query.device)
     if workspace_buffer is None:
         workspace_buffer = _workspace(paged_decode_workspace_size(params), query.device)
     paged_decode_run(params, query, k, v, paged_kv_indptr, paged_kv_indices, seq_lens, out, lse,

@@ -142,6 +142,7 @@ bool prefill_params_ok(const paged_prefill_params* p) {
   if (p->mask_type != PAGED_ATTN_MASK_DENSE && p->mask_type != PAGED_ATTN_MASK_CAUSAL) return false;
   if (p->window_left < -1) return false;
   if (p->window_left >= 0 && p->mask_type != PAGED_ATTN_MASK_CAUSAL) return false;
+  if (p->out_dtype < PAGED_ATTN_DTYPE_BF16 || p->out_dtype > PAGED_ATTN_DTYPE_FP32) return false;
   if (static_cast<long long>(p->num_pages) * p->num_kv_heads * p->page_size >= (1LL << 31))
     return false;
   return true;
@@ -202,6 +203,7 @@ bool decode_params_ok(const paged_decode_params* p) {
   if (p->window_left >= 0 && p->mask_type != PAGED_ATTN_MASK_CAUSAL) return false;
   if (p->split_chunk < 0 || p->split_chunk % 128) return false;
   if (p->seq_len_q < 0 || p->max_seq_len_q < 0 || p->total_q < 0) return false;
+  if (p->out_dtype < PAGED_ATTN_DTYPE_BF16 || p->out_dtype > PAGED_ATTN_DTYPE_FP32) return false;
   if (decode_packed(p)) {
     if (p->seq_len_q > 1) return false;                    // one form at a time
     if (p->total_q < p->batch) return false;               // every request owns >= 1 row
@@ -396,7 +398,8 @@ int decode_run_tiled(const paged_decode_params* p, const DecodeLayout& s, const 
   a.block_sparse = 0;
   a.block_indices = nullptr;
   a.kv_block_size = kKvTile;
-  a.out = static_cast<__nv_bfloat16*>(out);
+  a.out = out;
+  a.out_dtype = p->out_dtype;
   a.lse = lse;
   a.status = status;
   a.Hq = Hq;
@@ -580,7 +583,8 @@ int paged_attn_run(const paged_attn_params* p, const paged_attn_meta* m, const v
   a.block_sparse = 1;
   a.block_indices = m->block_indices_dev;
   a.kv_block_size = p->kv_block_size;
-  a.out = static_cast<__nv_bfloat16*>(out);
+  a.out = out;
+  a.out_dtype = PAGED_ATTN_DTYPE_BF16;
   a.lse = lse;
   a.status = status;
   a.Hq = Hq;
@@ -656,7 +660,8 @@ int paged_prefill_run(const paged_prefill_params* p, const void* q, const void* 
   a.block_sparse = 0;
   a.block_indices = nullptr;
   a.kv_block_size = kKvTile;
-  a.out = static_cast<__nv_bfloat16*>(out);
+  a.out = out;
+  a.out_dtype = p->out_dtype;
   a.lse = lse;
   a.status = status;
   a.Hq = Hq;
@@ -751,7 +756,8 @@ int paged_decode_run(const paged_decode_params* p, const void* query, const void
   a.order = order;
   a.part_o = at<float>(ws, s.part_o);
   a.part_lse = at<float>(ws, s.part_lse);
-  a.out = static_cast<__nv_bfloat16*>(out);
+  a.out = out;
+  a.out_dtype = p->out_dtype;
   a.lse = lse;
   a.status = status;
   a.B = p->batch;

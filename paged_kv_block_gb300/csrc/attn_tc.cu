@@ -689,14 +689,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mbar_arrive(&ctl->o_empty[w]);
           }
         }
-        if (row_valid) {
+        if (row_valid && a.out_dtype == kOutF32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * kD + q * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = have_o ? make_float4(__uint_as_float(ov[4 * i]) * inv,
+                                          __uint_as_float(ov[4 * i + 1]) * inv,
+                                          __uint_as_float(ov[4 * i + 2]) * inv,
+                                          __uint_as_float(ov[4 * i + 3]) * inv)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else if (row_valid) {
           uint32_t pkd[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            pkd[i] = have_o ? pack_bf16(__uint_as_float(ov[2 * i]) * inv,
-                                        __uint_as_float(ov[2 * i + 1]) * inv)
+            pkd[i] = have_o ? pack_out2(__uint_as_float(ov[2 * i]) * inv,
+                                        __uint_as_float(ov[2 * i + 1]) * inv, a.out_dtype)
                             : 0u;
-          uint4* dst = reinterpret_cast<uint4*>(a.out + orow * kD + q * 32);
+          uint4* dst =
+              reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * kD + q * 32);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);

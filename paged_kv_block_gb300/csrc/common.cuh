@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda.h>
 
 namespace pa {
@@ -38,6 +39,36 @@ __device__ __forceinline__ void report_error(uint32_t* status, uint32_t bit) {
 // timeout: later CTAs then skip their work so that a broken launch ends quickly.
 __device__ __forceinline__ bool launch_aborted(const uint32_t* status) {
   return status && (*reinterpret_cast<const volatile uint32_t*>(status) & kErrTimeout);
+}
+
+// Output element types (PAGED_ATTN_DTYPE_* of the C ABI): the normalised fp32 result is
+// rounded to nearest-even into the caller's type.
+constexpr int kOutBf16 = 0;
+constexpr int kOutF16 = 1;
+constexpr int kOutF32 = 2;
+
+__device__ __forceinline__ uint32_t pack_out2(float a, float b, int dt) {
+  if (dt == kOutF16) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+// One element at index i of `out`.
+__device__ __forceinline__ void store_out1(void* out, long long i, float v, int dt) {
+  if (dt == kOutF32) static_cast<float*>(out)[i] = v;
+  else if (dt == kOutF16) static_cast<__half*>(out)[i] = __float2half_rn(v);
+  else static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
+}
+// Four consecutive elements from index i (a multiple of 4).
+__device__ __forceinline__ void store_out4(void* out, long long i, float4 v, int dt) {
+  if (dt == kOutF32) {
+    reinterpret_cast<float4*>(static_cast<float*>(out) + i)[0] = v;
+  } else {
+    uint2* dst = reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + i);
+    dst[0] = make_uint2(pack_out2(v.x, v.y, dt), pack_out2(v.z, v.w, dt));
+  }
 }
 
 // Programmatic dependent launch.  A kernel launched with programmatic stream serialization

@@ -162,9 +162,9 @@ __device__ __forceinline__ void merge_rows(const DecodeLaunch& a, long long base
     if (qrow < 0 || qrow >= a.q_rows) continue;
     const float sc = wsum[r] > 0.f ? a.out_scale / wsum[r] : 0.f;
     const long long orow = static_cast<long long>(qrow) * a.Hq + g * G + m % G;
-    __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(a.out + orow * kD) + lane * 2;
-    dst[0] = __floats2bfloat162_rn(acc[r].x * sc, acc[r].y * sc);
-    dst[1] = __floats2bfloat162_rn(acc[r].z * sc, acc[r].w * sc);
+    store_out4(a.out, orow * kD + lane * 4,
+               make_float4(acc[r].x * sc, acc[r].y * sc, acc[r].z * sc, acc[r].w * sc),
+               a.out_dtype);
     if (a.lse && lane == 0) a.lse[orow] = wsum[r] > 0.f ? Mx[r] + __logf(wsum[r]) : -INFINITY;
   }
 }
@@ -608,7 +608,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           const int qrow = q_row0 + m / G;
           if (qrow < 0 || qrow >= a.q_rows) continue;
           const long long orow = static_cast<long long>(qrow) * a.Hq + g * G + m % G;
-          a.out[orow * kD + d] = __float2bfloat16_rn(on * a.out_scale);
+          store_out1(a.out, orow * kD + d, on * a.out_scale, a.out_dtype);
           if (a.lse && d == 0) a.lse[orow] = lse_nat;
         } else {
           const long long prow = static_cast<long long>(item) * M + m;

@@ -108,7 +108,8 @@ struct DecodeLaunch {
   const int* order;          // claim order: the k-th claimed item is items[order[k]]
   float* part_o;             // [items, M, D]
   float* part_lse;           // [items, M]
-  __nv_bfloat16* out;        // [q_rows, Hq, D]
+  void* out;                 // [q_rows, Hq, D] of out_dtype
+  int out_dtype;             // kOutBf16, kOutF16 or kOutF32
   float* lse;                // [q_rows, Hq] or nullptr
   uint32_t* status;
   int B, Hq, Hkv, D, page_size, page_rows, k_head_off, v_head_off, num_pages;
@@ -141,7 +142,8 @@ struct AttnLaunch {
   int block_sparse;          // 1: KV tiles walk block_indices; 0: dense KV tile ranges
   const int* block_indices;  // BSR form (may be null when no row lists a block)
   int kv_block_size;
-  __nv_bfloat16* out;
+  void* out;                 // rows of out_dtype
+  int out_dtype;             // kOutBf16, kOutF16 or kOutF32
   float* lse;
   uint32_t* status;
   int Hq, Hkv, G, D, page_size, page_rows, k_head_off, v_head_off, num_pages;
