@@ -232,6 +232,8 @@ def make_workload(name):
         return W.prefill_b16(window_left=-1)
     if name == "prefill_b16_w1023":
         return W.prefill_b16(window_left=1023)
+    if name == "prefill_b16_d256":
+        return W.prefill_b16_d256()
     if name == "long_bsr":
         return W.long_bsr()
     if name == "qsa_t32k":
@@ -260,6 +262,7 @@ def describe(name, p):
     if p["form"] == "prefill":
         return {"workload": name, "batch": int(p["seq_lens_kv"].numel()),
                 "total_q": int(p["q"].shape[0]), "num_qo_heads": int(p["q"].shape[1]),
+                "head_dim": int(p["q"].shape[2]),
                 "page_size": int(p["page_size"]), "mask": p["mask_type"],
                 "window_left": p["window_left"]}
     d = {"workload": name, "tokens": int(p["q"].shape[0]), "num_qo_heads": int(p["q"].shape[1]),
@@ -591,7 +594,7 @@ def main():
     if not args.no_extra and rank == 0:
         extra = {}
         for name in ("decode_b64_sq4", "tiny_bsr", "prefill_b16", "prefill_b16_w1023",
-                     "long_bsr", "qsa_t32k", "qsa_t32k_indexed"):
+                     "prefill_b16_d256", "long_bsr", "qsa_t32k", "qsa_t32k_indexed"):
             if name == args.workload:
                 continue
             try:

@@ -176,7 +176,7 @@ int paged_attn_run(const paged_attn_params* params, const paged_attn_meta* meta,
 typedef struct paged_prefill_params {
   int batch;            /* B                                                              */
   int total_q;          /* rows of q / out ([PRE] q: [total_q, Hq, D])                    */
-  int num_qo_heads, num_kv_heads, head_dim; /* D = 128                                    */
+  int num_qo_heads, num_kv_heads, head_dim; /* D = 128 or 256 ([PRE] notes)             */
   int page_size;        /* 16, 32, 64 or 128 ([PRE] summary)                              */
   int num_pages;        /* P                                                              */
   int max_pages_per_request; /* C: columns of block_tables ([PRE] block_tables [B, C])     */

@@ -135,7 +135,7 @@ bool prefill_params_ok(const paged_prefill_params* p) {
   if (p->batch < 0 || p->total_q < 0) return false;
   if (p->num_qo_heads <= 0 || p->num_kv_heads <= 0 || p->num_qo_heads % p->num_kv_heads) return false;
   const int G = p->num_qo_heads / p->num_kv_heads;
-  if (G > 128 || p->head_dim != 128) return false;
+  if (G > 128 || (p->head_dim != 128 && p->head_dim != 256)) return false;
   if (!(p->page_size == 16 || p->page_size == 32 || p->page_size == 64 || p->page_size == 128))
     return false;
   if (p->num_pages <= 0 || p->max_pages_per_request <= 0) return false;
@@ -154,7 +154,8 @@ PrefillLayout prefill_layout(const paged_prefill_params* p) {
   s.status = l.take(sizeof(uint32_t) * 4);
   s.n_tiles = s.status + sizeof(uint32_t);
   const int G = p->num_qo_heads / p->num_kv_heads;
-  s.tile_tokens = cta_tile_tokens(G);
+  // D = 128: two 128-row sub-tiles per tile; D = 256: one
+  s.tile_tokens = p->head_dim == 256 ? sub_tile_tokens(G) : cta_tile_tokens(G);
   s.capacity = static_cast<int>(static_cast<long long>(p->num_kv_heads) *
                                 (ceil_div(p->total_q, s.tile_tokens) + p->batch));
   const long long max_keys = static_cast<long long>(p->max_pages_per_request) * p->page_size;
@@ -641,7 +642,7 @@ int paged_prefill_run(const paged_prefill_params* p, const void* q, const void* 
                    at<int>(ws, s.offs), st);
   const float scale = p->sm_scale > 0.f ? p->sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
   AttnLaunch a{};
-  const int R = page_piece_rows(ps, kKvTile);
+  const int R = page_piece_rows(ps, D == 256 ? 64 : kKvTile);   // keys per KV tile: 64 / 128
   const long long pool_rows = static_cast<long long>(p->num_pages) * Hkv * ps;
   if (!encode_q_map(&a.qmap, q, p->total_q, Hq, D, G, sub_tile_tokens(G)) ||
       !encode_rows_map(&a.kmap, kc, pool_rows, D, R) || !encode_rows_map(&a.vmap, vc, pool_rows, D, R))
@@ -679,7 +680,7 @@ int paged_prefill_run(const paged_prefill_params* p, const void* q, const void* 
   a.out_scale = p->output_scale;
   void* tok;
   timer_begin(st, &tok);
-  const int rc = launch_attn(a, st);
+  const int rc = D == 256 ? launch_attn256(a, st) : launch_attn(a, st);
   timer_end(st, tok);
   if (rc == -2) return PAGED_ATTN_ERR_UNSUPPORTED;
   return rc == 0 ? PAGED_ATTN_OK : PAGED_ATTN_ERR_CUDA;

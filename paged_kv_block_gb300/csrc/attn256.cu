@@ -1,0 +1,510 @@
+// Dense packed-Q prefill (batch_prefill_with_paged_kv_cache, whose notes allow a head
+// dimension of 256) on the 5th-generation tensor cores, for D = 256.
+//
+// Persistent: one CTA per SM walks the prefill planner's tile list (largest first) with a
+// stride of the grid size.  A work tile is one Q sub-tile of 128 rows, a row being a
+// (token, head-in-group) pair, so the G query heads that share a KV head share every K/V
+// tile.  K and V are walked in 64-key tiles over the keys the tile's rows can see.
+// Roles (224 threads):
+//   warps 0-3  softmax + epilogue (thread t <-> TMEM lane t <-> row t)
+//   warp  4    TMA producer of Q (once per work tile) and K (2-stage ring)
+//   warp  5    TMEM owner and MMA issuer (one thread)
+//   warp  6    TMA producer of V (2-stage ring)
+// Tensor memory (512 columns allocated): S_0 [0,64) S_1 [64,128) O [128,384).  The scores of
+// KV tile i (counted over the whole launch) land in S_(i%2); P is written over the first 32
+// columns of that buffer as packed bf16 and read from TMEM by the PV MMA.  The MMA issuer
+// queues QK(i+2) behind PV(i), so the softmax of tile i+1 runs while PV(i) and QK(i+2) do.
+// Per 64-key tile the MMAs take 2 x 128 x 64 x 256 multiply-adds and the softmax 64 exp2 per
+// row, so one softmax warpgroup keeps up with the tensor core.
+// The online softmax runs in the log2 domain; the running maximum only moves (and O is
+// rescaled in TMEM) when a tile's maximum exceeds it by more than 8.
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kD = 256;
+constexpr int kKeys = 64;                      // keys per KV tile
+constexpr int kChunks = kD / 64;               // 64-column (128-byte) chunks of a row
+constexpr int kRows = 128;                     // rows of a Q sub-tile
+constexpr int kQChunk = kRows * 128;           // 128 rows x 64 columns of bf16
+constexpr int kQBytes = kChunks * kQChunk;     // 64 KB
+constexpr int kKvChunk = kKeys * 128;          // 64 keys x 64 columns
+constexpr int kKvBytes = kChunks * kKvChunk;   // 32 KB per K (or V) tile
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
+constexpr int kProdK = 4, kMmaWarp = 5, kProdV = 6;
+constexpr int kThreads = 7 * 32;
+constexpr int kTmemS = 0;                      // S_0, S_1: 64 columns each
+constexpr int kTmemO = 128;                    // O: 256 columns
+constexpr float kRescaleThreshold = 8.0f;      // log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct Ctrl {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t s_full[2], p_full[2];
+  uint64_t pv_done, o_final, o_empty;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr int kSmemBytes =
+    kQBytes + (kKStages + kVStages) * kKvBytes + static_cast<int>(sizeof(Ctrl)) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+// One work tile as every role sees it.
+struct Tile {
+  int b, g, tok0, ntok, q_row0, L, nq;
+  int kt0, N;          // 64-key tiles kt0 .. kt0 + N - 1
+};
+
+// The keys the tile's rows can see are [lo, hi): hi = min(L, p(last row) + 1) under the
+// causal mask (L otherwise) and lo = max(0, p(first row) - window_left) with a window, where
+// p(token i) = L - nq + i.  They are walked in 64-key tiles.
+__device__ __forceinline__ Tile make_tile(const AttnLaunch& a, const TileRec& r) {
+  Tile t;
+  t.b = r.b;
+  t.g = r.g;
+  t.tok0 = r.tok0;
+  t.ntok = r.ntok;
+  t.q_row0 = r.q_row0;
+  t.L = __ldg(a.seq_lens + r.b);
+  t.nq = a.qo_indptr ? __ldg(a.qo_indptr + r.b + 1) - __ldg(a.qo_indptr + r.b) : a.q_len;
+  const long long p0 = static_cast<long long>(t.L) - t.nq + r.tok0;
+  const long long p1 = p0 + r.ntok - 1;
+  const long long hi = a.causal ? min(static_cast<long long>(t.L), p1 + 1)
+                                : static_cast<long long>(t.L);
+  const long long lo = (a.causal && a.window_left >= 0) ? max(0LL, p0 - a.window_left) : 0LL;
+  if (r.ntok <= 0 || r.kv_end <= r.kv_begin || hi <= lo) {
+    t.kt0 = 0;
+    t.N = 0;
+  } else {
+    t.kt0 = static_cast<int>(lo / kKeys);
+    t.N = static_cast<int>((hi + kKeys - 1) / kKeys) - t.kt0;
+  }
+  return t;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+               const __grid_constant__ CUtensorMap vmap, AttnLaunch a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* q_s = smem_align<1024>(smem_raw);
+  uint8_t* k_s = q_s + kQBytes;
+  uint8_t* v_s = k_s + kKStages * kKvBytes;
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(v_s + kVStages * kKvBytes);
+
+  const int n_live = a.n_tiles ? *a.n_tiles : a.capacity;
+  if (static_cast<int>(blockIdx.x) >= n_live) return;
+  const int G = a.G;
+  const int TM = kRows / G;                              // tokens per work tile
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl->q_full, 1);
+    mbar_init(&ctl->q_empty, 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&ctl->k_full[s], 1);
+      mbar_init(&ctl->k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&ctl->v_full[s], 1);
+      mbar_init(&ctl->v_empty[s], 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&ctl->s_full[w], 1);
+      mbar_init(&ctl->p_full[w], kRows);
+    }
+    mbar_init(&ctl->pv_done, 1);
+    mbar_init(&ctl->o_final, 1);
+    mbar_init(&ctl->o_empty, kRows);
+    // a launch that an earlier CTA already broke does nothing
+    ctl->abort_flag = launch_aborted(a.status) ? 1 : 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&ctl->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  volatile int* abort_flag = &ctl->abort_flag;
+
+  if (*abort_flag) {
+    // nothing to do; fall through to the teardown
+  } else if (warp == kProdK || warp == kProdV) {
+    // =============================== producers =========================================
+    // warp 4 copies Q (lane 0) and K, warp 6 copies V; lane p copies page piece p of a tile
+    // (R keys of one page, one TMA box per 64-column chunk)
+    const bool is_k = warp == kProdK;
+    if (lane == 0) {
+      if (is_k) {
+        tma_prefetch_desc(&qmap);
+        tma_prefetch_desc(&kmap);
+      } else {
+        tma_prefetch_desc(&vmap);
+      }
+    }
+    const int ps = a.page_size;
+    const int R = page_piece_rows(ps, kKeys);
+    const int pieces = kKeys / R;
+    const int stages = is_k ? kKStages : kVStages;
+    uint8_t* ring = is_k ? k_s : v_s;
+    uint64_t* full = is_k ? ctl->k_full : ctl->v_full;
+    uint64_t* empty = is_k ? ctl->k_empty : ctl->v_empty;
+    const CUtensorMap* map = is_k ? &kmap : &vmap;
+    const int head_off = is_k ? a.k_head_off : a.v_head_off;
+    int kv_it = 0, qcount = 0, issued = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
+      const Tile t = make_tile(a, a.tiles[idx]);
+      if (t.N == 0) continue;
+      const int* pt = a.pt_indptr ? a.pt + __ldg(a.pt_indptr + t.b)
+                                  : a.pt + static_cast<long long>(t.b) * a.pt_stride;
+      auto key_of = [&](int n) {                 // first key of this lane's piece, or -1
+        const int key = (t.kt0 + n) * kKeys + lane * R;
+        return (lane < pieces && key < t.L) ? key : -1;
+      };
+      int key = key_of(0);
+      int page = key >= 0 ? __ldg(pt + key / ps) : 0;
+      if (is_k) {
+        if (qcount > 0 &&
+            !mbar_wait_warp<true>(&ctl->q_empty, (qcount - 1) & 1, a.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          // box: 64 columns x G heads x TM tokens; rows past the tensor read as zero
+          mbar_arrive_expect_tx(&ctl->q_full, static_cast<uint32_t>(kChunks * 128 * G * TM));
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_3d(q_s + c * kQChunk, &qmap, &ctl->q_full, c * 64, t.g * G, t.q_row0);
+        }
+        ++qcount;
+      }
+      for (int n = 0; n < t.N; ++n) {
+        const int it = kv_it + n, slot = it % stages;
+        if (it >= stages &&
+            !mbar_wait_warp<true>(&empty[slot], ((it / stages) - 1) & 1, a.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        bool live = key >= 0;
+        if (live && (page < 0 || page >= a.num_pages)) {
+          report_error(a.status, kErrMetadata);
+          live = false;
+        }
+        const uint32_t nlive = __popc(__ballot_sync(0xffffffffu, live));
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], nlive * R * 128u * kChunks);
+        __syncwarp();
+        if (live) {
+          uint8_t* dst = ring + slot * kKvBytes + static_cast<uint32_t>(lane * R) * 128u;
+          const int row = page * a.page_rows + t.g * ps + key % ps + head_off;
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_2d(dst + c * kKvChunk, map, &full[slot], c * 64, row);
+        }
+        issued = it + 1;
+        if (n + 1 < t.N) {                       // the next tile's page ids
+          key = key_of(n + 1);
+          page = key >= 0 ? __ldg(pt + key / ps) : 0;
+        }
+      }
+      kv_it += t.N;
+    }
+    if (!ok && lane == 0) {                      // let copies in flight land before exiting
+      for (int it = issued > stages ? issued - stages : 0; it < issued; ++it)
+        drain_wait(&full[it % stages], (it / stages) & 1);
+      if (is_k && qcount > 0) drain_wait(&ctl->q_full, (qcount - 1) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    // =============================== MMA issuer ========================================
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16(kRows, kKeys, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(kRows, kD, false, true);
+      // Descriptors of the first k-step; later steps add the byte offset / 16 to the start
+      // address field, which never carries out of it inside shared memory.
+      const uint64_t q_desc0 = sdesc_sw128(smem_u32(q_s), 16, 1024);
+      const uint64_t k_desc0 = sdesc_sw128(smem_u32(k_s), 16, 1024);
+      const uint64_t v_desc0 = sdesc_sw128(smem_u32(v_s), kKvChunk, 1024);
+      auto issue_qk = [&](int it) {              // S_(it%2) = Q K(it)^T, 16 k-steps of 16
+        const uint64_t kd = k_desc0 + static_cast<uint64_t>(((it % kKStages) * kKvBytes) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < kD / 16; ++ks) {
+          const uint32_t qoff = ((ks >> 2) * kQChunk + (ks & 3) * 32) >> 4;
+          const uint32_t koff = ((ks >> 2) * kKvChunk + (ks & 3) * 32) >> 4;
+          mma_ss(tmem + kTmemS + (it & 1) * kKeys, q_desc0 + qoff, kd + koff, idesc_qk, ks > 0);
+        }
+        mma_commit(&ctl->s_full[it & 1]);
+      };
+      auto issue_pv = [&](int it, bool acc) {    // O += P(it) V(it), 4 k-steps of 16 keys
+        const uint64_t vd = v_desc0 + static_cast<uint64_t>(((it % kVStages) * kKvBytes) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < kKeys / 16; ++ks)
+          mma_ts(tmem + kTmemO, tmem + kTmemS + (it & 1) * kKeys + ks * 8,
+                 vd + ((ks * 16 * 128) >> 4), idesc_pv, acc || ks > 0);
+      };
+      auto wait = [&](uint64_t* bar, int parity) {
+        return mbar_wait<true>(bar, parity, a.status, abort_flag);
+      };
+      int kv_it = 0, qcount = 0, ep = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
+        const Tile t = make_tile(a, a.tiles[idx]);
+        const int N = t.N;
+        if (N == 0) continue;
+        const int it0 = kv_it;
+        if (!wait(&ctl->q_full, qcount & 1)) {
+          ok = false;
+          break;
+        }
+        ++qcount;
+        for (int n = 0; ok && n < 2 && n < N; ++n) {   // the first two score tiles
+          const int it = it0 + n;
+          if (!wait(&ctl->k_full[it % kKStages], (it / kKStages) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_qk(it);
+          mma_commit(&ctl->k_empty[it % kKStages]);
+          if (n == N - 1) mma_commit(&ctl->q_empty);
+        }
+        for (int n = 0; ok && n < N; ++n) {
+          const int it = it0 + n, vs = it % kVStages;
+          // O is free once the previous work tile's epilogue has read it
+          if (!wait(&ctl->v_full[vs], (it / kVStages) & 1) ||
+              !wait(&ctl->p_full[it & 1], (it >> 1) & 1) ||
+              (n == 0 && ep > 0 && !wait(&ctl->o_empty, (ep - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(it, n > 0);
+          mma_commit(&ctl->pv_done);
+          mma_commit(&ctl->v_empty[vs]);
+          if (n == N - 1) mma_commit(&ctl->o_final);
+          if (n + 2 < N) {                       // QK(it + 2) into the buffer P(it) came from
+            const int it2 = it + 2;
+            if (!wait(&ctl->k_full[it2 % kKStages], (it2 / kKStages) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_qk(it2);
+            mma_commit(&ctl->k_empty[it2 % kKStages]);
+            if (n + 2 == N - 1) mma_commit(&ctl->q_empty);
+          }
+        }
+        kv_it += N;
+        ++ep;
+      }
+    }
+  } else if (warp < 4) {
+    // =============================== softmax (one row per thread) =======================
+    const int m = threadIdx.x;                           // row of the work tile
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t o_col = tmem + lane_base + kTmemO;
+    const float sl2 = a.scale_log2;
+    const bool causal = a.causal != 0;
+    const int wl = a.window_left;
+    int kv_it = 0, ep = 0;
+    bool ok = true;
+    for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
+      const Tile t = make_tile(a, a.tiles[idx]);
+      const int tok = m / G;                             // token inside the work tile
+      const bool row_valid = m < G * TM && tok < t.ntok;
+      const int pos = t.L - t.nq + t.tok0 + tok;        // query position
+      // keys [klo, khi) of this row
+      const int khi = causal ? min(t.L, pos + 1) : t.L;
+      const int klo = (causal && wl >= 0) ? max(0, pos - wl) : 0;
+      const int kspan = max(khi - klo, 0);
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int n = 0; n < t.N; ++n) {
+        const int it = kv_it + n;
+        if (!mbar_wait_warp<true>(&ctl->s_full[it & 1], (it >> 1) & 1, a.status, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t s_col = tmem + lane_base + kTmemS + (it & 1) * kKeys;
+        uint32_t r[kKeys];
+        tmem_ld32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_ld_wait();
+        const int key0 = (t.kt0 + n) * kKeys;
+        if (key0 < klo || key0 + kKeys > khi) {
+          // one unsigned range test and a select per column (the limits differ per row)
+          const int lo_c = klo - key0;
+#pragma unroll
+          for (int c = 0; c < kKeys; ++c) {
+            const bool out = static_cast<unsigned>(c - lo_c) >= static_cast<unsigned>(kspan);
+            r[c] = out ? 0xff800000u : r[c];
+          }
+        }
+        // row maximum: 8 independent chains of 3-input max, then a short tree
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kKeys; c += 2)
+          mx[(c >> 1) & 7] = max3f(mx[(c >> 1) & 7], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+        // scores are scaled by sl2 > 0 after the maximum, which commutes with it
+        const float mt = fmaxf(max3f(mx[0], mx[1], mx[2]),
+                               max3f(mx[3], mx[4], fmaxf(mx[5], fmaxf(mx[6], mx[7])))) * sl2;
+        // ---- online softmax with a lazily moved maximum ----------------------------------
+        float alpha = 1.f;
+        if (mt > m_run + kRescaleThreshold || (m_run == -INFINITY && mt > -INFINITY)) {
+          alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - mt);
+          m_run = mt;
+        }
+        const float nmu = m_run == -INFINITY ? 0.f : -m_run;
+        // ---- P = exp2(s * sl2 - mu) and the row sum; bf16 pairs packed in place into r[j] ---
+        float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < kKeys / 2; ++j) {
+          float x0, x1;
+          ffma2_bcast(x0, x1, __uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]), sl2, nmu);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          if (j & 1) fadd2(sb0, sb1, p0, p1);
+          else fadd2(sa0, sa1, p0, p1);
+          r[j] = pack_bf16(p0, p1);
+        }
+        tmem_st32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        l_run = l_run * alpha + ((sa0 + sa1) + (sb0 + sb1));
+        if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O holds PV of the previous KV tile, which may still run: wait for it, then scale
+          if (!mbar_wait_warp<true>(&ctl->pv_done, (it - 1) & 1, a.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int q = 0; q < kD / 32; ++q) {
+            uint32_t ov[32];
+            tmem_ld32(o_col + q * 32, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(o_col + q * 32, ov);
+          }
+        }
+        tmem_st_wait();
+        if (key0 + kKeys > t.L) {
+          // Rows of keys past the length hold stale or non-finite data (tail slots of the
+          // last page, or nothing copied); P is 0 there, so make V exactly 0 as well.
+          const int vs = it % kVStages;
+          if (!mbar_wait_warp<true>(&ctl->v_full[vs], (it / kVStages) & 1, a.status,
+                                    abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (m < kKeys && key0 + m >= t.L) {
+            uint8_t* vt = v_s + vs * kKvBytes + m * 128;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(vt + c * kKvChunk + i * 16) = z;
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        mbar_arrive(&ctl->p_full[it & 1]);
+      }
+      if (!ok) break;
+      // ---- epilogue --------------------------------------------------------------------
+      bool have_o = false;
+      if (t.N > 0) {
+        have_o = mbar_wait_warp<true>(&ctl->o_final, ep & 1, a.status, abort_flag);
+        ++ep;
+        if (!have_o) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      const long long orow = static_cast<long long>(t.q_row0 + tok) * a.Hq + t.g * G + (m % G);
+      const float inv = l_run > 0.f ? a.out_scale / l_run : 0.f;
+#pragma unroll 1
+      for (int q = 0; q < kD / 32; ++q) {
+        uint32_t ov[32];
+        if (have_o) {
+          tmem_ld32(o_col + q * 32, ov);
+          tmem_ld_wait();
+          if (q == kD / 32 - 1) {                // O fully read: the next work tile may write
+            tc_fence_before();
+            mbar_arrive(&ctl->o_empty);
+          }
+        }
+        if (row_valid && a.out_dtype == kOutF32) {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * kD + q * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = have_o ? make_float4(__uint_as_float(ov[4 * i]) * inv,
+                                          __uint_as_float(ov[4 * i + 1]) * inv,
+                                          __uint_as_float(ov[4 * i + 2]) * inv,
+                                          __uint_as_float(ov[4 * i + 3]) * inv)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else if (row_valid) {
+          uint32_t pkd[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pkd[i] = have_o ? pack_out2(__uint_as_float(ov[2 * i]) * inv,
+                                        __uint_as_float(ov[2 * i + 1]) * inv, a.out_dtype)
+                            : 0u;
+          uint4* dst =
+              reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * kD + q * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+        }
+      }
+      if (row_valid && a.lse)
+        a.lse[orow] = l_run > 0.f ? (m_run + fast_log2(l_run)) * kLn2 : -INFINITY;
+      kv_it += t.N;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+int g_num_sms = 0;
+
+}  // namespace
+
+// Prefill tiles of D = 256 (one 128-row sub-tile each; the planner's tile_tokens is 128 / G).
+int launch_attn256(const AttnLaunch& a, cudaStream_t st) {
+  if (a.D != kD || a.G < 1 || a.G > kRows) return -2;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(attn256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess)
+      return -1;
+    attr_set = true;
+  }
+  if (g_num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return -1;
+  }
+  if (a.capacity <= 0) return 0;
+  const int grid = a.capacity < g_num_sms ? a.capacity : g_num_sms;
+  attn256_kernel<<<grid, kThreads, kSmemBytes, st>>>(a.qmap, a.kmap, a.vmap, a);
+  count_launches(1);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace pa

@@ -158,6 +158,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 
 // Warp-uniform variant for code that follows with warp-collective (.sync.aligned)
 // instructions: the warp proceeds only if every lane's wait succeeded.
+// After an abort: wait (bounded, without reporting) for a copy still in flight into shared
+// memory, so that the CTA does not exit while a TMA engine writes its shared memory.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_test(bar, parity) && clock64() - t0 < kWaitCycles) {
+  }
+}
+
 template <bool kInlineLoop = false>
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status,
                                                volatile int* abort) {

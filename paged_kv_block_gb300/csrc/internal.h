@@ -151,6 +151,8 @@ struct AttnLaunch {
   float scale_log2, out_scale;
 };
 int launch_attn(const AttnLaunch& a, cudaStream_t st);
+// Dense prefill tiles of head dimension 256 (one 128-row sub-tile per planner tile).
+int launch_attn256(const AttnLaunch& a, cudaStream_t st);
 
 // ---- tensor maps (api.cu) -----------------------------------------------------------------
 bool encode_rows_map(CUtensorMap* map, const void* base, long long rows, int D, int box_rows);

@@ -114,14 +114,6 @@ __device__ __forceinline__ float ord2f(int i) { return __int_as_float(i >= 0 ? i
 __device__ __forceinline__ int unit_k(int n) { return n == 0 ? 0 : 2 * n - 1; }
 __device__ __forceinline__ int unit_v(int n, int N) { return n == N - 1 ? 2 * N - 1 : 2 * n + 2; }
 
-// Wait for copies still in flight before the CTA exits after an abort (bounded; ignores the
-// abort flag, which is already set).
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (!mbar_test(bar, parity) && clock64() - t0 < kWaitCycles) {
-  }
-}
-
 // Row r of V of tile n (unit u of the pair sequence) is zeroed once its copy has landed: P is
 // 0 there, but 0 x (inf or NaN) would not be.
 __device__ __noinline__ bool zero_dead_v_row(QsaCtrl* ctl, uint8_t* ring, int u, int r,

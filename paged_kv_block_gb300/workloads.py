@@ -448,6 +448,15 @@ def prefill_b16(seed=1003, window_left=-1):
                                 mask_type="causal", window_left=window_left)
 
 
+def prefill_b16_d256(seed=1003, window_left=-1):
+    """prefill_b16 (the same query lengths, prefixes and heads) with head dimension 256."""
+    rng = np.random.default_rng(seed)
+    q_lens = rng.integers(128, 2048, size=16, endpoint=True)
+    prefix = rng.integers(0, 2048, size=16, endpoint=True)
+    return make_prefill_problem(seed, q_lens, prefix, Hq=32, Hkv=8, D=256, page_size=32,
+                                mask_type="causal", window_left=window_left)
+
+
 def long_bsr(seed=1004, S=65536, Hq=64, Hkv=8):
     """Long-context block-sparse prefill: B=1, Sq=Skv=S, page 64, q block 128, kv block 64,
     sink + 16 recent + 48 random earlier blocks per row, causal, 1% invalid tokens."""
