@@ -438,40 +438,11 @@ __device__ __forceinline__ void fadd2(float& a0, float& a1, float b0, float b1) 
       : "f"(b0), "f"(b1));
 }
 
-// (2^x0, 2^x1) through one packed half-precision MUFU op: the arguments are rounded to fp16
-// (11 significant bits), the results come back as fp32.  -inf gives 0; results below the
-// fp16 range flush to 0.
-__device__ __forceinline__ void exp2_pair_f16(float x0, float x1, float& p0, float& p1) {
-  asm("{\n\t.reg .b32 h, e;\n\t.reg .b16 e0, e1;\n\t"
-      "cvt.rn.f16x2.f32 h, %3, %2;\n\t"
-      "ex2.approx.f16x2 e, h;\n\t"
-      "mov.b32 {e0, e1}, e;\n\t"
-      "cvt.f32.f16 %0, e0;\n\tcvt.f32.f16 %1, e1;\n\t}"
-      : "=f"(p0), "=f"(p1)
-      : "f"(x0), "f"(x1));
-}
-
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// 2^x on the FMA pipe.  Range reduction by rounding to nearest (x = j + f, f in [-0.5, 0.5],
-// using the 1.5 * 2^23 addition trick), 2^f by a cubic whose coefficients were fitted here to
-// minimise the maximum relative error on [-0.5, 0.5] (iteratively reweighted least squares;
-// max relative error 7.5e-5 in fp32), and 2^j added into the exponent field.  Arguments
-// below -125 (including -inf) give exactly 0.
-__device__ __forceinline__ float poly_exp2(float x) {
-  const float xc = fmaxf(x, -125.f);
-  const float t = xc + 12582912.f;
-  const float j = t - 12582912.f;
-  const float f = xc - j;
-  float p = fmaf(fmaf(fmaf(0.0551715009f, f, 0.2426109612f), f, 0.6932609677f), f,
-                 0.9999280572f);
-  p = __int_as_float(__float_as_int(p) + ((__float_as_int(t) - 0x4B400000) << 23));
-  return x < -125.f ? 0.f : p;
-}
-
 __device__ __forceinline__ float fast_log2(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
