@@ -12,6 +12,7 @@ Sources (FlashInfer API pages):
   [PRE]  flashinfer.attention.prims_ts.batch_prefill_with_paged_kv_cache
   [QSA]  flashinfer.qsa.qsa_forward
   [DEC]  flashinfer.attention.prims_ts.prims_ts_batch_decode_with_kv_cache
+  [SAGE] flashinfer.cute_dsl.sparse.bsa_attn_sm120.bsa_attn_sm120_blk64_sage_fwd
 
 Readings where the pages are silent (each also listed in the design notes):
   * query position: query i of a request with len_q queries and len_kv keys sits at
@@ -419,6 +420,67 @@ def qsa_indexed_forward(q, k, v, sel_indices, lo, hi, block_first, block_last, s
             out[t, g * G:(g + 1) * G] = o[0]
             lse[g * G:(g + 1) * G, t] = s[0]
     return out, lse
+
+
+# ----------------------------------------------------------------------------------------
+# [SAGE] prequantized block-sparse attention
+# ----------------------------------------------------------------------------------------
+
+def fp8_e4m3_to_f64(codes):
+    """Decode FP8 E4M3 bytes (the e4m3fn format: 1 sign, 4 exponent bits with bias 7, 3
+    mantissa bits, no infinities, S.1111.111 = NaN) to float64 (torch's conversion)."""
+    t = codes if isinstance(codes, torch.Tensor) else torch.from_numpy(np.asarray(codes))
+    return t.contiguous().view(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def sage_block_sparse_attention(q_int8, k_int8, v_fp8, q_scale, k_scale, v_scale,
+                                q2k_block_index, block_sparse_num, block_sizes=None,
+                                q2k_block_nums=None, softmax_scale=None):
+    """[SAGE] forward on the dequantized values (signature, parameters and notes).
+
+    q = q_int8 * q_scale[b, h, i // 32] (four scales per 128 queries), k = k_int8 *
+    k_scale[b, h, j // 64] (one per 64-key block), v[j, d] = e4m3(v_fp8[b, h, d, j]) *
+    v_scale[b, h, d].  Query block r = i // 64 selects the first n_r entries of
+    q2k_block_index[b, h, r] (n_r = q2k_block_nums[b, h, r], else block_sparse_num); key j of
+    selected block c is visible iff j < Sk and j - 64 c < block_sizes[c] (block_sizes given as
+    [NB], [B, NB] or [B, H, NB]; all 64 when omitted).  No causal mask (non-causal forward).
+    O = softmax(softmax_scale * q k^T) v over the visible keys; a row with none gives exactly
+    0.  Returns O [B, H, Sq, 128] in float64."""
+    qi = f64(q_int8)
+    ki = f64(k_int8)
+    vf = fp8_e4m3_to_f64(v_fp8)
+    B, H, Sq, D = qi.shape
+    Sk = ki.shape[2]
+    qs, ks, vs = f64(q_scale), f64(k_scale), f64(v_scale)
+    idx = i64(q2k_block_index)
+    NB = -(-Sk // 64)
+    scale = (1.0 / math.sqrt(D)) if softmax_scale is None else float(softmax_scale)
+    if block_sizes is None:
+        bs = np.full((B, H, NB), 64, dtype=np.int64)
+    else:
+        bsz = i64(block_sizes)
+        bs = np.broadcast_to(bsz.reshape((1,) * (3 - bsz.ndim) + bsz.shape), (B, H, bsz.shape[-1]))
+    nums = i64(q2k_block_nums) if q2k_block_nums is not None else None
+    out = np.zeros((B, H, Sq, D))
+    for b in range(B):
+        for h in range(H):
+            q = qi[b, h] * qs[b, h][np.arange(Sq) // 32][:, None]
+            k = ki[b, h] * ks[b, h][np.arange(Sk) // 64][:, None]
+            v = vf[b, h, :, :Sk].T * vs[b, h][None, :]
+            for r in range(-(-Sq // 64)):
+                rows = np.arange(r * 64, min(Sq, r * 64 + 64))
+                n = int(nums[b, h, r]) if nums is not None else int(block_sparse_num)
+                keys = []
+                for c in idx[b, h, r, :n]:
+                    c = int(c)
+                    if 0 <= c < NB:
+                        keys.extend(j for j in range(64 * c, min(Sk, 64 * c + 64))
+                                    if j - 64 * c < bs[b, h, c])
+                keys = np.array(sorted(keys), dtype=np.int64)
+                vis = np.ones((rows.size, keys.size), bool)
+                o, _ = masked_softmax_attention(q[rows][:, None, :], k[keys], v[keys], vis, scale)
+                out[b, h, rows] = o[:, 0]
+    return out
 
 
 # ----------------------------------------------------------------------------------------

@@ -410,6 +410,67 @@ def make_qsa_indexed_problem(seed, seq_lens, Hq, Hkv, D, *, block_size=4, n_near
 
 
 # ----------------------------------------------------------------------------------------
+# Prequantized block-sparse attention (int8 Q/K, FP8 E4M3 V)
+# ----------------------------------------------------------------------------------------
+
+def make_sage_problem(seed, B, H, Sq, Sk, *, capacity=8, uniform=None, sizes="none",
+                      empty_rows=0.0, D=128):
+    """Q, K, V drawn N(0, 1) and quantized as a Sage quantizer would: Q to int8 with one scale
+    per 32 queries, K to int8 with one scale per 64-key block (scale = max |x| / 127, round to
+    nearest), V to FP8 E4M3 with one scale per channel (max |v| / 448), stored HDS
+    [B, H, D, ceil(Sk / 64) * 64] (the padding columns are 0).  Query block r of (b, h) selects
+    distinct uniform KV blocks: `uniform` of them each (block_sparse_num) or a per-row count
+    uniform in [0, capacity] (q2k_block_nums; a fraction empty_rows of rows select none).
+    sizes: "none" (block_sizes omitted), "nb" [NB], "bnb" [B, NB] or "bhnb" [B, H, NB] with
+    uniform valid-token counts in [1, 64] (the last block never above Sk - 64 (NB - 1))."""
+    gen = _gen(seed)
+    rng = np.random.default_rng(seed)
+    QB, NB = -(-Sq // 64), -(-Sk // 64)
+    q = torch.randn((B, H, Sq, D), generator=gen, dtype=torch.float32)
+    k = torch.randn((B, H, Sk, D), generator=gen, dtype=torch.float32)
+    v = torch.randn((B, H, Sk, D), generator=gen, dtype=torch.float32)
+    QG = -(-Sq // 128) * 4
+    qp = torch.zeros((B, H, QG * 32, D))
+    qp[:, :, :Sq] = q
+    q_scale = (qp.abs().reshape(B, H, QG, 32 * D).amax(-1) / 127.0).clamp_min(1e-8)
+    q_int8 = torch.round(qp / q_scale.repeat_interleave(32, dim=2)[..., None])[:, :, :Sq]
+    kp = torch.zeros((B, H, NB * 64, D))
+    kp[:, :, :Sk] = k
+    k_scale = (kp.abs().reshape(B, H, NB, 64 * D).amax(-1) / 127.0).clamp_min(1e-8)
+    k_int8 = torch.round(kp / k_scale.repeat_interleave(64, dim=2)[..., None])[:, :, :Sk]
+    v_scale = (v.abs().amax(2) / 448.0).clamp_min(1e-8)                      # [B, H, D]
+    vq = (v / v_scale[:, :, None, :]).to(torch.float8_e4m3fn)               # [B, H, Sk, D]
+    v_hds = torch.zeros((B, H, D, NB * 64), dtype=torch.uint8)
+    v_hds[:, :, :, :Sk] = vq.view(torch.uint8).transpose(2, 3)
+    cap = capacity if uniform is None else max(capacity, uniform)
+    idx = np.zeros((B, H, QB, cap), dtype=np.int32)
+    nums = np.zeros((B, H, QB), dtype=np.int32)
+    for b in range(B):
+        for h in range(H):
+            for r in range(QB):
+                n = uniform if uniform is not None else int(rng.integers(0, min(capacity, NB) + 1))
+                if uniform is None and rng.random() < empty_rows:
+                    n = 0
+                n = min(n, NB)
+                idx[b, h, r, :n] = rng.choice(NB, size=n, replace=False)
+                idx[b, h, r, n:] = rng.integers(0, NB, size=cap - n)   # unused entries
+                nums[b, h, r] = n
+    last = Sk - 64 * (NB - 1)
+    block_sizes = None
+    if sizes != "none":
+        shape = {"nb": (NB,), "bnb": (B, NB), "bhnb": (B, H, NB)}[sizes]
+        bsz = rng.integers(1, 65, size=shape).astype(np.int32)
+        bsz[..., NB - 1] = np.minimum(bsz[..., NB - 1], last)
+        block_sizes = torch.from_numpy(bsz)
+    return dict(form="sage", q_int8=q_int8.to(torch.int8), k_int8=k_int8.to(torch.int8),
+                v_fp8=v_hds, q_scale=q_scale.float(), k_scale=k_scale.float(),
+                v_scale=v_scale.float(), q2k_block_index=torch.from_numpy(idx),
+                block_sparse_num=int(uniform) if uniform is not None else 0,
+                q2k_block_nums=None if uniform is not None else torch.from_numpy(nums),
+                block_sizes=block_sizes, softmax_scale=1.0 / math.sqrt(D), Sq=Sq, Sk=Sk)
+
+
+# ----------------------------------------------------------------------------------------
 # The named workloads
 # ----------------------------------------------------------------------------------------
 

@@ -230,3 +230,57 @@ def qsa_indexed_bruteforce(prob):
             o, s = _softmax_row(_vec(q[t, h].float()), keys, vals, prob["scale"])
             O[t, h], LSE[h, t] = o, s
     return O, LSE
+
+
+def e4m3_value(code):
+    """FP8 E4M3 (e4m3fn) from its bit fields: sign, 4-bit exponent with bias 7 (0 =
+    subnormal), 3-bit mantissa; S.1111.111 is NaN and there is no infinity."""
+    code = int(code) & 0xFF
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 0x7
+    if e == 0xF and m == 0x7:
+        return math.nan
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def sage_bruteforce(prob):
+    """Dequantized block-sparse attention by plain loops (bit-level FP8 decoding)."""
+    qi, ki, vh = prob["q_int8"], prob["k_int8"], prob["v_fp8"]
+    B, H, Sq, D = qi.shape
+    Sk = ki.shape[2]
+    NB = -(-Sk // 64)
+    bs = prob["block_sizes"]
+
+    def bsize(b, h, c):
+        if bs is None:
+            return 64
+        if bs.dim() == 1:
+            return int(bs[c])
+        if bs.dim() == 2:
+            return int(bs[b, c])
+        return int(bs[b, h, c])
+
+    O = np.zeros((B, H, Sq, D))
+    for b in range(B):
+        for h in range(H):
+            for i in range(Sq):
+                r = i // 64
+                n = (int(prob["q2k_block_nums"][b, h, r]) if prob["q2k_block_nums"] is not None
+                     else int(prob["block_sparse_num"]))
+                listed = [int(c) for c in prob["q2k_block_index"][b, h, r, :n]]
+                qs = float(prob["q_scale"][b, h, i // 32])
+                q = [int(x) * qs for x in qi[b, h, i]]
+                keys, vals = [], []
+                for j in range(Sk):
+                    c = j // 64
+                    if c not in listed or j - 64 * c >= bsize(b, h, c):
+                        continue
+                    ks = float(prob["k_scale"][b, h, c])
+                    keys.append([int(x) * ks for x in ki[b, h, j]])
+                    vals.append([e4m3_value(vh[b, h, d, j]) * float(prob["v_scale"][b, h, d])
+                                 for d in range(D)])
+                o, _ = _softmax_row(q, keys, vals, prob["softmax_scale"])
+                O[b, h, i] = o
+    return O

@@ -155,6 +155,80 @@ def test_qsa_indexed_equals_bitmap_form():
     _close(s_i, s_b, 1e-13)
 
 
+def _run_sage(p, **kw):
+    return A.sage_block_sparse_attention(p["q_int8"], p["k_int8"], p["v_fp8"], p["q_scale"],
+                                         p["k_scale"], p["v_scale"], p["q2k_block_index"],
+                                         p["block_sparse_num"], p["block_sizes"],
+                                         p["q2k_block_nums"], p["softmax_scale"], **kw)
+
+
+def test_fp8_e4m3_decoding_follows_the_format():
+    codes = np.arange(256, dtype=np.uint8)
+    got = A.fp8_e4m3_to_f64(codes)
+    want = np.array([BF.e4m3_value(c) for c in codes])
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(B=1, H=2, Sq=70, Sk=150, capacity=2, sizes="bhnb", empty_rows=0.3),
+    dict(B=2, H=1, Sq=64, Sk=64, uniform=1, sizes="nb"),
+    dict(B=1, H=1, Sq=33, Sk=190, uniform=2, sizes="none"),
+])
+def test_sage_matches_bruteforce(kw):
+    p = W.make_sage_problem(45, D=8, **kw)
+    _close(_run_sage(p), BF.sage_bruteforce(p), 1e-12)
+
+
+def test_sage_with_unit_scales_equals_block_sparse_form():
+    """Unit scales make the dequantized values the integers and the FP8 values themselves:
+    the result is then the [BSA] forward (non-causal, 64-query and 64-key blocks, one KV head
+    per (b, h)) on those values."""
+    p = W.make_sage_problem(46, B=1, H=2, Sq=100, Sk=180, capacity=3, sizes="none", D=8)
+    p["q_scale"] = torch.ones_like(p["q_scale"])
+    p["k_scale"] = torch.ones_like(p["k_scale"])
+    p["v_scale"] = torch.ones_like(p["v_scale"])
+    o = _run_sage(p)
+    B, H, Sq, D = p["q_int8"].shape
+    Sk = p["k_int8"].shape[2]
+    NB = -(-Sk // 64)
+    vf = A.fp8_e4m3_to_f64(p["v_fp8"])[:, :, :, :Sk]
+    for h in range(H):
+        # one request of the [BSA] form: identity pages of 64 keys
+        kc = torch.zeros((NB, 1, 64, D), dtype=torch.float64)
+        vc = torch.zeros((NB, 1, 64, D), dtype=torch.float64)
+        kc.view(NB * 64, D)[:Sk] = p["k_int8"][0, h].double()
+        vc.view(NB * 64, D)[:Sk] = torch.from_numpy(vf[0, h].T.copy())
+        nums = p["q2k_block_nums"][0, h]
+        ptr = np.concatenate([[0], np.cumsum(nums.numpy())]).reshape(1, 1, -1)
+        ids = torch.cat([p["q2k_block_index"][0, h, r, :int(nums[r])] for r in range(nums.numel())])
+        ob, _ = A.block_sparse_attention(
+            p["q_int8"][0:1, h][:, :, None, :].double(), torch.tensor([0, NB]), torch.arange(NB),
+            torch.from_numpy(ptr), ids, 64, 64, torch.tensor([Sk]), k_cache=kc, v_cache=vc,
+            mask_type="dense", sm_scale=p["softmax_scale"])
+        _close(o[0, h], ob[0, :, 0], 1e-12)
+
+
+def test_sage_zero_query_gives_the_mean_of_visible_values():
+    """q = 0: O = the mean of the visible dequantized V rows, an integer count that pins the
+    block selection, the counts and the block sizes; a row selecting nothing is exactly 0."""
+    p = W.make_sage_problem(47, B=1, H=1, Sq=128, Sk=250, capacity=3, sizes="bhnb",
+                            empty_rows=0.3, D=8)
+    p["q_int8"] = torch.zeros_like(p["q_int8"])
+    o = _run_sage(p)
+    vf = A.fp8_e4m3_to_f64(p["v_fp8"])[0, 0] * p["v_scale"][0, 0].double().numpy()[:, None]
+    for r in range(2):
+        n = int(p["q2k_block_nums"][0, 0, r])
+        js = [j for c in p["q2k_block_index"][0, 0, r, :n].tolist()
+              for j in range(64 * c, min(250, 64 * c + int(p["block_sizes"][0, 0, c])))]
+        rows = o[0, 0, 64 * r:64 * r + 64]
+        if not js:
+            assert np.all(rows == 0.0)
+        else:
+            _close(rows, np.broadcast_to(vf[:, js].mean(axis=1), rows.shape), 1e-13)
+
+
 def test_prefill_matches_torch_sdpa():
     p = W.make_prefill_problem(11, q_lens=[7, 12], prefix_lens=[9, 3], Hq=6, Hkv=2, D=16,
                                page_size=8, mask_type="causal", window_left=5)
