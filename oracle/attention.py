@@ -459,7 +459,14 @@ def sage_block_sparse_attention(q_int8, k_int8, v_fp8, q_scale, k_scale, v_scale
         bs = np.full((B, H, NB), 64, dtype=np.int64)
     else:
         bsz = i64(block_sizes)
-        bs = np.broadcast_to(bsz.reshape((1,) * (3 - bsz.ndim) + bsz.shape), (B, H, bsz.shape[-1]))
+        # [NB] is shared by all (b, h); [B, NB] is per batch, shared by the heads
+        if bsz.ndim == 1:
+            full = bsz[None, None, :]
+        elif bsz.ndim == 2:
+            full = bsz[:, None, :]
+        else:
+            full = bsz
+        bs = np.broadcast_to(full, (B, H, bsz.shape[-1]))
     nums = i64(q2k_block_nums) if q2k_block_nums is not None else None
     out = np.zeros((B, H, Sq, D))
     for b in range(B):

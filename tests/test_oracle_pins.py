@@ -175,6 +175,8 @@ def test_fp8_e4m3_decoding_follows_the_format():
     dict(B=1, H=2, Sq=70, Sk=150, capacity=2, sizes="bhnb", empty_rows=0.3),
     dict(B=2, H=1, Sq=64, Sk=64, uniform=1, sizes="nb"),
     dict(B=1, H=1, Sq=33, Sk=190, uniform=2, sizes="none"),
+    dict(B=2, H=3, Sq=40, Sk=130, capacity=3, sizes="bnb"),     # [B, NB]: per batch
+    dict(B=2, H=2, Sq=20, Sk=130, capacity=3, sizes="bnb"),     # B = H must not mix them up
 ])
 def test_sage_matches_bruteforce(kw):
     p = W.make_sage_problem(45, D=8, **kw)
