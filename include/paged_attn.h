@@ -258,6 +258,49 @@ int paged_decode_run(const paged_decode_params* params, const void* query_dev,
                      const int32_t* qo_indptr_dev, void* out_dev, float* lse_dev,
                      void* workspace_dev, size_t workspace_bytes, void* stream);
 
+/* ---- [SAGE] prequantized block-sparse attention ---------------------------------------
+ * bsa_attn_sm120_blk64_sage_fwd computes block-sparse attention on dequantized inputs:
+ * q = q_int8 * q_scale[b, h, i / 32] (four scales per 128 queries, [SAGE] q_scale shape
+ * [B, H, ceil(Sq / 128) * 4]), k = k_int8 * k_scale[b, h, j / 64], v[j, d] = e4m3(v_fp8[b, h,
+ * d, j]) * v_scale[b, h, d]; query block r = i / 64 of (b, h) sees the keys of the first n
+ * entries of q2k_block_index[b, h, r] (n = q2k_block_nums[b, h, r], or block_sparse_num
+ * when the counts are NULL or uniform_block_count is set), a key j of block c only when
+ * j < Sk and j - 64 c < block_sizes[..c]; no causal mask; a query block selecting nothing
+ * gets exactly 0 ([SAGE] notes).  The library computes the integer scores exactly (bf16
+ * tensor-core MMAs on the int8 values) and applies the scales in fp32.  The
+ * contiguous_block_indices hint of the page changes nothing here and has no field. */
+typedef struct paged_sage_params {
+  int batch;                 /* B                                                        */
+  int num_heads;             /* H: the same heads for Q, K and V (MHA)                   */
+  int q_len, kv_len;         /* Sq, Sk                                                   */
+  int head_dim;              /* 128                                                      */
+  int capacity;              /* last dimension of q2k_block_index                        */
+  int block_sparse_num;      /* blocks per query block without per-row counts            */
+  int uniform_block_count;   /* 1: every query block uses block_sparse_num               */
+  int block_sizes_rank;      /* 0: no block_sizes (64 keys each); 1: [NB]; 2: [B, NB];
+                                3: [B, H, NB]; NB = ceil(Sk / 64)                        */
+  float softmax_scale;       /* > 0; <= 0 selects 1/sqrt(128)                              */
+} paged_sage_params;
+
+/* Workspace bytes of paged_sage_run (bf16 copies of Q, K and V, and the block-sparse plan);
+ * 0 on invalid params. */
+size_t paged_sage_workspace_size(const paged_sage_params* params);
+
+/* Run the prequantized form.  Device pointers: q_int8_dev [B, H, Sq, 128] int8 (16-byte
+ * aligned); k_int8_dev [B, H, Sk, 128] int8 (16-byte aligned); v_fp8_dev [B, H, 128, NB * 64]
+ * FP8 E4M3 bytes (4-byte aligned); q_scale_dev [B, H, ceil(Sq / 128) * 4], k_scale_dev
+ * [B, H, NB], v_scale_dev [B, H, 128] fp32, all positive; q2k_block_index_dev
+ * [B, H, ceil(Sq / 64), capacity] int32; q2k_block_nums_dev [B, H, ceil(Sq / 64)] int32 or
+ * NULL; block_sizes_dev of rank block_sizes_rank (NULL for rank 0); out_dev [B, H, Sq, 128]
+ * bf16.  Counts outside [0, capacity] and block ids outside [0, NB) break the contract: they
+ * are clamped or dropped and the metadata bit is set in the status word. */
+int paged_sage_run(const paged_sage_params* params, const int8_t* q_int8_dev,
+                   const int8_t* k_int8_dev, const uint8_t* v_fp8_dev, const float* q_scale_dev,
+                   const float* k_scale_dev, const float* v_scale_dev,
+                   const int32_t* q2k_block_index_dev, const int32_t* q2k_block_nums_dev,
+                   const int32_t* block_sizes_dev, void* out_dev, void* workspace_dev,
+                   size_t workspace_bytes, void* stream);
+
 /* Decode without a workspace argument.  The pages describe no counterpart of this entry
  * point; it exists for callers that cannot allocate device memory at call time (code inside
  * an allocator or out-of-memory handler, plugins whose host owns every device allocation,

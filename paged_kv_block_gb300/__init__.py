@@ -71,6 +71,13 @@ class DecodeParams(C.Structure):
                 ("total_q", C.c_int), ("out_dtype", C.c_int)]
 
 
+class SageParams(C.Structure):
+    _fields_ = [("batch", C.c_int), ("num_heads", C.c_int), ("q_len", C.c_int),
+                ("kv_len", C.c_int), ("head_dim", C.c_int), ("capacity", C.c_int),
+                ("block_sparse_num", C.c_int), ("uniform_block_count", C.c_int),
+                ("block_sizes_rank", C.c_int), ("softmax_scale", C.c_float)]
+
+
 class PlanLayout(C.Structure):
     _fields_ = [("status_offset", C.c_size_t), ("tiles_offset", C.c_size_t),
                 ("tiles_capacity", C.c_int64), ("count_offset", C.c_size_t),
@@ -104,6 +111,9 @@ _EXPORTS = {
     "paged_decode_plan_layout_of": (C.c_int, [C.POINTER(DecodeParams), C.POINTER(PlanLayout)]),
     "paged_decode_run_static": (C.c_int, [C.POINTER(DecodeParams)] + [C.c_void_p] * 10),
     "paged_attn_workspace_status": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(C.c_uint32)]),
+    "paged_sage_workspace_size": (C.c_size_t, [C.POINTER(SageParams)]),
+    "paged_sage_run": (C.c_int, [C.POINTER(SageParams)] + [C.c_void_p] * 11
+                       + [C.c_size_t, C.c_void_p]),
     "paged_attn_strerror": (C.c_char_p, [C.c_int]),
     "paged_attn_kernel_timer": (C.c_int, [C.c_int]),
     "paged_attn_kernel_timer_read": (C.c_int, [C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
@@ -530,3 +540,57 @@ def qsa_indexed_forward(q, k, v, sel_indices, lo, hi, block_first, block_last, s
     paged_attn_plan(params, meta, workspace, stream)
     paged_attn_run(params, meta, q, k, v, out, out_fp32, lse, workspace, stream)
     return out, out_fp32, lse
+
+
+def sage_params(q_int8, k_int8, q2k_block_index, block_sparse_num, *, block_sizes=None,
+                softmax_scale=None, uniform_block_count=False) -> SageParams:
+    B, H, Sq, D = q_int8.shape
+    Sk = k_int8.shape[2]
+    return SageParams(batch=B, num_heads=H, q_len=Sq, kv_len=Sk, head_dim=D,
+                      capacity=q2k_block_index.shape[-1], block_sparse_num=int(block_sparse_num),
+                      uniform_block_count=int(bool(uniform_block_count)),
+                      block_sizes_rank=0 if block_sizes is None else block_sizes.dim(),
+                      softmax_scale=float(softmax_scale or 0.0))
+
+
+def paged_sage_workspace_size(params: SageParams) -> int:
+    return int(lib().paged_sage_workspace_size(C.byref(params)))
+
+
+def paged_sage_run(params: SageParams, q_int8, k_int8, v_fp8, q_scale, k_scale, v_scale,
+                   q2k_block_index, q2k_block_nums, block_sizes, out, workspace,
+                   stream=None) -> None:
+    _check(lib().paged_sage_run(C.byref(params), _dev(q_int8, "q_int8"), _dev(k_int8, "k_int8"),
+                                _dev(v_fp8, "v_fp8"), _dev(q_scale, "q_scale"),
+                                _dev(k_scale, "k_scale"), _dev(v_scale, "v_scale"),
+                                _dev(q2k_block_index, "q2k_block_index"),
+                                _dev(q2k_block_nums, "q2k_block_nums"),
+                                _dev(block_sizes, "block_sizes"), _dev(out, "out"),
+                                _dev(workspace, "workspace"),
+                                workspace.numel() * workspace.element_size(), _stream(stream)),
+           "paged_sage_run")
+
+
+def bsa_sage_fwd(q_int8, k_int8, v_fp8, q_scale, k_scale, v_scale, q2k_block_index,
+                 block_sparse_num, block_sizes=None, q2k_block_nums=None, softmax_scale=None, *,
+                 out=None, uniform_block_count=False, contiguous_block_indices=False,
+                 workspace=None, stream=None):
+    """Prequantized block-sparse attention with the arguments of
+    bsa_attn_sm120_blk64_sage_fwd: int8 Q/K [B, H, S, 128], FP8 E4M3 V [B, H, 128,
+    ceil(Sk / 64) * 64] (uint8 or float8_e4m3fn storage), fp32 scales; returns out bf16
+    [B, H, Sq, 128].  contiguous_block_indices is a hint that changes nothing here."""
+    if softmax_scale is not None and not (softmax_scale > 0 and math.isfinite(softmax_scale)):
+        raise ValueError("softmax_scale must be positive and finite")
+    if contiguous_block_indices and not uniform_block_count:
+        raise ValueError("contiguous_block_indices requires uniform_block_count")
+    params = sage_params(q_int8, k_int8, q2k_block_index, block_sparse_num,
+                         block_sizes=block_sizes, softmax_scale=softmax_scale,
+                         uniform_block_count=uniform_block_count)
+    if out is None:
+        out = torch.empty(q_int8.shape, dtype=torch.bfloat16, device=q_int8.device)
+    if workspace is None:
+        workspace = _workspace(paged_sage_workspace_size(params), q_int8.device)
+    v = v_fp8.view(torch.uint8) if v_fp8.dtype != torch.uint8 else v_fp8
+    paged_sage_run(params, q_int8, k_int8, v, q_scale, k_scale, v_scale, q2k_block_index,
+                   q2k_block_nums, block_sizes, out, workspace, stream)
+    return out

@@ -268,6 +268,77 @@ DecodeLayout decode_layout(const paged_decode_params* p) {
   return s;
 }
 
+// ---- prequantized block-sparse layout ------------------------------------------------------
+struct SageLayout {
+  paged_attn_params bsr;       // the block-sparse form the inputs are turned into
+  SparseLayout s;              // its plan, at offset 0 (so the status word is the usual one)
+  size_t q_bf16, k_bf16, v_bf16, counts, block_indptr, block_indices, kv_indptr, kv_indices,
+      seq_lens, valid_bits, total;
+  int NB, QB, QG, BH;
+};
+
+bool sage_params_ok(const paged_sage_params* p) {
+  if (!p) return false;
+  if (p->batch < 0 || p->num_heads <= 0 || p->q_len < 0 || p->kv_len < 0) return false;
+  if (p->head_dim != 128 || p->capacity < 0) return false;
+  if (p->block_sparse_num < 0 || p->block_sparse_num > p->capacity) return false;
+  if (p->block_sizes_rank < 0 || p->block_sizes_rank > 3) return false;
+  const long long BH = static_cast<long long>(p->batch) * p->num_heads;
+  if (BH > 65535) return false;
+  const long long NB = (p->kv_len + 63) / 64;
+  if (BH * NB * 64 * 128 >= (1LL << 31) || BH * p->q_len >= (1LL << 31)) return false;
+  return true;
+}
+
+SageLayout sage_layout(const paged_sage_params* p) {
+  SageLayout g{};
+  g.BH = p->batch * p->num_heads;
+  g.NB = (p->kv_len + 63) / 64;
+  g.QB = (p->q_len + 63) / 64;
+  g.QG = (p->q_len + 127) / 128 * 4;
+  paged_attn_params& b = g.bsr;
+  b.form = PAGED_ATTN_FORM_BSR;
+  b.batch = g.BH;
+  b.q_len = p->q_len;
+  b.num_qo_heads = 1;
+  b.num_kv_heads = 1;
+  b.head_dim = 128;
+  b.page_size = 64;
+  b.num_pages = g.BH * g.NB > 0 ? g.BH * g.NB : 1;
+  b.combined_cache = 0;
+  b.q_block_size = 64;
+  b.kv_block_size = 64;
+  b.max_seq_len_kv = g.NB * 64;
+  b.mask_type = PAGED_ATTN_MASK_DENSE;
+  b.has_valid_bits = 1;
+  b.sm_scale = p->softmax_scale;
+  g.s = sparse_layout(&b);
+  Layout l;
+  l.off = g.s.total;
+  const size_t BH = static_cast<size_t>(g.BH), NB = static_cast<size_t>(g.NB);
+  const size_t QB = static_cast<size_t>(g.QB);
+  g.q_bf16 = l.take(BH * p->q_len * 128 * 2 + 16);
+  g.k_bf16 = l.take(BH * NB * 64 * 128 * 2 + 16);
+  g.v_bf16 = l.take(BH * NB * 64 * 128 * 2 + 16);
+  g.counts = l.take(sizeof(int) * (BH * QB + 1));
+  g.block_indptr = l.take(sizeof(int) * (BH * (QB + 1) + 1));
+  g.block_indices = l.take(sizeof(int) * (BH * QB * static_cast<size_t>(p->capacity) + 1));
+  g.kv_indptr = l.take(sizeof(int) * (BH + 1));
+  g.kv_indices = l.take(sizeof(int) * (BH * NB + 1));
+  g.seq_lens = l.take(sizeof(int) * (BH + 1));
+  g.valid_bits = l.take(sizeof(uint32_t) * (BH * 2 * NB + 1));
+  g.total = l.off;
+  return g;
+}
+
+// Scales of the prequantized form (see AttnLaunch).
+struct ScaleSet {
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
+  int q_group, q_stride, k_stride, v_stride;
+};
+
 template <class T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
@@ -426,6 +497,72 @@ int decode_run_tiled(const paged_decode_params* p, const DecodeLayout& s, const 
 
 }  // namespace
 
+// Block-sparse launch of a planned BSR form (the workspace holds the plan at `s`); `sc`
+// carries the scales of the prequantized form, nullptr otherwise.
+int bsr_launch(const paged_attn_params* p, const paged_attn_meta* m, const SparseLayout& s,
+               const void* q, const void* k, const void* v, void* out, float* lse, void* ws,
+               uint32_t* status, float scale, const ScaleSet* sc, cudaStream_t st) {
+  const int D = p->head_dim;
+  if (s.capacity == 0) return PAGED_ATTN_OK;
+  const int Hq = p->num_qo_heads, Hkv = p->num_kv_heads, G = Hq / Hkv, ps = p->page_size;
+  AttnLaunch a{};
+  const int ck = attn_sub_chunk(p->kv_block_size, true);
+  const int R = page_piece_rows(ps, ck);
+  const long long pool_rows = static_cast<long long>(p->num_pages) * (p->combined_cache ? 2 : 1) *
+                              Hkv * ps;
+  if (!encode_q_map(&a.qmap, q, static_cast<long long>(p->batch) * p->q_len, Hq, D, G,
+                    sub_tile_tokens(G)) ||
+      !encode_rows_map(&a.kmap, k, pool_rows, D, R) ||
+      !encode_rows_map(&a.vmap, p->combined_cache ? k : v, pool_rows, D, R))
+    return PAGED_ATTN_ERR_CUDA;
+  a.tiles = at<TileRec>(ws, s.sorted);
+  a.n_tiles = nullptr;
+  a.capacity = s.capacity;
+  a.pt = m->kv_indices_dev;
+  a.pt_indptr = m->kv_indptr_dev;
+  a.pt_stride = 0;
+  a.seq_lens = m->seq_lens_kv_dev;
+  a.qo_indptr = nullptr;
+  a.q_len = p->q_len;
+  a.valid_bits = p->has_valid_bits ? m->kv_valid_bits_dev : nullptr;
+  a.valid_words = ceil_div(p->max_seq_len_kv > 0 ? p->max_seq_len_kv : 1, 32);
+  a.block_sparse = 1;
+  a.block_indices = m->block_indices_dev;
+  a.kv_block_size = p->kv_block_size;
+  a.out = out;
+  a.out_dtype = PAGED_ATTN_DTYPE_BF16;
+  a.lse = lse;
+  a.status = status;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = G;
+  a.D = D;
+  a.page_size = ps;
+  a.page_rows = (p->combined_cache ? 2 : 1) * Hkv * ps;
+  a.k_head_off = 0;
+  a.v_head_off = p->combined_cache ? Hkv * ps : 0;
+  a.num_pages = p->num_pages;
+  a.causal = p->mask_type == PAGED_ATTN_MASK_CAUSAL;
+  a.window_left = -1;
+  a.scale_log2 = scale * kLog2e;
+  a.out_scale = 1.0f;
+  if (sc) {
+    a.q_scale = sc->q_scale;
+    a.k_scale = sc->k_scale;
+    a.v_scale = sc->v_scale;
+    a.q_scale_group = sc->q_group;
+    a.q_scale_stride = sc->q_stride;
+    a.k_scale_stride = sc->k_stride;
+    a.v_scale_stride = sc->v_stride;
+  }
+  void* tok;
+  timer_begin(st, &tok);
+  const int rc = launch_attn(a, st);
+  timer_end(st, tok);
+  if (rc == -2) return PAGED_ATTN_ERR_UNSUPPORTED;
+  return rc == 0 ? PAGED_ATTN_OK : PAGED_ATTN_ERR_CUDA;
+}
+
 }  // namespace pa
 
 using namespace pa;
@@ -558,55 +695,7 @@ int paged_attn_run(const paged_attn_params* p, const paged_attn_meta* m, const v
   if (p->has_valid_bits && !m->kv_valid_bits_dev) return PAGED_ATTN_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(k) || (v && !aligned16(v)) || !aligned16(out))
     return PAGED_ATTN_ERR_INVALID_ARGUMENT;
-  if (s.capacity == 0) return PAGED_ATTN_OK;
-  const int Hq = p->num_qo_heads, Hkv = p->num_kv_heads, G = Hq / Hkv, ps = p->page_size;
-  AttnLaunch a{};
-  const int ck = attn_sub_chunk(p->kv_block_size, true);
-  const int R = page_piece_rows(ps, ck);
-  const long long pool_rows = static_cast<long long>(p->num_pages) * (p->combined_cache ? 2 : 1) *
-                              Hkv * ps;
-  if (!encode_q_map(&a.qmap, q, static_cast<long long>(p->batch) * p->q_len, Hq, D, G,
-                    sub_tile_tokens(G)) ||
-      !encode_rows_map(&a.kmap, k, pool_rows, D, R) ||
-      !encode_rows_map(&a.vmap, p->combined_cache ? k : v, pool_rows, D, R))
-    return PAGED_ATTN_ERR_CUDA;
-  a.tiles = at<TileRec>(ws, s.sorted);
-  a.n_tiles = nullptr;
-  a.capacity = s.capacity;
-  a.pt = m->kv_indices_dev;
-  a.pt_indptr = m->kv_indptr_dev;
-  a.pt_stride = 0;
-  a.seq_lens = m->seq_lens_kv_dev;
-  a.qo_indptr = nullptr;
-  a.q_len = p->q_len;
-  a.valid_bits = p->has_valid_bits ? m->kv_valid_bits_dev : nullptr;
-  a.valid_words = ceil_div(p->max_seq_len_kv > 0 ? p->max_seq_len_kv : 1, 32);
-  a.block_sparse = 1;
-  a.block_indices = m->block_indices_dev;
-  a.kv_block_size = p->kv_block_size;
-  a.out = out;
-  a.out_dtype = PAGED_ATTN_DTYPE_BF16;
-  a.lse = lse;
-  a.status = status;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.G = G;
-  a.D = D;
-  a.page_size = ps;
-  a.page_rows = (p->combined_cache ? 2 : 1) * Hkv * ps;
-  a.k_head_off = 0;
-  a.v_head_off = p->combined_cache ? Hkv * ps : 0;
-  a.num_pages = p->num_pages;
-  a.causal = p->mask_type == PAGED_ATTN_MASK_CAUSAL;
-  a.window_left = -1;
-  a.scale_log2 = scale * kLog2e;
-  a.out_scale = 1.0f;
-  void* tok;
-  timer_begin(st, &tok);
-  const int rc = launch_attn(a, st);
-  timer_end(st, tok);
-  if (rc == -2) return PAGED_ATTN_ERR_UNSUPPORTED;
-  return rc == 0 ? PAGED_ATTN_OK : PAGED_ATTN_ERR_CUDA;
+  return bsr_launch(p, m, s, q, k, v, out, lse, ws, status, scale, nullptr, st);
 }
 
 size_t paged_prefill_workspace_size(const paged_prefill_params* p) {
@@ -863,6 +952,82 @@ int paged_attn_workspace_status(const void* ws, void* stream, uint32_t* raw) {
   if (word & kErrCapacity) return PAGED_ATTN_ERR_CAPACITY;
   if (word & kErrMetadata) return PAGED_ATTN_ERR_METADATA;
   return PAGED_ATTN_OK;
+}
+
+
+size_t paged_sage_workspace_size(const paged_sage_params* p) {
+  if (!sage_params_ok(p)) return 0;
+  return sage_layout(p).total;
+}
+
+int paged_sage_run(const paged_sage_params* p, const int8_t* q_int8, const int8_t* k_int8,
+                   const uint8_t* v_fp8, const float* q_scale, const float* k_scale,
+                   const float* v_scale, const int32_t* idx, const int32_t* nums,
+                   const int32_t* block_sizes, void* out, void* ws, size_t ws_bytes,
+                   void* stream) {
+  if (!sage_params_ok(p) || !out) return PAGED_ATTN_ERR_INVALID_ARGUMENT;
+  const SageLayout g = sage_layout(p);
+  if (!ws || ws_bytes < g.total) return PAGED_ATTN_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t* status = at<uint32_t>(ws, g.s.status);
+  if (cudaMemsetAsync(status, 0, 4 * sizeof(uint32_t), st) != cudaSuccess) return PAGED_ATTN_ERR_CUDA;
+  if (g.BH == 0 || p->q_len == 0) return PAGED_ATTN_OK;
+  if (g.NB == 0) {                               // no keys: every row is empty, O = 0
+    return cudaMemsetAsync(out, 0, static_cast<size_t>(g.BH) * p->q_len * 128 * 2, st) ==
+                   cudaSuccess
+               ? PAGED_ATTN_OK
+               : PAGED_ATTN_ERR_CUDA;
+  }
+  if (!q_int8 || !k_int8 || !v_fp8 || !q_scale || !k_scale || !v_scale || (p->capacity > 0 && !idx) ||
+      (p->block_sizes_rank > 0 && !block_sizes))
+    return PAGED_ATTN_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q_int8) || !aligned16(k_int8) || (reinterpret_cast<uintptr_t>(v_fp8) & 3u) ||
+      !aligned16(out))
+    return PAGED_ATTN_ERR_INVALID_ARGUMENT;
+  SagePrepare sp{};
+  sp.q_int8 = q_int8;
+  sp.k_int8 = k_int8;
+  sp.v_fp8 = v_fp8;
+  sp.q_bf16 = at<__nv_bfloat16>(ws, g.q_bf16);
+  sp.k_bf16 = at<__nv_bfloat16>(ws, g.k_bf16);
+  sp.v_bf16 = at<__nv_bfloat16>(ws, g.v_bf16);
+  sp.idx = idx;
+  sp.nums = p->uniform_block_count ? nullptr : nums;
+  sp.uniform = p->block_sparse_num;
+  sp.cap = p->capacity;
+  sp.block_sizes = block_sizes;
+  sp.bs_rank = p->block_sizes_rank;
+  sp.B = p->batch;
+  sp.H = p->num_heads;
+  sp.Sq = p->q_len;
+  sp.Sk = p->kv_len;
+  sp.NB = g.NB;
+  sp.QB = g.QB;
+  sp.counts = at<int>(ws, g.counts);
+  sp.block_indptr = at<int>(ws, g.block_indptr);
+  sp.block_indices = at<int>(ws, g.block_indices);
+  sp.kv_indptr = at<int>(ws, g.kv_indptr);
+  sp.kv_indices = at<int>(ws, g.kv_indices);
+  sp.seq_lens = at<int>(ws, g.seq_lens);
+  sp.valid_bits = at<uint32_t>(ws, g.valid_bits);
+  sp.status = status;
+  launch_sage_prepare(sp, st);
+  // the block-sparse plan of the (b, h) requests
+  const SparseLayout& s = g.s;
+  launch_bsr_tiles(sp.block_indptr, g.BH, 1, p->q_len, 64, s.tile_tokens, at<TileRec>(ws, s.tmp), st);
+  launch_tile_sort(at<TileRec>(ws, s.tmp), at<TileRec>(ws, s.sorted), nullptr, s.capacity,
+                   s.capacity, s.max_cost, at<int>(ws, s.hist), at<int>(ws, s.offs), st);
+  paged_attn_meta m{};
+  m.kv_indptr_dev = sp.kv_indptr;
+  m.kv_indices_dev = sp.kv_indices;
+  m.block_indptr_dev = sp.block_indptr;
+  m.block_indices_dev = sp.block_indices;
+  m.seq_lens_kv_dev = sp.seq_lens;
+  m.kv_valid_bits_dev = sp.valid_bits;
+  ScaleSet sc{q_scale, k_scale, v_scale, 32, g.QG, g.NB, 128};
+  const float scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / std::sqrt(128.0f);
+  return bsr_launch(&g.bsr, &m, s, sp.q_bf16, sp.k_bf16, sp.v_bf16, out, nullptr, ws, status,
+                    scale, &sc, st);
 }
 
 }  // extern "C"

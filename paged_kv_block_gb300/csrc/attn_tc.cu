@@ -57,6 +57,7 @@ struct TileFacts {
   int kmin, kmax;          // key range of the used sub-chunks
   int zero_v;              // some key slot is not live (V rows to zero)
   int pad;
+  float cs[kKvTile / 8];   // scaled form: key scale of each sub-chunk's block
 };
 
 struct Ctrl {
@@ -144,7 +145,9 @@ __device__ __forceinline__ int piece_key(const AttnLaunch& a, const TileInfo<CK>
   return (k0 >= 0 && key < t.L && key / ps < max_page_idx) ? key : -1;
 }
 
-template <int CK, bool FACTS>
+// SCALED: the prequantized form, whose scores carry a scale per query group and per key
+// block and whose output carries a scale per channel (all positive).
+template <int CK, bool FACTS, bool SCALED>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                const __grid_constant__ CUtensorMap vmap, AttnLaunch a) {
@@ -298,6 +301,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         const bool has_c = lane < NSUB;          // lane c: sub-chunk c
         const int k0 = has_c ? t.walk.key0(n, lane) : -1;
         if (has_c) f->k0[lane] = k0;
+        if (SCALED && has_c)
+          f->cs[lane] = k0 >= 0 ? __ldg(a.k_scale + static_cast<long long>(t.rec.b) *
+                                                        a.k_scale_stride + k0 / a.kv_block_size)
+                                : 0.f;
         // lane s < NSUB * PARTS: span `part` of sub-chunk c
         const int c_of = min(lane / PARTS, NSUB - 1);
         const int kc = __shfl_sync(0xffffffffu, k0, c_of);
@@ -469,6 +476,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       const int tok = t.rec.tok0 + w * TM + m / G;   // token index inside the request
       const bool row_valid = (m < G * TM) && (m / G < ntok_w);
       const int pos = L - t.nq + tok;                // query position
+      // scaled form: the row's query scale joins the softmax scale (scales are positive)
+      float sl2r = sl2;
+      if constexpr (SCALED)
+        if (row_valid)
+          sl2r = sl2 * __ldg(a.q_scale + static_cast<long long>(t.rec.b) * a.q_scale_stride +
+                             tok / a.q_scale_group);
       float m_run = -INFINITY, l_run = 0.f;
       for (int n = 0; n < N; ++n) {
         const int it = kv_it + n;
@@ -480,6 +493,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         tc_fence_after();
         // ---- per-tile column facts, identical for every row ----------------------------
         int k0[NSUB];
+        float cs[NSUB];                            // scaled form: key scale per sub-chunk
         uint32_t colmask[4];
         int kmin, kmax;
         bool zero_v, full;
@@ -497,6 +511,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           kmin = fc->kmin;
           kmax = fc->kmax;
           zero_v = fc->zero_v != 0;
+          if constexpr (SCALED) {
+#pragma unroll
+            for (int c = 0; c < NSUB; ++c) cs[c] = fc->cs[c];
+          }
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl->facts_empty[it % kFacts]);
           full = !a.valid_bits && !zero_v && (!causal || kmax <= pos) && (wl < 0 || kmin >= pos - wl);
@@ -552,6 +570,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         for (int q = 0; q < 4; ++q)
           tmem_ld32(s_col + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[q * 32]));
         tmem_ld_wait();
+        if constexpr (SCALED) {
+#pragma unroll
+          for (int c = 0; c < kKvTile; ++c)
+            r[c] = __float_as_uint(__uint_as_float(r[c]) * cs[c / CK]);
+        }
         if (!full) {
           // Invisible scores become -inf in place.  Column facts (slot live, j < len, valid
           // bit) are the same for every row: only 32-column words with a dead key are touched.
@@ -608,7 +631,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         // scores are scaled by sl2 > 0 after the maximum, which commutes with it
         const float mt =
             fmaxf(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], fmaxf(mx[5], fmaxf(mx[6], mx[7])))) *
-            sl2;
+            sl2r;
         // ---- online softmax with a lazily moved maximum ----------------------------------
         float alpha = 1.f;
         if (mt > m_run + kRescaleThreshold || (m_run == -INFINITY && mt > -INFINITY)) {
@@ -621,7 +644,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 #pragma unroll
         for (int j = 0; j < kKvTile / 2; ++j) {
           float x0, x1;
-          ffma2_bcast(x0, x1, __uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]), sl2, nmu);
+          ffma2_bcast(x0, x1, __uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]), sl2r, nmu);
           // two f32 ex2 per pair outrun the f16x2 form, whose three conversions cost more
           // than the second ex2
           const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
@@ -688,6 +711,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             tc_fence_before();
             mbar_arrive(&ctl->o_empty[w]);
           }
+          if constexpr (SCALED) {             // per-channel value scales
+            const float* vs = a.v_scale + static_cast<long long>(t.rec.b) * a.v_scale_stride + q * 32;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * __ldg(vs + i));
+          }
         }
         if (row_valid && a.out_dtype == kOutF32) {
           float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * kD + q * 32);
@@ -728,11 +756,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
 
 int g_num_sms = 0;
 
-template <int CK, bool FACTS>
+template <int CK, bool FACTS, bool SCALED = false>
 int launch_ck(const AttnLaunch& a, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_tc_kernel<CK, FACTS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_tc_kernel<CK, FACTS, SCALED>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess)
       return -1;
     attr_set = true;
@@ -744,7 +773,7 @@ int launch_ck(const AttnLaunch& a, cudaStream_t st) {
       return -1;
   }
   const int grid = a.capacity < g_num_sms ? a.capacity : g_num_sms;
-  attn_tc_kernel<CK, FACTS><<<grid, kThreads, kSmemBytes, st>>>(a.qmap, a.kmap, a.vmap, a);
+  attn_tc_kernel<CK, FACTS, SCALED><<<grid, kThreads, kSmemBytes, st>>>(a.qmap, a.kmap, a.vmap, a);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
@@ -753,6 +782,12 @@ int launch_ck(const AttnLaunch& a, cudaStream_t st) {
 
 int launch_attn(const AttnLaunch& a, cudaStream_t st) {
   if (a.capacity <= 0) return 0;
+  if (a.k_scale) {                               // the prequantized form: 64-key blocks only
+    if (!a.block_sparse || attn_sub_chunk(a.kv_block_size, true) != 64 || !a.q_scale ||
+        !a.v_scale || a.q_scale_group <= 0)
+      return -2;
+    return launch_ck<64, true, true>(a, st);
+  }
   switch (attn_sub_chunk(a.kv_block_size, a.block_sparse != 0)) {
     case 8: return launch_ck<8, true>(a, st);
     case 16: return launch_ck<16, true>(a, st);

@@ -149,10 +149,45 @@ struct AttnLaunch {
   int Hq, Hkv, G, D, page_size, page_rows, k_head_off, v_head_off, num_pages;
   int causal, window_left;
   float scale_log2, out_scale;
+  // Prequantized form (all nullptr otherwise): score scale q_scale[b * q_scale_stride +
+  // token / q_scale_group] * k_scale[b * k_scale_stride + key / kv_block_size], output column
+  // d scaled by v_scale[b * v_scale_stride + d]; every scale positive.
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
+  int q_scale_group, q_scale_stride, k_scale_stride, v_scale_stride;
 };
 int launch_attn(const AttnLaunch& a, cudaStream_t st);
 // Dense prefill tiles of head dimension 256 (one 128-row sub-tile per planner tile).
 int launch_attn256(const AttnLaunch& a, cudaStream_t st);
+
+// ---- prequantized block-sparse form (sage.cu) ------------------------------------------------
+// Exact bf16 copies of the int8 Q/K and FP8 V, and the block-sparse metadata of the (b, h)
+// requests: identity pages of 64 keys, lengths, validity bits from the block sizes, BSR rows
+// from the index rows (ids outside [0, NB) dropped and reported).
+struct SagePrepare {
+  const int8_t* q_int8;          // [B, H, Sq, 128]
+  const int8_t* k_int8;          // [B, H, Sk, 128]
+  const uint8_t* v_fp8;          // [B, H, 128, NB * 64]
+  __nv_bfloat16* q_bf16;         // [B * H, Sq, 128]
+  __nv_bfloat16* k_bf16;         // [B * H * NB pages, 64, 128]
+  __nv_bfloat16* v_bf16;         // [B * H * NB pages, 64, 128]
+  const int* idx;                // [B, H, QB, cap]
+  const int* nums;               // [B, H, QB] or nullptr (uniform)
+  int uniform, cap;
+  const int* block_sizes;        // rank bs_rank: 0 none, 1 [NB], 2 [B, NB], 3 [B, H, NB]
+  int bs_rank;
+  int B, H, Sq, Sk, NB, QB;
+  int* counts;                   // [B * H * QB] scratch
+  int* block_indptr;             // [B * H, QB + 1]
+  int* block_indices;            // [B * H * QB * cap]
+  int* kv_indptr;                // [B * H + 1]
+  int* kv_indices;               // [B * H * NB]
+  int* seq_lens;                 // [B * H]
+  uint32_t* valid_bits;          // [B * H, 2 * NB]
+  uint32_t* status;
+};
+void launch_sage_prepare(const SagePrepare& s, cudaStream_t st);
 
 // ---- tensor maps (api.cu) -----------------------------------------------------------------
 bool encode_rows_map(CUtensorMap* map, const void* base, long long rows, int D, int box_rows);
