@@ -217,6 +217,29 @@ def qsa_indexed_pairs(p):
         p["q"].shape[1]
 
 
+def sage_pairs(p):
+    """Visible (query, head, key) triples of the prequantized form."""
+    B, H, Sq, _ = p["q_int8"].shape
+    Sk = p["k_int8"].shape[2]
+    idx = p["q2k_block_index"].numpy()
+    nums = p["q2k_block_nums"].numpy() if p["q2k_block_nums"] is not None else None
+    bs = p["block_sizes"]
+    total = 0
+    for b in range(B):
+        for h in range(H):
+            for r in range(-(-Sq // 64)):
+                n = int(nums[b, h, r]) if nums is not None else p["block_sparse_num"]
+                rows = min(64, Sq - 64 * r)
+                for c in idx[b, h, r, :n]:
+                    c = int(c)
+                    size = min(64, Sk - 64 * c)
+                    if bs is not None:
+                        size = min(size, int(bs.reshape(-1)[c] if bs.dim() == 1 else
+                                              (bs[b, c] if bs.dim() == 2 else bs[b, h, c])))
+                    total += rows * max(size, 0)
+    return total
+
+
 # ----------------------------------------------------------------------------------------
 # one workload on the GPU
 # ----------------------------------------------------------------------------------------
@@ -240,10 +263,17 @@ def make_workload(name):
         return W.qsa_t32k()
     if name == "qsa_t32k_indexed":
         return W.qsa_t32k_indexed()
+    if name == "sage_b2h16":
+        return W.sage_b2h16()
     raise ValueError(name)
 
 
 def describe(name, p):
+    if p["form"] == "sage":
+        B, H, Sq, D = p["q_int8"].shape
+        return {"workload": name, "batch": B, "num_heads": H, "q_len": Sq,
+                "kv_len": int(p["k_int8"].shape[2]), "head_dim": D, "blocks_per_row":
+                p["block_sparse_num"], "inputs": "int8 Q/K, FP8 E4M3 V, fp32 scales"}
     if p["form"] == "decode":
         d = {"workload": name, "batch": int(p["q"].shape[0]), "num_qo_heads": int(p["q"].shape[-2]),
              "num_kv_heads": int(p["kv_cache"].shape[2]), "head_dim": int(p["q"].shape[-1]),
@@ -315,6 +345,14 @@ class Runner:
                                   dtype=torch.uint8, device=dev)
             self.out = torch.empty_like(d["q"])
             self.lse = torch.empty(d["q"].shape[:2], dtype=torch.float32, device=dev)
+        elif self.form == "sage":
+            self.params = pkb.sage_params(d["q_int8"], d["k_int8"], d["q2k_block_index"],
+                                          p["block_sparse_num"], block_sizes=d["block_sizes"],
+                                          softmax_scale=p["softmax_scale"],
+                                          uniform_block_count=p["q2k_block_nums"] is None)
+            self.ws = torch.zeros(pkb.paged_sage_workspace_size(self.params), dtype=torch.uint8,
+                                  device=dev)
+            self.out = torch.empty(d["q_int8"].shape, dtype=torch.bfloat16, device=dev)
         else:
             if self.form == "qsa_indexed":
                 self.params = pkb.qsa_indexed_params(d["q"], d["k"], d["block_first"].numel(),
@@ -344,7 +382,9 @@ class Runner:
                  "qsa": ["q", "k", "v", "sel_blocks", "lo", "hi", "blk_base", "tok_base",
                          "block_first", "block_last"],
                  "qsa_indexed": ["q", "k", "v", "sel_indices", "lo", "hi", "block_first",
-                                 "block_last"]}[self.form]
+                                 "block_last"],
+                 "sage": ["q_int8", "k_int8", "v_fp8", "q_scale", "k_scale", "v_scale",
+                          "q2k_block_index", "q2k_block_nums", "block_sizes"]}[self.form]
         return [(n, self.d[n]) for n in names if isinstance(self.d.get(n), torch.Tensor)]
 
     def step(self):
@@ -357,6 +397,10 @@ class Runner:
             pkb.paged_attn_plan(self.params, self.meta, self.ws)
             pkb.paged_attn_run(self.params, self.meta, d["q"], self.k, self.v, self.out, None,
                                self.lse, self.ws)
+        elif self.form == "sage":
+            pkb.paged_sage_run(self.params, d["q_int8"], d["k_int8"], d["v_fp8"], d["q_scale"],
+                               d["k_scale"], d["v_scale"], d["q2k_block_index"],
+                               d["q2k_block_nums"], d["block_sizes"], self.out, self.ws)
         elif self.form == "prefill":
             pkb.paged_prefill_run(self.params, d["q"], d["k_cache"], d["v_cache"],
                                   d["qo_indptr"], d["block_tables"], d["seq_lens_kv"], self.out,
@@ -560,8 +604,8 @@ def main():
     else:
         nbytes = None
         units = {"bsr": bsr_pairs, "prefill": prefill_pairs, "qsa": qsa_pairs,
-                 "qsa_indexed": qsa_indexed_pairs}[p["form"]](p)
-        units *= 4 * p["q"].shape[-1]
+                 "qsa_indexed": qsa_indexed_pairs, "sage": sage_pairs}[p["form"]](p)
+        units *= 4 * (p["q"] if "q" in p else p["q_int8"]).shape[-1]
         unit, scale = "TFLOP/s", 1e12
         kernel = "qsa_kernel" if p["form"] in ("qsa", "qsa_indexed") else "attn_tc_kernel"
         bound, peak = "tensor", pk["bf16_tflops"]
@@ -594,7 +638,8 @@ def main():
     if not args.no_extra and rank == 0:
         extra = {}
         for name in ("decode_b64_sq4", "tiny_bsr", "prefill_b16", "prefill_b16_w1023",
-                     "prefill_b16_d256", "long_bsr", "qsa_t32k", "qsa_t32k_indexed"):
+                     "prefill_b16_d256", "long_bsr", "qsa_t32k", "qsa_t32k_indexed",
+                     "sage_b2h16"):
             if name == args.workload:
                 continue
             try:
@@ -615,8 +660,8 @@ def main():
                     torch.cuda.empty_cache()
                     continue
                 n = {"bsr": bsr_pairs, "prefill": prefill_pairs, "qsa": qsa_pairs,
-                     "qsa_indexed": qsa_indexed_pairs}[q["form"]](q)
-                flops = 4 * q["q"].shape[-1] * n
+                     "qsa_indexed": qsa_indexed_pairs, "sage": sage_pairs}[q["form"]](q)
+                flops = 4 * (q["q"] if "q" in q else q["q_int8"]).shape[-1] * n
                 extra[name] = {"tflops_step": flops / (reg / steps * 1e-3) / 1e12,
                                "tflops_kernel": flops / (kms * 1e-3) / 1e12,
                                "frac_bf16_peak": flops / (kms * 1e-3) / 1e12 / pk["bf16_tflops"],

@@ -538,3 +538,10 @@ def qsa_t32k_indexed(seed=1005, lens=(4096, 8192, 8192, 12288)):
     row's selected block ids in a seeded random order (rows with fewer blocks padded with -1)."""
     return make_qsa_indexed_problem(seed, list(lens), Hq=24, Hkv=2, D=256, block_size=4,
                                     n_near=16, n_random=256, scale=1.0 / 16)
+
+
+def sage_b2h16(seed=1006):
+    """Prequantized block-sparse attention: B=2, H=16, Sq=Sk=4096, D=128, 16 distinct uniform
+    64-key blocks per 64-query block (block_sparse_num, uniform), no block sizes."""
+    return make_sage_problem(seed, B=2, H=16, Sq=4096, Sk=4096, capacity=16, uniform=16,
+                             sizes="none")
