@@ -118,6 +118,8 @@ KERNEL_SOURCES = {
     "qsa_kernel": ["paged_kv_block_gb300/csrc/qsa.cu", "paged_kv_block_gb300/csrc/common.cuh"],
     "attn_tc_kernel": ["paged_kv_block_gb300/csrc/attn_tc.cu",
                        "paged_kv_block_gb300/csrc/common.cuh"],
+    "attn256_kernel": ["paged_kv_block_gb300/csrc/attn256.cu",
+                       "paged_kv_block_gb300/csrc/common.cuh"],
 }
 
 
@@ -608,6 +610,8 @@ def main():
         units *= 4 * (p["q"] if "q" in p else p["q_int8"]).shape[-1]
         unit, scale = "TFLOP/s", 1e12
         kernel = "qsa_kernel" if p["form"] in ("qsa", "qsa_indexed") else "attn_tc_kernel"
+        if p["form"] == "prefill" and p["q"].shape[-1] == 256:
+            kernel = "attn256_kernel"
         bound, peak = "tensor", pk["bf16_tflops"]
     value = units * world / (ms_step * 1e-3) / scale
     achieved = units / (kernel_ms * 1e-3) / scale
