@@ -67,15 +67,17 @@ struct Tile {
 // The keys the tile's rows can see are [lo, hi): hi = min(L, p(last row) + 1) under the
 // causal mask (L otherwise) and lo = max(0, p(first row) - window_left) with a window, where
 // p(token i) = L - nq + i.  They are walked in 64-key tiles.
-__device__ __forceinline__ Tile make_tile(const AttnLaunch& a, const TileRec& r) {
+// L and nq are request b's KV length and query count.
+__device__ __forceinline__ Tile tile_from_parts(const AttnLaunch& a, const TileRec& r, int L,
+                                                int nq) {
   Tile t;
   t.b = r.b;
   t.g = r.g;
   t.tok0 = r.tok0;
   t.ntok = r.ntok;
   t.q_row0 = r.q_row0;
-  t.L = __ldg(a.seq_lens + r.b);
-  t.nq = a.qo_indptr ? __ldg(a.qo_indptr + r.b + 1) - __ldg(a.qo_indptr + r.b) : a.q_len;
+  t.L = L;
+  t.nq = nq;
   const long long p0 = static_cast<long long>(t.L) - t.nq + r.tok0;
   const long long p1 = p0 + r.ntok - 1;
   const long long hi = a.causal ? min(static_cast<long long>(t.L), p1 + 1)
@@ -89,6 +91,17 @@ __device__ __forceinline__ Tile make_tile(const AttnLaunch& a, const TileRec& r)
     t.N = static_cast<int>((hi + kKeys - 1) / kKeys) - t.kt0;
   }
   return t;
+}
+
+__device__ __forceinline__ void request_lengths(const AttnLaunch& a, int b, int& L, int& nq) {
+  L = __ldg(a.seq_lens + b);
+  nq = a.qo_indptr ? __ldg(a.qo_indptr + b + 1) - __ldg(a.qo_indptr + b) : a.q_len;
+}
+
+__device__ __forceinline__ Tile make_tile(const AttnLaunch& a, const TileRec& r) {
+  int L, nq;
+  request_lengths(a, r.b, L, nq);
+  return tile_from_parts(a, r, L, nq);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -316,8 +329,16 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int wl = a.window_left;
     int kv_it = 0, ep = 0;
     bool ok = true;
+    // The next work tile's record is read after the current tile's last softmax and its KV
+    // length and query count after the wait for O, so a work tile starts without a global
+    // round trip.
+    TileRec rec_nx = a.tiles[blockIdx.x];
+    int L_nx, nq_nx;
+    request_lengths(a, rec_nx.b, L_nx, nq_nx);
     for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
-      const Tile t = make_tile(a, a.tiles[idx]);
+      const Tile t = tile_from_parts(a, rec_nx, L_nx, nq_nx);
+      const int idx_nx = idx + static_cast<int>(gridDim.x);
+      const bool has_nx = idx_nx < n_live;
       const int tok = m / G;                             // token inside the work tile
       const bool row_valid = m < G * TM && tok < t.ntok;
       const int pos = t.L - t.nq + t.tok0 + tok;        // query position
@@ -419,6 +440,7 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         mbar_arrive(&ctl->p_full[it & 1]);
       }
       if (!ok) break;
+      if (has_nx) rec_nx = a.tiles[idx_nx];
       // ---- epilogue --------------------------------------------------------------------
       bool have_o = false;
       if (t.N > 0) {
@@ -430,40 +452,58 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
         tc_fence_after();
       }
+      if (has_nx) request_lengths(a, rec_nx.b, L_nx, nq_nx);
       const long long orow = static_cast<long long>(t.q_row0 + tok) * a.Hq + t.g * G + (m % G);
       const float inv = l_run > 0.f ? a.out_scale / l_run : 0.f;
+      // one row per thread in two 128-column halves (four loads in flight each), 32 bytes per
+      // store where the output allows it (rows are 512 or 1024 bytes: the base decides)
+      const bool wide = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
 #pragma unroll 1
-      for (int q = 0; q < kD / 32; ++q) {
-        uint32_t ov[32];
+      for (int h = 0; h < 2; ++h) {
+        uint32_t ov[128];
         if (have_o) {
-          tmem_ld32(o_col + q * 32, ov);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            tmem_ld32(o_col + h * 128 + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[q * 32]));
           tmem_ld_wait();
-          if (q == kD / 32 - 1) {                // O fully read: the next work tile may write
+          if (h == 1) {                          // O fully read: the next work tile may write
             tc_fence_before();
             mbar_arrive(&ctl->o_empty);
           }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) ov[i] = 0u;
         }
         if (row_valid && a.out_dtype == kOutF32) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * kD + q * 32);
+          float* dst = static_cast<float*>(a.out) + orow * kD + h * 128;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = have_o ? make_float4(__uint_as_float(ov[4 * i]) * inv,
-                                          __uint_as_float(ov[4 * i + 1]) * inv,
-                                          __uint_as_float(ov[4 * i + 2]) * inv,
-                                          __uint_as_float(ov[4 * i + 3]) * inv)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int i = 0; i < 16; ++i) {
+            uint32_t v8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v8[e] = __float_as_uint(__uint_as_float(ov[8 * i + e]) * inv);
+            if (wide) {
+              st_global_v8(dst + 8 * i, v8);
+            } else {
+              reinterpret_cast<uint4*>(dst + 8 * i)[0] = make_uint4(v8[0], v8[1], v8[2], v8[3]);
+              reinterpret_cast<uint4*>(dst + 8 * i)[1] = make_uint4(v8[4], v8[5], v8[6], v8[7]);
+            }
+          }
         } else if (row_valid) {
-          uint32_t pkd[16];
+          uint16_t* dst = static_cast<uint16_t*>(a.out) + orow * kD + h * 128;
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pkd[i] = have_o ? pack_out2(__uint_as_float(ov[2 * i]) * inv,
-                                        __uint_as_float(ov[2 * i + 1]) * inv, a.out_dtype)
-                            : 0u;
-          uint4* dst =
-              reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * kD + q * 32);
+          for (int i = 0; i < 8; ++i) {
+            uint32_t v8[8];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+            for (int e = 0; e < 8; ++e)
+              v8[e] = pack_out2(__uint_as_float(ov[16 * i + 2 * e]) * inv,
+                                __uint_as_float(ov[16 * i + 2 * e + 1]) * inv, a.out_dtype);
+            if (wide) {
+              st_global_v8(dst + 16 * i, v8);
+            } else {
+              reinterpret_cast<uint4*>(dst + 16 * i)[0] = make_uint4(v8[0], v8[1], v8[2], v8[3]);
+              reinterpret_cast<uint4*>(dst + 16 * i)[1] = make_uint4(v8[4], v8[5], v8[6], v8[7]);
+            }
+          }
         }
       }
       if (row_valid && a.lse)

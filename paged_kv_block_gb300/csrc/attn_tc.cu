@@ -103,17 +103,24 @@ struct TileInfo {
   KvWalk<CK> walk;
 };
 
+// KV length and query count of request b (the two global reads a work tile needs beyond its
+// record).
+__device__ __forceinline__ void request_lengths(const AttnLaunch& a, int b, int& L, int& nq) {
+  L = __ldg(a.seq_lens + b);
+  nq = a.qo_indptr ? (__ldg(a.qo_indptr + b + 1) - __ldg(a.qo_indptr + b)) : a.q_len;
+}
+
 template <int CK>
-__device__ __forceinline__ TileInfo<CK> tile_from_rec(const AttnLaunch& a, const TileRec& rec) {
+__device__ __forceinline__ TileInfo<CK> tile_from_parts(const AttnLaunch& a, const TileRec& rec,
+                                                        int L, int nq) {
   TileInfo<CK> t;
   t.rec = rec;
   const int TM = kMTileRows / a.G;
   t.ntok0 = min(t.rec.ntok, TM);
   t.ntok1 = t.rec.ntok - t.ntok0;
   t.nsub = t.ntok1 > 0 ? 2 : 1;
-  t.L = __ldg(a.seq_lens + t.rec.b);
-  t.nq = a.qo_indptr ? (__ldg(a.qo_indptr + t.rec.b + 1) - __ldg(a.qo_indptr + t.rec.b))
-                     : a.q_len;
+  t.L = L;
+  t.nq = nq;
   t.walk.dense = !a.block_sparse;
   t.walk.kv_begin = t.rec.kv_begin;
   t.walk.kv_end = t.rec.kv_end;
@@ -126,8 +133,10 @@ __device__ __forceinline__ TileInfo<CK> tile_from_rec(const AttnLaunch& a, const
 }
 
 template <int CK>
-__device__ __forceinline__ TileInfo<CK> load_tile(const AttnLaunch& a, int idx) {
-  return tile_from_rec<CK>(a, a.tiles[idx]);
+__device__ __forceinline__ TileInfo<CK> tile_from_rec(const AttnLaunch& a, const TileRec& rec) {
+  int L, nq;
+  request_lengths(a, rec.b, L, nq);
+  return tile_from_parts<CK>(a, rec, L, nq);
 }
 
 // Page piece `lane` of KV tile n: keys [key, key + R) of one page (R = page_piece_rows).
@@ -458,8 +467,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int wl = a.window_left;
     int kv_it = 0, sc = 0, oc = 0;
     bool ok = true;
+    // The next work tile's record is read after the current tile's last softmax and its KV
+    // length and query count after the wait for O, so both reads overlap the end of the tile
+    // and a work tile starts without a global round trip.
+    TileRec rec_nx = a.tiles[blockIdx.x];
+    int L_nx, nq_nx;
+    request_lengths(a, rec_nx.b, L_nx, nq_nx);
     for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
-      const TileInfo<CK> t = load_tile<CK>(a, idx);
+      const TileInfo<CK> t = tile_from_parts<CK>(a, rec_nx, L_nx, nq_nx);
+      const int idx_nx = idx + static_cast<int>(gridDim.x);
+      const bool has_nx = idx_nx < n_live;
       const int N = t.N;
       const int ntok_w = w == 0 ? t.ntok0 : t.ntok1;
       if (w >= t.nsub) {                           // this sub-tile is empty
@@ -468,6 +485,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           ok = mbar_wait_warp<true>(&ctl->facts_full[it % kFacts], (it / kFacts) & 1, a.status,
                                     abort_flag);
           if (ok && lane == 0) mbar_arrive(&ctl->facts_empty[it % kFacts]);
+        }
+        if (has_nx) {
+          rec_nx = a.tiles[idx_nx];
+          request_lengths(a, rec_nx.b, L_nx, nq_nx);
         }
         kv_it += N;
         continue;
@@ -691,6 +712,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         tc_fence_before();
         mbar_arrive(&ctl->p_full[w]);
       }
+      if (has_nx) rec_nx = a.tiles[idx_nx];
       // ---- epilogue ------------------------------------------------------------------------
       bool have_o = false;
       if (ok && N > 0) {
@@ -698,46 +720,60 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         ++oc;
         if (have_o) tc_fence_after();
       }
+      if (has_nx) request_lengths(a, rec_nx.b, L_nx, nq_nx);
       const int head = t.rec.g * G + (m % G);
       const long long orow = static_cast<long long>(t.rec.q_row0 + w * TM + m / G) * a.Hq + head;
       const float inv = l_run > 0.f ? a.out_scale / l_run : 0.f;
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        uint32_t ov[32];
-        if (have_o) {
-          tmem_ld32(o_col + q * 32, ov);
-          tmem_ld_wait();
-          if (q == 3) {                       // O_w fully read: the next tile may overwrite it
-            tc_fence_before();
-            mbar_arrive(&ctl->o_empty[w]);
-          }
-          if constexpr (SCALED) {             // per-channel value scales
-            const float* vs = a.v_scale + static_cast<long long>(t.rec.b) * a.v_scale_stride + q * 32;
+      // the whole O row in flight at once; O_w is then free for the next tile's PV
+      uint32_t ov[kD];
+      if (have_o) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * __ldg(vs + i));
+        for (int q = 0; q < 4; ++q)
+          tmem_ld32(o_col + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[q * 32]));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&ctl->o_empty[w]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kD; ++i) ov[i] = 0u;
+      }
+      if constexpr (SCALED) {                 // per-channel value scales
+        const float* vsc = a.v_scale + static_cast<long long>(t.rec.b) * a.v_scale_stride;
+#pragma unroll
+        for (int i = 0; i < kD; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * __ldg(vsc + i));
+      }
+      // one row per thread, 32 bytes per store where the output allows it (rows are 256 or
+      // 512 bytes, so only the base address decides)
+      const bool wide = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
+      if (row_valid && a.out_dtype == kOutF32) {
+        float* dst = static_cast<float*>(a.out) + orow * kD;
+#pragma unroll
+        for (int i = 0; i < kD / 8; ++i) {
+          uint32_t v8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v8[e] = __float_as_uint(__uint_as_float(ov[8 * i + e]) * inv);
+          if (wide) {
+            st_global_v8(dst + 8 * i, v8);
+          } else {
+            reinterpret_cast<uint4*>(dst + 8 * i)[0] = make_uint4(v8[0], v8[1], v8[2], v8[3]);
+            reinterpret_cast<uint4*>(dst + 8 * i)[1] = make_uint4(v8[4], v8[5], v8[6], v8[7]);
           }
         }
-        if (row_valid && a.out_dtype == kOutF32) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.out) + orow * kD + q * 32);
+      } else if (row_valid) {
+        uint16_t* dst = static_cast<uint16_t*>(a.out) + orow * kD;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = have_o ? make_float4(__uint_as_float(ov[4 * i]) * inv,
-                                          __uint_as_float(ov[4 * i + 1]) * inv,
-                                          __uint_as_float(ov[4 * i + 2]) * inv,
-                                          __uint_as_float(ov[4 * i + 3]) * inv)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-        } else if (row_valid) {
-          uint32_t pkd[16];
+        for (int i = 0; i < kD / 16; ++i) {
+          uint32_t v8[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pkd[i] = have_o ? pack_out2(__uint_as_float(ov[2 * i]) * inv,
-                                        __uint_as_float(ov[2 * i + 1]) * inv, a.out_dtype)
-                            : 0u;
-          uint4* dst =
-              reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + orow * kD + q * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+          for (int e = 0; e < 8; ++e)
+            v8[e] = pack_out2(__uint_as_float(ov[16 * i + 2 * e]) * inv,
+                              __uint_as_float(ov[16 * i + 2 * e + 1]) * inv, a.out_dtype);
+          if (wide) {
+            st_global_v8(dst + 16 * i, v8);
+          } else {
+            reinterpret_cast<uint4*>(dst + 16 * i)[0] = make_uint4(v8[0], v8[1], v8[2], v8[3]);
+            reinterpret_cast<uint4*>(dst + 16 * i)[1] = make_uint4(v8[4], v8[5], v8[6], v8[7]);
+          }
         }
       }
       if (row_valid && a.lse)

@@ -71,6 +71,13 @@ __device__ __forceinline__ void store_out4(void* out, long long i, float4 v, int
   }
 }
 
+// 32 bytes to a 32-byte aligned global address in one access.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Programmatic dependent launch.  A kernel launched with programmatic stream serialization
 // may start while the previous kernel of its stream still runs: grid_dependency_wait()
 // returns once that kernel has completed and its writes are visible (at once when there is

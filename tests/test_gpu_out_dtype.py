@@ -78,3 +78,26 @@ def test_decode_output_types(kw):
     lens = kw.pop("seq_lens")
     p = W.make_decode_problem(501, lens, D=128, page_size=16, **kw)
     _check_all(lambda dt: _decode(p, dt, split_chunk=256), _decode_ref(p))
+
+
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_prefill_output_at_16_byte_offset(D, dt):
+    """An output that is 16- but not 32-byte aligned takes the 16-byte store path of the
+    epilogue; it must hold exactly what the aligned output holds."""
+    p = W.make_prefill_problem(502, [200, 65], [50, 300], Hq=8, Hkv=2, D=D, page_size=32,
+                               mask_type="causal")
+    aligned, _ = _prefill(p, dt)
+    n = aligned.numel()
+    shift = 16 // aligned.element_size()
+    buf = torch.full((n + shift,), 7.0, dtype=dt, device=DEV)
+    view = buf[shift:].view(aligned.shape)
+    assert view.data_ptr() % 32 == 16
+    d = to_dev(p)
+    pkb.batch_prefill_with_paged_kv_cache(
+        d["q"], d["k_cache"], d["v_cache"], d["qo_indptr"], d["block_tables"], d["seq_lens_kv"],
+        page_size=p["page_size"], mask_type=p["mask_type"], window_left=p["window_left"],
+        sm_scale=p["sm_scale"], output_scale=p["output_scale"], out=view)
+    torch.cuda.synchronize()
+    assert torch.equal(view, aligned)
+    assert torch.all(buf[:shift] == 7.0)
