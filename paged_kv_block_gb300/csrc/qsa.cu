@@ -69,9 +69,12 @@ constexpr int8_t kDeadZero = 0;               // row the copy fills with zeros (
 
 struct QsaCtrl {
   uint64_t full[kPipes][kPairs];
-  uint64_t empty[kPipes][kPairs];
+  // empty[slot]: the MMAs that read the unit in that slot have completed (one barrier for
+  // both pipelines).  For a K unit that is also "S^T of its tile is ready": the softmax waits
+  // on it, which is safe because the slot's next phase belongs to V of the same tile, whose
+  // PV needs that softmax's P^T first.
+  uint64_t empty[kPairs];
   uint64_t tab_full[kTabBufs];
-  uint64_t s_full[2];                         // S^T of tiles n with n % 2 = index
   uint64_t p_full[2];                         // P^T of tiles n with n % 2 = index written
   uint64_t pv_done[2];                        // PV of tiles n with n % 2 = index complete
   uint64_t q_full, o_full;
@@ -212,14 +215,10 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
     *reinterpret_cast<uint4*>(q_s + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x == 0) {
     for (int p = 0; p < kPipes; ++p)
-      for (int i = 0; i < kPairs; ++i) {
-        mbar_init(&ctl->full[p][i], kProducers / kPipes);
-        mbar_init(&ctl->empty[p][i], 1);
-      }
+      for (int i = 0; i < kPairs; ++i) mbar_init(&ctl->full[p][i], kProducers / kPipes);
+    for (int i = 0; i < kPairs; ++i) mbar_init(&ctl->empty[i], 1);
     for (int i = 0; i < kTabBufs; ++i) mbar_init(&ctl->tab_full[i], 32 * kProducers);
     mbar_init(&ctl->q_full, 1);
-    mbar_init(&ctl->s_full[0], 1);
-    mbar_init(&ctl->s_full[1], 1);
     mbar_init(&ctl->pv_done[0], 1);
     mbar_init(&ctl->pv_done[1], 1);
     mbar_init(&ctl->p_full[0], 128);
@@ -305,7 +304,7 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
         b_nx = block_of(n + 2);
       }
       if (s >= kPairs &&
-          !mbar_wait_warp(&ctl->empty[pl][ps], ((s / kPairs) - 1) & 1, a.status, abort_flag))
+          !mbar_wait_warp(&ctl->empty[ps], ((s / kPairs) - 1) & 1, a.status, abort_flag))
         break;
       if (lane == 0) mbar_arrive_expect_tx(&ctl->full[pl][ps], kBlocksPerProducer * kBlockBytes);
       __syncwarp();
@@ -340,9 +339,7 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
           mma_ss(tmem + s_col(n), sdesc_sw128(ka, 16, kBlockBytes), sdesc_sw128(qa, 16, 1024),
                  idesc_qk, k > 0);
         }
-        mma_commit(&ctl->empty[0][sk]);
-        mma_commit(&ctl->empty[1][sk]);
-        mma_commit(&ctl->s_full[n & 1]);
+        mma_commit(&ctl->empty[sk]);                   // K(n) read, S^T(n) ready
         return true;
       };
       bool ok = mbar_wait(&ctl->q_full, 0, a.status, abort_flag) && issue_qk(0);
@@ -367,8 +364,7 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
                    sdesc_sw128(pa, 16, 1024), idesc_pv, (n > 0 || ks > 0));
           }
         }
-        mma_commit(&ctl->empty[0][sv]);
-        mma_commit(&ctl->empty[1][sv]);
+        mma_commit(&ctl->empty[sv]);
         mma_commit(&ctl->pv_done[n & 1]);
         if (n == N - 1) mma_commit(&ctl->o_full);
       }
@@ -390,7 +386,8 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
 #pragma unroll
     for (int h = 0; h < kGroupCols; ++h) l[h] = 0.f;
     for (int n = 0; n < N; ++n) {
-      if (!mbar_wait_warp(&ctl->s_full[n & 1], (n >> 1) & 1, a.status, abort_flag)) break;
+      const int uk = unit_k(n);                        // S^T(n) ready = K(n)'s slot released
+      if (!mbar_wait_warp(&ctl->empty[uk % kPairs], (uk / kPairs) & 1, a.status, abort_flag)) break;
       tc_fence_after();
       uint32_t sv[kN];
       tmem_ld32(tmem + lane_base + s_col(n), sv);
