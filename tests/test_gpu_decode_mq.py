@@ -139,3 +139,26 @@ def test_fixed_form_equals_packed_form():
     o_pk, l_pk, _, _ = _run(packed, 256)
     assert torch.equal(o_fix.reshape(9, 16, 128), o_pk)
     assert torch.equal(l_fix.reshape(9, 16), l_pk)
+
+
+@pytest.mark.slow
+def test_decode_b64_sq4_workload_sampled():
+    """The four-query bench workload at its full size (B=64, SQ=4, causal): the plan and the
+    claim order bit for bit, and the output and LSE of the shortest, the longest and a few
+    random requests against the oracle."""
+    p = W.decode_b64_sq4()
+    out, lse, ws, params = _run(p)
+    _check_plan(p, ws, params)
+    lens = p["seq_lens"].numpy()
+    reqs = {int(np.argmin(lens)), int(np.argmax(lens)), 0, int(lens.size) - 1}
+    reqs |= set(np.random.default_rng(9).integers(0, lens.size, 2).tolist())
+    reqs = sorted(reqs)
+    o_ref, l_ref = A.batch_decode(p["q"], p["kv_indptr"], p["kv_indices"], p["seq_lens"],
+                                  kv_cache=p.get("kv_cache"), k_cache=p.get("k_cache"),
+                                  v_cache=p.get("v_cache"), bmm1_scale=p["sm_scale"],
+                                  bmm2_scale=p["bmm2_scale"], mask_type=p["mask_type"],
+                                  window_left=p["window_left"], seq_len_q=p["seq_len_q"],
+                                  qo_indptr=p["qo_indptr"], rows=reqs)
+    check_out(out[reqs].reshape(-1, out.shape[-2], out.shape[-1]),
+              o_ref[reqs].reshape(-1, o_ref.shape[-2], o_ref.shape[-1]))
+    check_lse(lse[reqs].reshape(-1, lse.shape[-1]), l_ref[reqs].reshape(-1, l_ref.shape[-1]))

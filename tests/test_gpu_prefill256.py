@@ -115,3 +115,21 @@ def test_prefill256_b16_sampled():
     o_ref, l_ref = _oracle(p, rows=rows)
     check_out(out, o_ref, rows=rows)
     check_lse(lse[rows], l_ref[rows])
+
+
+@pytest.mark.slow
+def test_prefill_b16_d256_workload_sampled():
+    """The bench workload at its full size: 40 random rows plus every request's first and last
+    row against the oracle, and the whole plan bit for bit."""
+    p = W.prefill_b16_d256()
+    out, lse, ws, params = _run(p)
+    qo = p["qo_indptr"].numpy()
+    rng = np.random.default_rng(8)
+    rows = set(rng.integers(0, int(qo[-1]), 40).tolist())
+    for b in range(len(qo) - 1):
+        rows |= {int(qo[b]), int(qo[b + 1]) - 1}
+    rows = sorted(rows)
+    o_ref, l_ref = _oracle(p, rows=rows)
+    check_out(out[rows], o_ref[rows])
+    check_lse(lse[rows], l_ref[rows])
+    _check_plan(p, ws, params)

@@ -91,3 +91,14 @@ def test_sage_no_keys_gives_zeros():
                        d["v_scale"], d["q2k_block_index"], None, None, out, ws)
     torch.cuda.synchronize()
     assert torch.all(out.float() == 0)
+
+
+@pytest.mark.slow
+def test_sage_b2h16_workload_sampled():
+    """The bench workload at its full size (B=2, H=16, Sq=Sk=4096, 16 blocks per query block):
+    four (b, h) slices against the oracle, which treats every (b, h) independently."""
+    p = W.sage_b2h16()
+    out = _run(p, uniform_flag=True)
+    for b, h in ((0, 0), (0, 9), (1, 7), (1, 15)):
+        sub = {k: (v[b:b + 1, h:h + 1] if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+        check_out(_flat(out[b:b + 1, h:h + 1]), _flat(_oracle(sub)))
