@@ -9,11 +9,15 @@
  *     a row-strided page table   -> paged_prefill_run
  *   - decode over a CSR-paged cache (one, SQ fixed or packed queries per request) with
  *     split-KV partials and a merge -> paged_decode_run
- * The operations are those of the FlashInfer API pages
- *   [BSA] flashinfer.attention.prims_ts.block_sparse_attention_with_paged_kv_cache
- *   [PRE] flashinfer.attention.prims_ts.batch_prefill_with_paged_kv_cache
- *   [QSA] flashinfer.qsa.qsa_forward
- *   [DEC] flashinfer.attention.prims_ts.prims_ts_batch_decode_with_kv_cache
+ *   - block-sparse attention on prequantized inputs (int8 Q/K, FP8 E4M3 V, fp32 scales)
+ *     -> paged_sage_run
+ * The bitmap form also takes its selection as index rows (PAGED_ATTN_FORM_INDEXED).  The
+ * operations are those of the FlashInfer API pages
+ *   [BSA]  flashinfer.attention.prims_ts.block_sparse_attention_with_paged_kv_cache
+ *   [PRE]  flashinfer.attention.prims_ts.batch_prefill_with_paged_kv_cache
+ *   [QSA]  flashinfer.qsa.qsa_forward
+ *   [DEC]  flashinfer.attention.prims_ts.prims_ts_batch_decode_with_kv_cache
+ *   [SAGE] flashinfer.cute_dsl.sparse.bsa_attn_sm120.bsa_attn_sm120_blk64_sage_fwd
  * cited below by tag and by the section of the page (signature, a named parameter, or the
  * notes).
  *
@@ -24,8 +28,12 @@
  *     device work is enqueued on it; no entry point of the run path synchronises the host
  *     or copies device metadata back to the host, so a planned run can be captured in a
  *     CUDA graph ([BSA] summary; [DEC] notes: "no device-to-host synchronization").
- *   - Element types: Q, K, V and the output are bf16; page tables, lengths and offsets are
- *     int32; kv_valid_bits is uint32; LSE and fp32 outputs are float.
+ *   - Element types: Q, K and V are bf16 (int8 and FP8 E4M3 bytes in the prequantized
+ *     form); outputs are bf16, or fp16 / fp32 where out_dtype selects them (prefill and
+ *     decode); page tables, lengths and offsets are int32; kv_valid_bits is uint32; LSE and
+ *     fp32 outputs are float.
+ *   - Q, K, V and output base pointers must be 16-byte aligned (PAGED_ATTN_ERR_INVALID_ARGUMENT
+ *     otherwise; the FP8 V of the prequantized form needs 4 bytes).
  *   - Return value: PAGED_ATTN_OK or a negative PAGED_ATTN_ERR_* code.  Argument checks
  *     happen on the host before anything is enqueued.  Device-side faults of the contract
  *     that the kernels detect (a wait that timed out, a plan that outgrew its capacity) are
