@@ -38,8 +38,8 @@ constexpr int kQHalf = 128 * 128;              // bytes of a 128-row x 64-col bf
 constexpr int kQBytes = 2 * kQHalf;            // one Q sub-tile
 constexpr int kKvHalf = kKvTile * 128;         // 128 keys x 64 cols
 constexpr int kKvBytes = 2 * kKvHalf;          // one K (or V) tile
-constexpr int kKStages = 3;
-constexpr int kVStages = 2;
+constexpr int kKStages = 2;
+constexpr int kVStages = 3;
 // Register split after set-up (launch: 384 threads x 168): the producer / MMA warpgroup
 // gives registers to the two softmax warpgroups; 2 x 128 x 200 + 128 x 104 = 384 x 168.
 constexpr int kSoftmaxRegs = 200;
