@@ -9,6 +9,27 @@
 
 namespace pa {
 
+// Launch `kernel` with programmatic stream serialization: it may start while the previous
+// kernel of the stream still runs (once every CTA of that kernel has called
+// grid_launch_dependents() or exited), so its launch and prologue overlap that kernel's
+// tail.  The kernel must call grid_dependency_wait() before it reads anything the previous
+// kernels wrote.  After a copy or a memset the launch is an ordinary one.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_after_previous(void (*kernel)(Params...), dim3 grid, dim3 block,
+                                         size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Tile record written by the planner and read by the prefill / block-sparse kernel:
 // b, g, tok0, ntok, kv_begin, kv_end, q_row0, 0.
 struct TileRec {

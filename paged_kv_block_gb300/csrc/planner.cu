@@ -82,6 +82,7 @@ __device__ void block_exclusive_scan_n(const int (&v)[N], int (&ex)[N], int (&to
 // (b * Hkv + g) * tiles_per_bg + r * ceil(qbs / tt) + m.
 __global__ void bsr_tiles_kernel(const int* __restrict__ block_indptr, int B, int Hkv, int Sq,
                                  int qbs, int tt, TileRec* __restrict__ tmp) {
+  grid_launch_dependents();   // the tile sort may launch now; it waits for these records
   const int nqb = (Sq + qbs - 1) / qbs;
   const int row = blockIdx.x * blockDim.x + threadIdx.x;
   if (row >= B * Hkv * nqb) return;
@@ -111,6 +112,7 @@ __global__ void bsr_tiles_kernel(const int* __restrict__ block_indptr, int B, in
 __global__ void prefill_count_kernel(const int* __restrict__ qo, int q_len, int B, int Hkv,
                                      int tt, int capacity, int* __restrict__ off, int* n_tiles,
                                      uint32_t* status) {
+  grid_launch_dependents();
   __shared__ int warp_sums[32];
   int carry = 0;
   for (int base = 0; base < B; base += blockDim.x) {
@@ -140,6 +142,8 @@ __global__ void prefill_fill_kernel(const int* __restrict__ qo, int q_len,
                                     const int* __restrict__ lens, int Hkv, int tt, int causal,
                                     int window_left, int capacity, const int* __restrict__ off,
                                     TileRec* __restrict__ tmp) {
+  grid_launch_dependents();
+  grid_dependency_wait();     // the tile offsets of the count kernel
   const int b = blockIdx.x;
   const int nq = qo ? qo[b + 1] - qo[b] : q_len;
   const int row0 = qo ? qo[b] : b * q_len;
@@ -180,6 +184,8 @@ __device__ __forceinline__ int rec_cost(const TileRec& r, int maxc) {
 
 __global__ void sort_hist_kernel(const TileRec* __restrict__ in, const int* n_dev, int n_static,
                                  int maxc, int* __restrict__ hist) {
+  grid_launch_dependents();
+  grid_dependency_wait();     // the records and their count
   extern __shared__ int h[];
   const int n = n_dev ? *n_dev : n_static;
   for (int k = threadIdx.x; k <= maxc; k += blockDim.x) h[k] = 0;
@@ -193,6 +199,8 @@ __global__ void sort_hist_kernel(const TileRec* __restrict__ in, const int* n_de
 
 __global__ void sort_offsets_kernel(int nchunks, int maxc, const int* __restrict__ hist,
                                     int* __restrict__ offs) {
+  grid_launch_dependents();
+  grid_dependency_wait();     // the histograms
   extern __shared__ int tot[];
   __shared__ int warp_sums[32];
   const long long W = maxc + 1;
@@ -224,6 +232,8 @@ __global__ void sort_offsets_kernel(int nchunks, int maxc, const int* __restrict
 __global__ void sort_scatter_kernel(const TileRec* __restrict__ in, TileRec* __restrict__ out,
                                     const int* n_dev, int n_static, int maxc,
                                     const int* __restrict__ offs) {
+  grid_launch_dependents();   // the attention kernel may start its prologue
+  grid_dependency_wait();     // the offsets (and, through the chain, the records)
   extern __shared__ int cnt[];
   const int n = n_dev ? *n_dev : n_static;
   for (int k = threadIdx.x; k <= maxc; k += blockDim.x) cnt[k] = 0;
@@ -510,8 +520,9 @@ void launch_prefill_tiles(const int* qo_indptr, int q_len, const int* seq_lens, 
                                            tile_offsets, n_tiles, status);
   count_launches(1);
   if (B > 0) {
-    prefill_fill_kernel<<<B, 256, 0, st>>>(qo_indptr, q_len, seq_lens, Hkv, tile_tokens, causal,
-                                           window_left, capacity, tile_offsets, tmp);
+    launch_after_previous(prefill_fill_kernel, dim3(B), dim3(256), 0, st, qo_indptr, q_len,
+                          seq_lens, Hkv, tile_tokens, causal, window_left, capacity,
+                          static_cast<const int*>(tile_offsets), tmp);
     count_launches(1);
   }
 }
@@ -526,10 +537,12 @@ void launch_tile_sort(const TileRec* in, TileRec* out, const int* n_dev, int n_s
   if (capacity <= 0) return;
   const int nchunks = ceil_div(capacity, kSortChunk);
   const size_t sm = static_cast<size_t>(max_cost + 1) * sizeof(int);
-  sort_hist_kernel<<<nchunks, kSortChunk, sm, st>>>(in, n_dev, n_static, max_cost, hist);
-  sort_offsets_kernel<<<1, 1024, sm, st>>>(nchunks, max_cost, hist, offs);
-  sort_scatter_kernel<<<nchunks, kSortChunk, sm, st>>>(in, out, n_dev, n_static, max_cost,
-                                                       offs);
+  launch_after_previous(sort_hist_kernel, dim3(nchunks), dim3(kSortChunk), sm, st, in, n_dev,
+                        n_static, max_cost, hist);
+  launch_after_previous(sort_offsets_kernel, dim3(1), dim3(1024), sm, st, nchunks, max_cost,
+                        static_cast<const int*>(hist), offs);
+  launch_after_previous(sort_scatter_kernel, dim3(nchunks), dim3(kSortChunk), sm, st, in, out,
+                        n_dev, n_static, max_cost, static_cast<const int*>(offs));
   count_launches(3);
 }
 

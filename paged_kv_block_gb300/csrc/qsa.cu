@@ -198,7 +198,8 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
   uint8_t* p_s = q_s + kQBytes;
   QsaCtrl* ctl = reinterpret_cast<QsaCtrl*>(p_s + kPBufs * kPBytes);
 
-  if (launch_aborted(a.status)) return;
+  // one decision for the whole CTA: another CTA may set the status word meanwhile
+  if (__syncthreads_or(launch_aborted(a.status))) return;
   const int t = blockIdx.x / a.pairs, g0 = 2 * (blockIdx.x % a.pairs);
   const bool two = g0 + 1 < a.Hkv;
   const int G = a.G;
