@@ -421,6 +421,20 @@ def barrier(dist_on):
         torch.distributed.barrier()
 
 
+def max_over_ranks(x, dist_on, device):
+    """The largest x over all ranks: the job's time is its slowest rank's."""
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    if dist_on:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, world, ms_step, scale):
+    """Whole-job throughput: the units every rank processed in a step (each rank runs the same
+    workload) over the slowest rank's step time."""
+    return units_per_rank * world / (ms_step * 1e-3) / scale
+
+
 def time_steps(r, steps, warmup, dist_on):
     """(region ms, main-kernel ms per launch, kernel launches of this library in the region).
 
@@ -593,10 +607,7 @@ def main():
     rc, raw = r.status()
     if rc != pkb.OK:
         raise RuntimeError(f"device status {raw:#x}")
-    t = torch.tensor([region_ms], dtype=torch.float64, device=dev)
-    if dist_on:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    region_ms = float(t.item())
+    region_ms = max_over_ranks(region_ms, dist_on, dev)
     ms_step = region_ms / args.steps
 
     if p["form"] == "decode":
@@ -613,7 +624,7 @@ def main():
         if p["form"] == "prefill" and p["q"].shape[-1] == 256:
             kernel = "attn256_kernel"
         bound, peak = "tensor", pk["bf16_tflops"]
-    value = units * world / (ms_step * 1e-3) / scale
+    value = job_rate(units, world, ms_step, scale)
     achieved = units / (kernel_ms * 1e-3) / scale
     traffic = recorded_traffic(kernel, args.workload)
     e2e_ms, h2d, d2h = time_e2e(r, max(3, min(args.steps, 10)))
@@ -629,7 +640,7 @@ def main():
                          "unit": unit, "frac": achieved / peak, "traffic": traffic,
                          "kernel": kernel, "kernel_ms": kernel_ms,
                          "peak_source": f"{pk_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})"},
-            "e2e": {"value": units * world / (e2e_ms * 1e-3) / scale, "unit": unit,
+            "e2e": {"value": job_rate(units, world, e2e_ms, scale), "unit": unit,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
             "gpu_launches": launches,
