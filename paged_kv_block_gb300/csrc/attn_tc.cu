@@ -10,9 +10,10 @@
 // every K/V tile.  Roles (384 threads):
 //   warps 0-3  softmax + epilogue of sub-tile 0 (thread t <-> TMEM lane t <-> row t)
 //   warps 4-7  softmax + epilogue of sub-tile 1
-//   warp  8    TMA producer of Q (once per tile) and K (3-stage ring)
+//   warp  8    TMA producer of Q (once per tile) and K (2-stage ring)
 //   warp  9    TMEM owner and MMA issuer (one thread): S_w = Q_w K^T and O_w += P_w V
-//   warp 10    TMA producer of V (2-stage ring)
+//   warp 10    TMA producer of V (3-stage ring: a V stage is free only after PV of both
+//              sub-tiles, later than a K stage after QK, so V gets the deeper ring)
 //   warp 11    column facts of each KV tile (first key of each sub-chunk, live-key mask, key
 //              range), a few tiles ahead into a small ring, so that the softmax reads them
 //              from shared memory instead of issuing block-id and valid-bit loads
