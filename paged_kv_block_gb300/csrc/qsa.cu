@@ -17,10 +17,11 @@
 //   O^T [256 d x 32]   += V_tile^T [256 x 128] * P^T      (two M = 128 halves of d)
 // A tile is K then V, each 64 KB laid out [16 blocks][4 chunks][8 rows][128 B], so the MMAs
 // see 16 blocks at a 4 KB stride.  The copies run as two independent pipelines, one per half
-// of the blocks (0-7 and 8-15), each with its own barriers: the copy rate of one pipeline
-// (one chain of stage barriers) saturates well below the SM's, and two pipelines nearly
-// double it.  The two pipelines' 32 KB slots interleave into three 64 KB pair slots.  Units
-// are copied in the order the MMAs consume them, K(0), K(1), V(0), K(2), V(1), ..., V(N - 1):
+// of the blocks (0-7 and 8-15), each with its own full barriers: the copy rate of one
+// pipeline (one chain of stage barriers) saturates well below the SM's, and two pipelines
+// nearly double it.  A slot is released to both pipelines by one barrier.  The two
+// pipelines' 32 KB slots interleave into three 64 KB pair slots.  Units are copied in the
+// order the MMAs consume them, K(0), K(1), V(0), K(2), V(1), ..., V(N - 1):
 // S^T(n + 1) is computed before PV(n), so K(n + 1) can be in flight two tiles ahead and the
 // softmax of one tile follows the previous one without waiting for a copy.
 // Roles (288 threads):
