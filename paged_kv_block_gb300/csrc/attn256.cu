@@ -520,28 +520,17 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   }
 }
 
-int g_num_sms = 0;
-
 }  // namespace
 
 // Prefill tiles of D = 256 (one 128-row sub-tile each; the planner's tile_tokens is 128 / G).
 int launch_attn256(const AttnLaunch& a, cudaStream_t st) {
   if (a.D != kD || a.G < 1 || a.G > kRows) return -2;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attn256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-      return -1;
-    attr_set = true;
-  }
-  if (g_num_sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return -1;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  if (!kernel_smem_ready(attn256_kernel, kSmemBytes, smem_set)) return -1;
+  const int sms = current_sm_count();
+  if (sms <= 0) return -1;
   if (a.capacity <= 0) return 0;
-  const int grid = a.capacity < g_num_sms ? a.capacity : g_num_sms;
+  const int grid = a.capacity < sms ? a.capacity : sms;
   attn256_kernel<<<grid, kThreads, kSmemBytes, st>>>(a.qmap, a.kmap, a.vmap, a);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;

@@ -815,25 +815,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   }
 }
 
-int g_num_sms = 0;
-
 template <int CK, bool FACTS, bool SCALED = false>
 int launch_ck(const AttnLaunch& a, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_tc_kernel<CK, FACTS, SCALED>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-      return -1;
-    attr_set = true;
-  }
-  if (g_num_sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return -1;
-  }
-  const int grid = a.capacity < g_num_sms ? a.capacity : g_num_sms;
+  static std::atomic<uint64_t> smem_set{0};
+  if (!kernel_smem_ready(attn_tc_kernel<CK, FACTS, SCALED>, kSmemBytes, smem_set)) return -1;
+  const int sms = current_sm_count();
+  if (sms <= 0) return -1;
+  const int grid = a.capacity < sms ? a.capacity : sms;
   // Dense tiles: programmatic, so the prologue overlaps the planner's last kernel (one
   // GB300: dense prefill step 0.483 -> 0.455 ms).  Block-sparse tiles: an ordinary launch;
   // programmatic, the long block-sparse step got 3.6% slower.

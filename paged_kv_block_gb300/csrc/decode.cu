@@ -636,28 +636,17 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 }
 
-int g_num_sms = 0;
-
 template <int NRB, bool ROWMASK>
 int launch_decode_t(const DecodeLaunch& a, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(decode_split_kernel<NRB, ROWMASK>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_bytes(kMaxRows)) != cudaSuccess)
-      return -1;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  if (!kernel_smem_ready(decode_split_kernel<NRB, ROWMASK>, smem_bytes(kMaxRows), smem_set))
+    return -1;
   const int smem = smem_bytes(a.rows);
   const int per_sm = 2 * (smem + 1024) <= 228 * 1024 ? 2 : 1;
-  if (g_num_sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return -1;
-  }
+  const int sms = current_sm_count();
+  if (sms <= 0) return -1;
   if (a.capacity > 0) {
-    const int grid = a.capacity < per_sm * g_num_sms ? a.capacity : per_sm * g_num_sms;
+    const int grid = a.capacity < per_sm * sms ? a.capacity : per_sm * sms;
     void* tok;
     timer_begin(st, &tok);
     // programmatic dependent launch: the CTAs start their prologue while the planner runs

@@ -1,6 +1,7 @@
 // Declarations shared by the translation units of libpagedattn (not part of the ABI).
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -28,6 +29,34 @@ inline cudaError_t launch_after_previous(void (*kernel)(Params...), dim3 grid, d
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// A kernel's dynamic shared memory limit is set per device, so it is set once on every device
+// the library launches it on: `done` holds one bit per device index below 64 (devices past
+// that are set on every launch).
+template <typename Kernel>
+inline bool kernel_smem_ready(Kernel* kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return false;
+  if (bit != 0) done.fetch_or(bit, std::memory_order_acq_rel);
+  return true;
+}
+
+// SM count of the current device, looked up once per device index below 64; 0 on failure.
+inline int current_sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const bool cacheable = dev >= 0 && dev < 64;
+  if (cacheable && (n = cached[dev].load(std::memory_order_relaxed)) > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (cacheable) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 // Tile record written by the planner and read by the prefill / block-sparse kernel:

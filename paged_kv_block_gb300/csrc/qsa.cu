@@ -508,13 +508,8 @@ int launch_qsa(const paged_attn_params* p, const paged_attn_meta* m, const void*
       !encode_block_pair_map(&kmap, k, p->q_len, p->num_kv_heads, kD) ||
       !encode_block_pair_map(&vmap, v, p->q_len, p->num_kv_heads, kD))
     return PAGED_ATTN_ERR_CUDA;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(qsa_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-      return PAGED_ATTN_ERR_CUDA;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  if (!kernel_smem_ready(qsa_kernel, kSmemBytes, smem_set)) return PAGED_ATTN_ERR_CUDA;
   QsaLaunch a{};
   a.out = static_cast<__nv_bfloat16*>(out);
   a.out32 = out_fp32;
