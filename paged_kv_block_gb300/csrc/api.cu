@@ -965,8 +965,17 @@ int paged_sage_run(const paged_sage_params* p, const int8_t* q_int8, const int8_
                    const float* v_scale, const int32_t* idx, const int32_t* nums,
                    const int32_t* block_sizes, void* out, void* ws, size_t ws_bytes,
                    void* stream) {
-  if (!sage_params_ok(p) || !out) return PAGED_ATTN_ERR_INVALID_ARGUMENT;
+  if (!sage_params_ok(p) || !out || !aligned16(out)) return PAGED_ATTN_ERR_INVALID_ARGUMENT;
   const SageLayout g = sage_layout(p);
+  // every argument is checked before anything is enqueued; the inputs only matter when there
+  // are rows and keys
+  if (g.BH > 0 && p->q_len > 0 && g.NB > 0) {
+    if (!q_int8 || !k_int8 || !v_fp8 || !q_scale || !k_scale || !v_scale ||
+        (p->capacity > 0 && !idx) || (p->block_sizes_rank > 0 && !block_sizes))
+      return PAGED_ATTN_ERR_INVALID_ARGUMENT;
+    if (!aligned16(q_int8) || !aligned16(k_int8) || (reinterpret_cast<uintptr_t>(v_fp8) & 3u))
+      return PAGED_ATTN_ERR_INVALID_ARGUMENT;
+  }
   if (!ws || ws_bytes < g.total) return PAGED_ATTN_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* status = at<uint32_t>(ws, g.s.status);
@@ -978,12 +987,6 @@ int paged_sage_run(const paged_sage_params* p, const int8_t* q_int8, const int8_
                ? PAGED_ATTN_OK
                : PAGED_ATTN_ERR_CUDA;
   }
-  if (!q_int8 || !k_int8 || !v_fp8 || !q_scale || !k_scale || !v_scale || (p->capacity > 0 && !idx) ||
-      (p->block_sizes_rank > 0 && !block_sizes))
-    return PAGED_ATTN_ERR_INVALID_ARGUMENT;
-  if (!aligned16(q_int8) || !aligned16(k_int8) || (reinterpret_cast<uintptr_t>(v_fp8) & 3u) ||
-      !aligned16(out))
-    return PAGED_ATTN_ERR_INVALID_ARGUMENT;
   SagePrepare sp{};
   sp.q_int8 = q_int8;
   sp.k_int8 = k_int8;
