@@ -14,7 +14,7 @@ Sources (FlashInfer API pages):
   [DEC]  flashinfer.attention.prims_ts.prims_ts_batch_decode_with_kv_cache
   [SAGE] flashinfer.cute_dsl.sparse.bsa_attn_sm120.bsa_attn_sm120_blk64_sage_fwd
 
-Readings where the pages are silent (each also listed in the design notes):
+Readings where the pages are silent:
   * query position: query i of a request with len_q queries and len_kv keys sits at
     p(i) = len_kv - len_q + i (bottom-right aligned);
   * GQA: query head h reads KV head h // (Hq / Hkv);

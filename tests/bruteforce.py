@@ -245,39 +245,47 @@ def e4m3_value(code):
     return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
 
 
+def _sage_block_size(prob, b, h, c):
+    bs = prob["block_sizes"]
+    if bs is None:
+        return 64
+    if bs.dim() == 1:
+        return int(bs[c])
+    if bs.dim() == 2:
+        return int(bs[b, c])
+    return int(bs[b, h, c])
+
+
+def sage_visible(prob, b, h, i):
+    """Visible keys of query i of (b, h) in the prequantized form: walk every key and keep
+    those whose 64-key block is among the row's first n listed ids and whose offset inside
+    the block is below the block's size."""
+    Sk = prob["k_int8"].shape[2]
+    r = i // 64
+    n = (int(prob["q2k_block_nums"][b, h, r]) if prob["q2k_block_nums"] is not None
+         else int(prob["block_sparse_num"]))
+    listed = [int(c) for c in prob["q2k_block_index"][b, h, r, :n]]
+    out = []
+    for j in range(Sk):
+        c = j // 64
+        if c in listed and j - 64 * c < _sage_block_size(prob, b, h, c):
+            out.append(j)
+    return out
+
+
 def sage_bruteforce(prob):
     """Dequantized block-sparse attention by plain loops (bit-level FP8 decoding)."""
     qi, ki, vh = prob["q_int8"], prob["k_int8"], prob["v_fp8"]
     B, H, Sq, D = qi.shape
-    Sk = ki.shape[2]
-    NB = -(-Sk // 64)
-    bs = prob["block_sizes"]
-
-    def bsize(b, h, c):
-        if bs is None:
-            return 64
-        if bs.dim() == 1:
-            return int(bs[c])
-        if bs.dim() == 2:
-            return int(bs[b, c])
-        return int(bs[b, h, c])
-
     O = np.zeros((B, H, Sq, D))
     for b in range(B):
         for h in range(H):
             for i in range(Sq):
-                r = i // 64
-                n = (int(prob["q2k_block_nums"][b, h, r]) if prob["q2k_block_nums"] is not None
-                     else int(prob["block_sparse_num"]))
-                listed = [int(c) for c in prob["q2k_block_index"][b, h, r, :n]]
                 qs = float(prob["q_scale"][b, h, i // 32])
                 q = [int(x) * qs for x in qi[b, h, i]]
                 keys, vals = [], []
-                for j in range(Sk):
-                    c = j // 64
-                    if c not in listed or j - 64 * c >= bsize(b, h, c):
-                        continue
-                    ks = float(prob["k_scale"][b, h, c])
+                for j in sage_visible(prob, b, h, i):
+                    ks = float(prob["k_scale"][b, h, j // 64])
                     keys.append([int(x) * ks for x in ki[b, h, j]])
                     vals.append([e4m3_value(vh[b, h, d, j]) * float(prob["v_scale"][b, h, d])
                                  for d in range(D)])
