@@ -323,13 +323,21 @@ int paged_sage_run(const paged_sage_params* params, const int8_t* q_int8_dev,
  *     current at the call); make that first call before any stream capture.
  *   - Every call on a device uses the same array, so calls whose work may overlap on the
  *     GPU (other streams, other threads) race and must be serialised by the caller.
- *   - The device status word lives inside the array and is not readable by the caller. */
+ *   - The device status word (timeouts, page ids outside the pool, broken query offsets)
+ *     lives inside the array; read it with paged_decode_static_status. */
 #define PAGED_DECODE_STATIC_SCRATCH_BYTES (32u << 20)
 int paged_decode_run_static(const paged_decode_params* params, const void* query_dev,
                             const void* k_dev, const void* v_dev, const int32_t* kv_indptr_dev,
                             const int32_t* kv_indices_dev, const int32_t* seq_lens_dev,
                             const int32_t* qo_indptr_dev, void* out_dev, float* lse_dev,
                             void* stream);
+
+/* Status of the last paged_decode_run_static call on the current device: synchronises
+ * `stream` (the one that call used), reads the status word from the fixed array and maps it
+ * like paged_attn_workspace_status (PAGED_ATTN_OK, _ERR_TIMEOUT, _ERR_CAPACITY or
+ * _ERR_METADATA; the raw word to *raw_word when non-NULL).  Allocates nothing.  A call of
+ * paged_decode_run_static on this device that is enqueued in between overwrites the word. */
+int paged_decode_static_status(void* stream, uint32_t* raw_word);
 
 /* ---- plan inspection -------------------------------------------------------------------- */
 
@@ -373,6 +381,16 @@ int paged_attn_kernel_timer(int enable);
 /* Sum of the bracketed kernel times in milliseconds and the number of bracketed launches
  * since the timer was last enabled; waits for the recorded events. */
 int paged_attn_kernel_timer_read(double* total_ms, int64_t* launches);
+
+/* L2 read rate probe.  Enqueues on `stream` one kernel that reads the `bytes` bytes at
+ * buf_dev (16-byte aligned, a multiple of 16) `reps` times with 16-byte loads that bypass L1,
+ * spread over every SM; a buffer well inside L2 then measures the rate at which the SMs read
+ * L2, the second roofline of the bitmap form (its K/V rows are gathered from L2 once per
+ * selecting query).  Time it with events on the same stream: bytes * reps / time.  sink_dev
+ * (4 bytes) is written at most once, so that the loads are not optimised away.  Not part of
+ * the attention path ([QSA] names no such call). */
+int paged_attn_l2_read_probe(const void* buf_dev, size_t bytes, int reps, uint32_t* sink_dev,
+                             void* stream);
 
 /* Number of kernels this library has enqueued since it was loaded. */
 int64_t paged_attn_launch_count(void);

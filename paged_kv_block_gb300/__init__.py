@@ -110,6 +110,7 @@ _EXPORTS = {
     "paged_prefill_plan_layout_of": (C.c_int, [C.POINTER(PrefillParams), C.POINTER(PlanLayout)]),
     "paged_decode_plan_layout_of": (C.c_int, [C.POINTER(DecodeParams), C.POINTER(PlanLayout)]),
     "paged_decode_run_static": (C.c_int, [C.POINTER(DecodeParams)] + [C.c_void_p] * 10),
+    "paged_decode_static_status": (C.c_int, [C.c_void_p, C.POINTER(C.c_uint32)]),
     "paged_attn_workspace_status": (C.c_int, [C.c_void_p, C.c_void_p, C.POINTER(C.c_uint32)]),
     "paged_sage_workspace_size": (C.c_size_t, [C.POINTER(SageParams)]),
     "paged_sage_run": (C.c_int, [C.POINTER(SageParams)] + [C.c_void_p] * 11
@@ -118,6 +119,8 @@ _EXPORTS = {
     "paged_attn_kernel_timer": (C.c_int, [C.c_int]),
     "paged_attn_kernel_timer_read": (C.c_int, [C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
     "paged_attn_launch_count": (C.c_int64, []),
+    "paged_attn_l2_read_probe": (C.c_int, [C.c_void_p, C.c_size_t, C.c_int, C.c_void_p,
+                                           C.c_void_p]),
 }
 
 
@@ -271,6 +274,14 @@ def paged_decode_run_static(params: DecodeParams, query, k, v, kv_indptr, kv_ind
            "paged_decode_run_static")
 
 
+def paged_decode_static_status(stream=None):
+    """(status code, raw word) of the last paged_decode_run_static call on the current
+    device; synchronises the stream."""
+    raw = C.c_uint32(0)
+    rc = lib().paged_decode_static_status(_stream(stream), C.byref(raw))
+    return rc, raw.value
+
+
 def paged_attn_workspace_status(workspace, stream=None):
     """(status code, raw word) of the device status word; synchronises the stream."""
     raw = C.c_uint32(0)
@@ -289,6 +300,13 @@ def paged_attn_kernel_timer_read():
     _check(lib().paged_attn_kernel_timer_read(C.byref(ms), C.byref(n)),
            "paged_attn_kernel_timer_read")
     return ms.value, n.value
+
+
+def paged_attn_l2_read_probe(buf, reps, sink, stream=None) -> None:
+    """Enqueue the L2 read-rate probe over the bytes of `buf` (a device tensor)."""
+    _check(lib().paged_attn_l2_read_probe(_dev(buf, "buf"), buf.numel() * buf.element_size(),
+                                          int(reps), _dev(sink, "sink"), _stream(stream)),
+           "paged_attn_l2_read_probe")
 
 
 def paged_attn_launch_count() -> int:

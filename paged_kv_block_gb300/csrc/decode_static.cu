@@ -20,6 +20,23 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
+// Device address of the array on the current device, looked up on first use (host code
+// cannot use the symbol itself as an address).  Returns a status code.
+int scratch_of_current_device(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return PAGED_ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
+      return PAGED_ATTN_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return PAGED_ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" int paged_decode_run_static(const paged_decode_params* params, const void* query,
@@ -30,24 +47,20 @@ extern "C" int paged_decode_run_static(const paged_decode_params* params, const 
   const size_t need = paged_decode_workspace_size(params);
   if (need == 0) return PAGED_ATTN_ERR_INVALID_ARGUMENT;
   if (need > kScratchBytes) return PAGED_ATTN_ERR_WORKSPACE;   // over the fixed maximum
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return PAGED_ATTN_ERR_CUDA;
   void* scratch = nullptr;
-  {
-    // First call on this device: look up the array's device address (host code cannot use
-    // the symbol itself as an address).
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[dev]) {
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
-        return PAGED_ATTN_ERR_CUDA;
-      g_scratch_ptr[dev] = p;
-    }
-    scratch = g_scratch_ptr[dev];
-  }
+  const int rc = scratch_of_current_device(&scratch);
+  if (rc != PAGED_ATTN_OK) return rc;
   // The regular decode path clears the status word itself and overwrites every other part
   // of the scratch it reads, so stale contents from an earlier call do not leak in.
   return paged_decode_run(params, query, k, v, kv_indptr, kv_indices, seq_lens, qo_indptr, out,
                           lse, scratch, kScratchBytes, stream);
+}
+
+// The status word opens every decode scratch layout (byte offset 0), so the word of the last
+// paged_decode_run_static call on this device sits at the start of the array.
+extern "C" int paged_decode_static_status(void* stream, uint32_t* raw_word) {
+  void* scratch = nullptr;
+  const int rc = scratch_of_current_device(&scratch);
+  if (rc != PAGED_ATTN_OK) return rc;
+  return paged_attn_workspace_status(scratch, stream, raw_word);
 }
