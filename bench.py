@@ -541,6 +541,211 @@ def cpu_baseline_decode(p, budget_s=12.0):
 
 
 # ----------------------------------------------------------------------------------------
+# Oracle samples of the other workloads: seeded slices that are problems of their own, so
+# that their work is counted exactly by the same counters as the full workload.
+# ----------------------------------------------------------------------------------------
+
+def bsr_qblock_slice(p, r0, r1):
+    """Query blocks [r0, r1) of a block-sparse problem as a problem of its own.  The sampled
+    queries keep their positions: the KV length of each request is cut to the key after the
+    last sampled query's position (later keys are causally invisible to them), so the
+    bottom-right alignment p = L - Sq + i still places query i of the slice at its original
+    position."""
+    qbs = p["q_block_size"]
+    B, Sq = p["q"].shape[:2]
+    bptr = p["block_indptr"].numpy().astype(np.int64)
+    bidx = p["block_indices"].numpy().astype(np.int64)
+    Hkv = bptr.shape[1]
+    n = r1 - r0
+    i0, i1 = r0 * qbs, min(r1 * qbs, Sq)
+    lens = p["seq_lens_kv"].numpy().astype(np.int64)
+    new_lens = np.maximum(lens - Sq + i1, 0) if p["mask_type"] == "causal" else lens
+    ptr = np.zeros((B, Hkv, n + 1), dtype=np.int64)
+    rows, off = [], 0
+    for b in range(B):
+        for g in range(Hkv):
+            for k, r in enumerate(range(r0, r1)):
+                ptr[b, g, k] = off
+                rows.append(bidx[bptr[b, g, r]:bptr[b, g, r + 1]])
+                off += rows[-1].size
+            ptr[b, g, n] = off
+    return dict(p, q=p["q"][:, i0:i1].contiguous(),
+                block_indptr=torch.from_numpy(ptr.astype(np.int32)),
+                block_indices=torch.from_numpy(np.concatenate(rows).astype(np.int32)),
+                seq_lens_kv=torch.from_numpy(new_lens.astype(np.int32)),
+                max_seq_len_kv=int(new_lens.max()))
+
+
+def prefill_subbatch(p, reqs):
+    """Requests `reqs` of a packed prefill problem with their pages copied to compact pools."""
+    qo = p["qo_indptr"].numpy().astype(np.int64)
+    tables = p["block_tables"].numpy()[list(reqs)]
+    pages, inv = np.unique(tables, return_inverse=True)
+    rows = np.concatenate([np.arange(qo[b], qo[b + 1]) for b in reqs])
+    nq = [int(qo[b + 1] - qo[b]) for b in reqs]
+    pg = torch.from_numpy(pages).long()
+    return dict(p, q=p["q"][torch.from_numpy(rows)], k_cache=p["k_cache"][pg],
+                v_cache=p["v_cache"][pg],
+                qo_indptr=torch.tensor(np.concatenate([[0], np.cumsum(nq)]), dtype=torch.int32),
+                block_tables=torch.from_numpy(inv.reshape(tables.shape).astype(np.int32)),
+                seq_lens_kv=p["seq_lens_kv"][list(reqs)], num_pages=int(pages.size))
+
+
+def qsa_last_sequence(p):
+    """The last packed sequence of a bitmap (or indexed) problem, re-based to start at token 0
+    and block 0 (sequences never share blocks or keys)."""
+    tb = p["tok_base"].numpy() if "tok_base" in p else None
+    lo = p["lo"].numpy().astype(np.int64)
+    t0 = int(lo[-1])
+    bs = p["block_size"]
+    b0 = t0 // bs
+    sub = dict(p, q=p["q"][t0:], k=p["k"][t0:], v=p["v"][t0:],
+               lo=torch.from_numpy((lo[t0:] - t0).astype(np.int32)),
+               hi=torch.from_numpy((p["hi"].numpy()[t0:].astype(np.int64) - t0).astype(np.int32)),
+               block_first=p["block_first"][b0:] - t0, block_last=p["block_last"][b0:] - t0)
+    if tb is not None:
+        sub["tok_base"] = torch.from_numpy((tb[t0:] - t0).astype(np.int32))
+        sub["blk_base"] = torch.from_numpy((p["blk_base"].numpy()[t0:] - b0).astype(np.int32))
+    if "sel_blocks" in p:
+        sub["sel_blocks"] = p["sel_blocks"][t0:, b0:].contiguous()
+    else:
+        idx = p["sel_indices"].numpy()[t0:].astype(np.int64)
+        sub["sel_indices"] = torch.from_numpy(np.where(idx >= 0, idx - b0, idx).astype(np.int32))
+    return sub
+
+
+def qsa_rows(p, rows):
+    """The query rows `rows` of a bitmap or indexed problem, for counting their pairs."""
+    r = torch.as_tensor(rows, dtype=torch.long)
+    sub = dict(p, q=p["q"][r], lo=p["lo"][r], hi=p["hi"][r])
+    key = "sel_blocks" if "sel_blocks" in p else "sel_indices"
+    sub[key] = p[key][r]
+    return sub
+
+
+def oracle_sample_rate(name, p):
+    """Time the float64 oracle (as it stands) on a seeded slice of workload `p`; returns the
+    cpu_baseline record in the workload's unit."""
+    from oracle import attention as A
+    rng = np.random.default_rng(77)
+    cores = os.cpu_count()
+    form = p["form"]
+    if form == "decode":
+        B = p["q"].shape[0]
+        reqs = sorted(rng.choice(B, size=8, replace=False).tolist())
+        sub = decode_subbatch(p, reqs)
+        secs = oracle_decode_seconds(sub)
+        nb = decode_kv_bytes(sub)
+        return {"value": nb / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                "seconds": secs, "sample": f"requests {reqs} of {B} ({nb / 1e9:.3f} GB K/V)"}
+    t0 = time.perf_counter()
+    if form == "bsr":
+        Sq, qbs = p["q"].shape[1], p["q_block_size"]
+        nqb = -(-Sq // qbs)
+        if nqb <= 4:
+            sub, what = p, "the whole workload"
+        else:
+            r1 = int(rng.integers(nqb // 2, nqb + 1))
+            sub, what = bsr_qblock_slice(p, r1 - 4, r1), f"query blocks {r1 - 4}..{r1 - 1} of {nqb}"
+        t0 = time.perf_counter()
+        A.block_sparse_attention(
+            sub["q"], sub["kv_indptr"], sub["kv_indices"], sub["block_indptr"],
+            sub["block_indices"], sub["q_block_size"], sub["kv_block_size"], sub["seq_lens_kv"],
+            kv_cache=sub.get("kv_cache"), k_cache=sub.get("k_cache"), v_cache=sub.get("v_cache"),
+            kv_valid_bits=sub.get("kv_valid_bits"), mask_type=sub["mask_type"],
+            sm_scale=sub["sm_scale"])
+        pairs, D = bsr_pairs(sub), sub["q"].shape[-1]
+    elif form == "prefill":
+        B = p["seq_lens_kv"].numel()
+        reqs = sorted(rng.choice(B, size=2, replace=False).tolist())
+        sub, what = prefill_subbatch(p, reqs), f"requests {reqs} of {B}"
+        t0 = time.perf_counter()
+        A.batch_prefill(sub["q"], sub["k_cache"], sub["v_cache"], sub["qo_indptr"],
+                        sub["block_tables"], sub["seq_lens_kv"], mask_type=sub["mask_type"],
+                        window_left=sub["window_left"], sm_scale=sub["sm_scale"],
+                        output_scale=sub["output_scale"])
+        pairs, D = prefill_pairs(sub), sub["q"].shape[-1]
+    elif form in ("qsa", "qsa_indexed"):
+        seq = qsa_last_sequence(p)
+        T = seq["q"].shape[0]
+        rows = sorted(rng.choice(T, size=min(T, 384), replace=False).tolist())
+        what = f"{len(rows)} random tokens of the last packed sequence ({T} tokens)"
+        t0 = time.perf_counter()
+        if form == "qsa":
+            A.qsa_forward(seq["q"], seq["k"], seq["v"], seq["sel_blocks"], seq["lo"], seq["hi"],
+                          seq["blk_base"], seq["tok_base"], seq["block_first"],
+                          seq["block_last"], seq["scale"], seq["block_size"], rows=rows)
+            pairs = qsa_pairs(qsa_rows(seq, rows))
+        else:
+            A.qsa_indexed_forward(seq["q"], seq["k"], seq["v"], seq["sel_indices"], seq["lo"],
+                                  seq["hi"], seq["block_first"], seq["block_last"],
+                                  seq["scale"], seq["block_size"], rows=rows)
+            pairs = qsa_indexed_pairs(qsa_rows(seq, rows))
+        D = seq["q"].shape[-1]
+    elif form == "sage":
+        B, H = p["q_int8"].shape[:2]
+        b, h = int(rng.integers(0, B)), int(rng.integers(0, H))
+        sl = lambda t: None if t is None else t[b:b + 1, h:h + 1]  # noqa: E731
+        sub = dict(p, q_int8=sl(p["q_int8"]), k_int8=sl(p["k_int8"]), v_fp8=sl(p["v_fp8"]),
+                   q_scale=sl(p["q_scale"]), k_scale=sl(p["k_scale"]), v_scale=sl(p["v_scale"]),
+                   q2k_block_index=sl(p["q2k_block_index"]),
+                   q2k_block_nums=sl(p["q2k_block_nums"]))
+        if p["block_sizes"] is not None and p["block_sizes"].dim() > 1:
+            sub["block_sizes"] = (p["block_sizes"][b:b + 1] if p["block_sizes"].dim() == 2
+                                  else sl(p["block_sizes"]))
+        what = f"(b, h) = ({b}, {h}) of ({B}, {H})"
+        t0 = time.perf_counter()
+        A.sage_block_sparse_attention(sub["q_int8"], sub["k_int8"], sub["v_fp8"], sub["q_scale"],
+                                      sub["k_scale"], sub["v_scale"], sub["q2k_block_index"],
+                                      sub["block_sparse_num"], sub["block_sizes"],
+                                      sub["q2k_block_nums"], sub["softmax_scale"])
+        pairs, D = sage_pairs(sub), sub["q_int8"].shape[-1]
+    else:
+        raise ValueError(form)
+    secs = time.perf_counter() - t0
+    flops = 4 * D * pairs
+    return {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "seconds": secs,
+            "sample": f"{what}: {pairs} visible pairs, {flops / 1e9:.2f} GFLOP in {secs:.2f} s "
+                      "(BLAS threads = all host cores)"}
+
+
+def qsa_gathered_bytes(p):
+    """K/V bytes the bitmap (or indexed) form gathers: every query token reads the K and V
+    rows of each selected block that meets [lo, hi], for all KV heads."""
+    first = p["block_first"].numpy().astype(np.int64)
+    last = p["block_last"].numpy().astype(np.int64)
+    lo, hi = p["lo"].numpy().astype(np.int64), p["hi"].numpy().astype(np.int64)
+    if "sel_blocks" in p:
+        t, g = np.nonzero(p["sel_blocks"].numpy())
+    else:
+        idx = p["sel_indices"].numpy()
+        t, c = np.nonzero((idx >= 0) & (idx < first.size))
+        g = idx[t, c].astype(np.int64)
+    live = (np.minimum(last[g], hi[t]) >= np.maximum(first[g], lo[t]))
+    Hkv, D = p["k"].shape[1], p["k"].shape[2]
+    return int(live.sum()) * int(p["block_size"]) * Hkv * D * 2 * 2
+
+
+def l2_read_gbs(dev, mib=24, reps=64):
+    """The L2 read rate of this GPU: the library's probe over an L2-resident buffer, best of
+    5 launches, timed with events on the current stream."""
+    buf = torch.zeros(mib << 20, dtype=torch.uint8, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        pkb.paged_attn_l2_read_probe(buf, reps, sink)
+    best = float("inf")
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        pkb.paged_attn_l2_read_probe(buf, reps, sink)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    return buf.numel() * reps / (best * 1e-3) / 1e9
+
+
+# ----------------------------------------------------------------------------------------
 # main
 # ----------------------------------------------------------------------------------------
 
@@ -650,6 +855,18 @@ def main():
 
     if rank == 0 and world == 1 and not args.skip_cpu and p["form"] == "decode":
         line["cpu_baseline"] = cpu_baseline_decode(p)
+    l2_gbs = None
+    if p["form"] in ("qsa", "qsa_indexed"):
+        l2_gbs = l2_read_gbs(dev)
+        gb = qsa_gathered_bytes(p)
+        line["roofline_l2"] = {"bound": "l2", "achieved": gb / (kernel_ms * 1e-3) / 1e9,
+                               "peak": l2_gbs, "unit": "GB/s",
+                               "frac": gb / (kernel_ms * 1e-3) / 1e9 / l2_gbs,
+                               "gathered_bytes": gb,
+                               "peak_source": "measured in this run (paged_attn_l2_read_probe "
+                                              "over a 24 MiB L2-resident buffer)"}
+    if rank == 0 and world == 1 and not args.skip_cpu and p["form"] != "decode":
+        line["cpu_baseline"] = oracle_sample_rate(args.workload, p)
     if not args.no_extra and rank == 0:
         extra = {}
         for name in ("decode_b64_sq4", "tiny_bsr", "prefill_b16", "prefill_b16_w1023",
@@ -673,19 +890,37 @@ def main():
                                    "ms_step": reg / steps, "ms_kernel": kms, "kv_bytes": nb}
                     del rr
                     torch.cuda.empty_cache()
+                    if not args.skip_cpu:
+                        extra[name]["cpu_baseline"] = oracle_sample_rate(name, q)
                     continue
                 n = {"bsr": bsr_pairs, "prefill": prefill_pairs, "qsa": qsa_pairs,
                      "qsa_indexed": qsa_indexed_pairs, "sage": sage_pairs}[q["form"]](q)
                 flops = 4 * (q["q"] if "q" in q else q["q_int8"]).shape[-1] * n
+                tk = flops / (kms * 1e-3) / 1e12
                 extra[name] = {"tflops_step": flops / (reg / steps * 1e-3) / 1e12,
-                               "tflops_kernel": flops / (kms * 1e-3) / 1e12,
-                               "frac_bf16_peak": flops / (kms * 1e-3) / 1e12 / pk["bf16_tflops"],
+                               "tflops_kernel": tk,
+                               "frac_bf16_peak": tk / pk["bf16_tflops"],
+                               "frac_bf16_sustained": tk / pk.get("bf16_tflops_sustained",
+                                                                  pk["bf16_tflops"]),
                                "ms_step": reg / steps, "ms_kernel": kms,
                                "visible_pairs": n, "flops": flops}
+                if q["form"] in ("qsa", "qsa_indexed"):
+                    if l2_gbs is None:
+                        l2_gbs = l2_read_gbs(dev)
+                    gb = qsa_gathered_bytes(q)
+                    extra[name]["l2_gather"] = {
+                        "bound": "l2", "achieved": gb / (kms * 1e-3) / 1e9, "peak": l2_gbs,
+                        "unit": "GB/s", "frac": gb / (kms * 1e-3) / 1e9 / l2_gbs,
+                        "gathered_bytes": gb,
+                        "peak_source": "measured in this run (paged_attn_l2_read_probe over "
+                                       "a 24 MiB L2-resident buffer)"}
                 del rr
                 torch.cuda.empty_cache()
             except pkb.PagedAttnError as e:
                 extra[name] = {"unavailable": str(e)}
+                continue
+            if not args.skip_cpu:
+                extra[name]["cpu_baseline"] = oracle_sample_rate(name, q)
         line["per_config"] = extra
     if rank == 0:
         print(json.dumps(line))

@@ -12,7 +12,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libpagedattn.so")
 SOURCES = ["api.cu", "planner.cu", "decode.cu", "attn_tc.cu", "attn256.cu", "qsa.cu", "sage.cu",
-           "decode_static.cu"]
+           "decode_static.cu", "probe.cu"]
 HEADERS = ["common.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -108,12 +108,29 @@ def test_blocks_past_the_length_contribute_nothing():
 
 @pytest.mark.slow
 def test_long_bsr_workload_sampled():
+    """The 64K-token workload in its bench launch configuration.  Compared rows: every row of
+    the last 8 work tiles in launch order (the cheapest tiles, which run at the tail of the
+    persistent grid), one whole 128-row q-block, the edges of the first q-blocks, the last
+    row, and the rows of random whole tiles up to at least 1,024 in all."""
     p = W.long_bsr()
     out, lse, ws, params = _run(p)
-    rng = np.random.default_rng(5)
+    _check_plan(p, ws, params)
+    lay = pkb.plan_layout(params)
+    recs = read_ws(ws, lay.tiles_offset, 8 * lay.tiles_capacity).numpy().reshape(-1, 8)
     S = p["q"].shape[1]
-    rows = sorted(set(rng.integers(0, S, 48).tolist()) | {0, 1, 127, 128, S - 1})
+    rows = set()
+    for b, g, tok0, ntok, *_ in recs[-8:]:
+        assert b == 0
+        rows |= set(range(int(tok0), int(tok0) + int(ntok)))
+    qb = 300 * p["q_block_size"]
+    rows |= set(range(qb, qb + p["q_block_size"]))
+    rows |= {0, 1, 127, 128, S - 1}
+    rng = np.random.default_rng(5)
+    for t in rng.permutation(len(recs) - 8):        # whole random tiles
+        if len(rows) >= 1024:
+            break
+        rows |= set(range(int(recs[t, 2]), int(recs[t, 2]) + int(recs[t, 3])))
+    rows = sorted(rows)
     o_ref, l_ref = _oracle(p, rows=[(0, i) for i in rows])
     check_out(out[0, rows], o_ref[0, rows])
     check_lse(lse[0, rows], l_ref[0, rows])
-    _check_plan(p, ws, params)

@@ -72,15 +72,32 @@ def test_prefill_matches_oracle(case):
 @pytest.mark.slow
 @pytest.mark.parametrize("window", [-1, 1023])
 def test_prefill_b16_workload_sampled(window):
+    """The 16-request workload in its bench launch configuration.  Compared rows: every row
+    of the shortest request, of the last 16 work tiles in launch order (the tail of the
+    persistent grid) and of each request's last tile (a ragged second sub-tile), the first
+    and last row of every request, and random rows."""
     p = W.prefill_b16(window_left=window)
     out, lse, ws, params = _run(p)
+    _check_plan(p, ws, params)
+    lay = pkb.plan_layout(params)
+    n = int(read_ws(ws, lay.count_offset, 1)[0])
+    recs = read_ws(ws, lay.tiles_offset, 8 * n).numpy().reshape(-1, 8)
     qo = p["qo_indptr"].numpy()
-    rng = np.random.default_rng(7)
-    rows = set(rng.integers(0, int(qo[-1]), 40).tolist())
-    for b in range(len(qo) - 1):
+    nq = qo[1:] - qo[:-1]
+    rows = set()
+    b_min = int(np.argmin(nq))
+    rows |= set(range(int(qo[b_min]), int(qo[b_min + 1])))
+    for b, g, tok0, ntok, kv0, kv1, row0, _ in recs[-16:]:
+        rows |= set(range(int(row0), int(row0) + int(ntok)))
+    for b in range(len(nq)):
+        last = recs[(recs[:, 0] == b) & (recs[:, 2] + recs[:, 3] == nq[b])]
+        assert len(last) > 0
+        row0, ntok = int(last[0, 6]), int(last[0, 3])
+        rows |= set(range(row0, row0 + ntok))
         rows |= {int(qo[b]), int(qo[b + 1]) - 1}
+    rng = np.random.default_rng(7)
+    rows |= set(rng.integers(0, int(qo[-1]), 40).tolist())
     rows = sorted(rows)
     o_ref, l_ref = _oracle(p, rows=rows)
     check_out(out[rows], o_ref[rows])
     check_lse(lse[rows], l_ref[rows])
-    _check_plan(p, ws, params)

@@ -110,13 +110,23 @@ def test_qsa_capacity_overflow_is_reported():
 
 @pytest.mark.slow
 def test_qsa_t32k_workload_sampled():
+    """The 32K-token workload in its bench launch configuration.  Compared tokens: the first
+    and last 8 of every packed sequence (short and full-length selections) and random tokens
+    up to at least 512 in all."""
     p = W.qsa_t32k()
     out, out32, lse, ws, params = _run(p, max_blocks_per_query=272)
-    rng = np.random.default_rng(11)
+    _check_plan(p, ws, params)
     T = p["q"].shape[0]
-    rows = sorted(set(rng.integers(0, T, 24).tolist()) | {0, 1, 4095, 4096, T - 1})
+    starts = np.unique(p["tok_base"].numpy())
+    ends = np.concatenate([starts[1:], [T]])
+    rows = set()
+    for a, e in zip(starts.tolist(), ends.tolist()):
+        rows |= set(range(a, a + 8)) | set(range(e - 8, e))
+    rng = np.random.default_rng(11)
+    while len(rows) < 512:
+        rows.add(int(rng.integers(0, T)))
+    rows = sorted(rows)
     o_ref, l_ref = _oracle(p, rows=rows)
     check_out(out[rows], o_ref[rows])
     check_out(out32[rows], o_ref[rows])
     check_lse(lse[:, rows], l_ref[:, rows])
-    _check_plan(p, ws, params)
