@@ -201,7 +201,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&ctl->s_full[w], 1);
-      mbar_init(&ctl->p_full[w], 128);
+      mbar_init(&ctl->p_full[w], 4);           // one arrival per softmax warp
       mbar_init(&ctl->o_final[w], 1);
       mbar_init(&ctl->o_empty[w], 128);
     }
@@ -422,8 +422,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (N == 0) continue;
         const bool two = t.nsub > 1;
         const int it0 = kv_it;
-        ok = mbar_wait<true>(&ctl->q_full, qcount & 1, a.status, abort_flag) &&
-             mbar_wait<true>(&ctl->k_full[it0 % kKStages], (it0 / kKStages) & 1, a.status, abort_flag);
+        ok = mbar_wait_fast(&ctl->q_full, qcount & 1, a.status, abort_flag) &&
+             mbar_wait_fast(&ctl->k_full[it0 % kKStages], (it0 / kKStages) & 1, a.status, abort_flag);
         ++qcount;
         if (!ok) break;
         tc_fence_after();
@@ -433,45 +433,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (N == 1) mma_commit(&ctl->q_empty);
         for (int n = 0; n < N; ++n) {
           const int it = it0 + n, vs = it % kVStages;
-          if (!mbar_wait<true>(&ctl->v_full[vs], (it / kVStages) & 1, a.status, abort_flag) ||
-              !mbar_wait<true>(&ctl->p_full[0], it & 1, a.status, abort_flag) ||
+          const bool more = n + 1 < N;
+          const int ks_next = (it + 1) % kKStages;
+          // Every input of PV_0(n) and QK_0(n + 1) first (the next K stage has normally landed
+          // long before), so that the two groups issue back to back: the issuing thread
+          // blocks while the pipe accepts each MMA, and a wait between them would leave the
+          // pipe idle on this sub-tile's critical chain P -> PV -> QK -> S.
+          if (!mbar_wait_fast(&ctl->v_full[vs], (it / kVStages) & 1, a.status, abort_flag) ||
+              (more && !mbar_wait_fast(&ctl->k_full[ks_next], ((it + 1) / kKStages) & 1,
+                                        a.status, abort_flag)) ||
               (n == 0 && ep[0] > 0 &&
-               !mbar_wait<true>(&ctl->o_empty[0], (ep[0] - 1) & 1, a.status, abort_flag))) {
+               !mbar_wait_fast(&ctl->o_empty[0], (ep[0] - 1) & 1, a.status, abort_flag)) ||
+              !mbar_wait_fast(&ctl->p_full[0], it & 1, a.status, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_pv(0, vs, n > 0);
+          if (more) issue_qk(0, ks_next);
           if (n == N - 1) mma_commit(&ctl->o_final[0]);
-          const bool more = n + 1 < N;
-          const int ks_next = (it + 1) % kKStages;
-          if (more) {
-            if (!mbar_wait<true>(&ctl->k_full[ks_next], ((it + 1) / kKStages) & 1, a.status,
-                           abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_qk(0, ks_next);
-          }
           if (two) {
-            if (!mbar_wait<true>(&ctl->p_full[1], pc1 & 1, a.status, abort_flag) ||
+            if (!mbar_wait_fast(&ctl->p_full[1], pc1 & 1, a.status, abort_flag) ||
                 (n == 0 && ep[1] > 0 &&
-                 !mbar_wait<true>(&ctl->o_empty[1], (ep[1] - 1) & 1, a.status, abort_flag))) {
+                 !mbar_wait_fast(&ctl->o_empty[1], (ep[1] - 1) & 1, a.status, abort_flag))) {
               ok = false;
               break;
             }
             ++pc1;
             tc_fence_after();
             issue_pv(1, vs, n > 0);
+            if (more) issue_qk(1, ks_next);
             if (n == N - 1) mma_commit(&ctl->o_final[1]);
           }
-          mma_commit(&ctl->v_empty[vs]);
           if (more) {
-            if (two) issue_qk(1, ks_next);
             mma_commit(&ctl->k_empty[ks_next]);
             if (n + 1 == N - 1) mma_commit(&ctl->q_empty);
           }
+          mma_commit(&ctl->v_empty[vs]);
         }
         kv_it += N;
         ++ep[0];
@@ -531,7 +529,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       float m_run = -INFINITY, l_run = 0.f;
       for (int n = 0; n < N; ++n) {
         const int it = kv_it + n;
-        if (!mbar_wait_warp<true>(&ctl->s_full[w], sc & 1, a.status, abort_flag)) {
+        if (!mbar_wait_fast_warp(&ctl->s_full[w], sc & 1, a.status, abort_flag)) {
           ok = false;
           break;
         }
@@ -735,7 +733,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           }
         }
         tc_fence_before();
-        mbar_arrive(&ctl->p_full[w]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->p_full[w]);
       }
       if (has_nx) rec_nx = a.tiles[idx_nx];
       // ---- epilogue ------------------------------------------------------------------------
