@@ -27,7 +27,8 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  All
  *     device work is enqueued on it; no entry point of the run path synchronises the host
  *     or copies device metadata back to the host, so a planned run can be captured in a
- *     CUDA graph ([BSA] summary; [DEC] notes: "no device-to-host synchronization").
+ *     CUDA graph ([BSA] summary; [DEC] notes, which rule out any read-back of device
+ *     metadata to the host during a launch).
  *   - Element types: Q, K and V are bf16 (int8 and FP8 E4M3 bytes in the prequantized
  *     form); outputs are bf16, or fp16 / fp32 where out_dtype selects them (prefill and
  *     decode); page tables, lengths and offsets are int32; kv_valid_bits is uint32; LSE and
@@ -142,8 +143,9 @@ typedef struct paged_attn_meta {
  * (0 on invalid params).  The workspace holds the status word and the plan. */
 size_t paged_attn_workspace_size(const paged_attn_params* params);
 
-/* Host-side validation of BSR metadata, the analogue of the synchronous checks of the
- * [BSA] convenience entry point (summary: "validates live page and sparse metadata").
+/* Host-side validation of BSR metadata, the analogue of the synchronous checks that the
+ * [BSA] convenience entry point makes on the page table and the block lists before it runs
+ * ([BSA] summary).
  * All pointers are HOST copies.  Checks: kv_indptr starts at 0, is non-decreasing and
  * ends at num_kv_indices; every request owns ceil(len / page_size) pages; every live page
  * id is in [0, num_pages); 0 <= len <= max_seq_len_kv; block_indptr rows are
