@@ -645,6 +645,15 @@ int paged_attn_plan(const paged_attn_params* p, const paged_attn_meta* m, void* 
   if (!ws || ws_bytes < s.total) return PAGED_ATTN_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t* status = at<uint32_t>(ws, s.status);
+  if (p->form == PAGED_ATTN_FORM_BSR && m->block_indptr_dev &&
+      bsr_plan_is_small(p->batch, p->num_kv_heads, p->q_len, p->q_block_size, s.capacity,
+                        s.max_cost)) {
+    // one launch: tiles, their order and the status clear
+    launch_bsr_plan_small(m->block_indptr_dev, p->batch, p->num_kv_heads, p->q_len,
+                          p->q_block_size, s.tile_tokens, s.capacity, s.max_cost,
+                          at<TileRec>(ws, s.sorted), status, st);
+    return cudaGetLastError() == cudaSuccess ? PAGED_ATTN_OK : PAGED_ATTN_ERR_CUDA;
+  }
   if (cudaMemsetAsync(status, 0, 4 * sizeof(uint32_t), st) != cudaSuccess) return PAGED_ATTN_ERR_CUDA;
   if (p->form == PAGED_ATTN_FORM_BSR) {
     if (!m->block_indptr_dev) return PAGED_ATTN_ERR_INVALID_ARGUMENT;

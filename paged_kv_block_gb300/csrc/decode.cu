@@ -332,10 +332,14 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
     constexpr int slice_keys = kStageKeys / kg; // 16 * NRB
     int sg = 0;
     int jcount = 0;                            // merge jobs handed to the merge warp
+    // The consumer warps meet at named barriers every item, so they leave the item loop
+    // only together: each failed wait is carried to a barrier whose reduction (bar.red.or)
+    // tells every warp.
     for (int icount = 0;; ++icount) {
       const int islot = icount % kItemSlots;
-      if (!mbar_wait_warp(&sm->item_full[islot], (icount / kItemSlots) & 1, a.status, abort_flag))
-        break;
+      const bool got = mbar_wait_warp(&sm->item_full[islot], (icount / kItemSlots) & 1,
+                                      a.status, abort_flag);
+      if (named_bar_or(1, kConsumerWarps * 32, !got)) break;
       const int item = sm->item_id[islot];
       if (item < 0) {
         if (threadIdx.x == 0) {                  // end of the merge queue
@@ -544,7 +548,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap kmap,
           }
         }
       }
-      if (!ok) break;
+      if (named_bar_or(1, kConsumerWarps * 32, !ok)) break;   // some warp's stage wait failed
 
       // ---- combine the key slices of each row ---------------------------------------------
       // red_o [kg][M][128] fp32 in the item's last stage, which no warp reads any more once

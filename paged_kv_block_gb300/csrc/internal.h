@@ -96,6 +96,13 @@ inline int cta_tile_tokens(int G) { return 2 * sub_tile_tokens(G); }
 // All write the status word on capacity problems; none synchronises the host.
 void launch_bsr_tiles(const int* block_indptr, int B, int Hkv, int Sq, int qbs, int tile_tokens,
                       TileRec* tmp, cudaStream_t st);
+// A block-sparse plan small enough for one CTA (capacity and rows within one sort chunk):
+// launch_bsr_plan_small then writes the sorted records directly and clears the 4 status
+// words, in place of launch_bsr_tiles + launch_tile_sort.
+bool bsr_plan_is_small(int B, int Hkv, int Sq, int qbs, int capacity, int max_cost);
+void launch_bsr_plan_small(const int* block_indptr, int B, int Hkv, int Sq, int qbs,
+                           int tile_tokens, int capacity, int max_cost, TileRec* out,
+                           uint32_t* status, cudaStream_t st);
 // Request b has qo_indptr[b + 1] - qo_indptr[b] queries at rows from qo_indptr[b], or
 // (qo_indptr == nullptr) q_len queries at rows from b * q_len.
 void launch_prefill_tiles(const int* qo_indptr, int q_len, const int* seq_lens, int B, int Hkv,

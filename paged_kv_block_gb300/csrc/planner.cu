@@ -262,6 +262,77 @@ __global__ void sort_scatter_kernel(const TileRec* __restrict__ in, TileRec* __r
   }
 }
 
+// ---- block-sparse plan of at most one sort chunk, in one CTA ------------------------------
+// The records of bsr_tiles_kernel and the stable counting sort of the three sort kernels
+// (same records, same order), built in shared memory by one CTA of kSortChunk threads: a
+// small plan costs one launch instead of four.  Also clears the workspace status words.
+__global__ void __launch_bounds__(kSortChunk)
+bsr_plan_small_kernel(const int* __restrict__ block_indptr, int B, int Hkv, int Sq, int qbs,
+                      int tt, int maxc, int n, TileRec* __restrict__ out,
+                      uint32_t* __restrict__ status) {
+  extern __shared__ int4 sm_small[];
+  TileRec* recs = reinterpret_cast<TileRec*>(sm_small);          // n records
+  int* cnt = reinterpret_cast<int*>(recs + n);                   // maxc + 1 bins
+  __shared__ int warp_sums[32];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (tid < 4) status[tid] = 0u;
+  // tiles in their natural order (the indexing of bsr_tiles_kernel)
+  const int nqb = (Sq + qbs - 1) / qbs;
+  if (tid < B * Hkv * nqb) {
+    const int r = tid % nqb, bg = tid / nqb, g = bg % Hkv, b = bg / Hkv;
+    const int full_tiles = (qbs + tt - 1) / tt;
+    const int last_n = Sq - (nqb - 1) * qbs;
+    const int tiles_per_bg = (nqb - 1) * full_tiles + (last_n + tt - 1) / tt;
+    const int n_r = min(qbs, Sq - r * qbs);
+    const int base = bg * tiles_per_bg + r * full_tiles;
+    const int kb = block_indptr[bg * (nqb + 1) + r];
+    const int ke = block_indptr[bg * (nqb + 1) + r + 1];
+    for (int m = 0; m * tt < n_r; ++m) {
+      TileRec t;
+      t.b = b;
+      t.g = g;
+      t.tok0 = r * qbs + m * tt;
+      t.ntok = min(tt, n_r - m * tt);
+      t.kv_begin = kb;
+      t.kv_end = ke;
+      t.q_row0 = b * Sq + t.tok0;
+      t.pad = 0;
+      recs[base + m] = t;
+    }
+  }
+  for (int k = tid; k <= maxc; k += blockDim.x) cnt[k] = 0;
+  __syncthreads();
+  const bool live = tid < n;
+  const int k = live ? rec_cost(recs[tid], maxc) : -1;
+  if (live) atomicAdd(&cnt[k], 1);
+  __syncthreads();
+  // cnt[k] := number of records with a larger cost (scan of the bins from the top)
+  int carry = 0;
+  for (int d0 = 0; d0 <= maxc; d0 += blockDim.x) {
+    const int d = d0 + tid;
+    const int v = d <= maxc ? cnt[maxc - d] : 0;
+    int total;
+    const int ex = block_exclusive_scan(v, warp_sums, total);
+    if (d <= maxc) cnt[maxc - d] = carry + ex;
+    carry += total;
+  }
+  __syncthreads();
+  // stable scatter: warps take their turn in index order, lanes by rank among equal costs
+  const unsigned peers = __match_any_sync(0xffffffffu, k);
+  const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
+  const int leader = __ffs(peers) - 1;
+  int my_base = 0;
+  for (int step = 0; step < (kSortChunk >> 5); ++step) {
+    if (w == step) {
+      if (live) my_base = cnt[k];
+      __syncwarp();
+      if (live && lane == leader) cnt[k] = my_base + __popc(peers);
+    }
+    __syncthreads();
+  }
+  if (live) out[my_base + rank_in_warp] = recs[tid];
+}
+
 // ---- bitmap planner ------------------------------------------------------------------------
 __device__ __forceinline__ int first_block_ending_at_or_after(const int* __restrict__ blast,
                                                               int NB, int lo) {
@@ -509,6 +580,23 @@ void launch_bsr_tiles(const int* block_indptr, int B, int Hkv, int Sq, int qbs, 
   if (rows <= 0) return;
   bsr_tiles_kernel<<<ceil_div(rows, 256), 256, 0, st>>>(block_indptr, B, Hkv, Sq, qbs,
                                                         tile_tokens, tmp);
+  count_launches(1);
+}
+
+bool bsr_plan_is_small(int B, int Hkv, int Sq, int qbs, int capacity, int max_cost) {
+  const long long rows = static_cast<long long>(B) * Hkv * ceil_div(Sq, qbs);
+  const long long smem = static_cast<long long>(capacity) * sizeof(TileRec) +
+                         static_cast<long long>(max_cost + 1) * sizeof(int);
+  return capacity > 0 && capacity <= kSortChunk && rows <= kSortChunk && smem <= 40 * 1024;
+}
+
+void launch_bsr_plan_small(const int* block_indptr, int B, int Hkv, int Sq, int qbs,
+                           int tile_tokens, int capacity, int max_cost, TileRec* out,
+                           uint32_t* status, cudaStream_t st) {
+  const size_t smem = static_cast<size_t>(capacity) * sizeof(TileRec) +
+                      static_cast<size_t>(max_cost + 1) * sizeof(int);
+  bsr_plan_small_kernel<<<1, kSortChunk, smem, st>>>(block_indptr, B, Hkv, Sq, qbs, tile_tokens,
+                                                     max_cost, capacity, out, status);
   count_launches(1);
 }
 

@@ -387,21 +387,27 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
     float l[kGroupCols];
 #pragma unroll
     for (int h = 0; h < kGroupCols; ++h) l[h] = 0.f;
+    // The four softmax warps meet at named barriers every tile, so they must take the same
+    // path through the loop: a failed wait does not leave the loop at once but is carried
+    // in `ok` to the tile's first barrier, whose reduction tells every warp to leave together.
     for (int n = 0; n < N; ++n) {
       const int uk = unit_k(n);                        // S^T(n) ready = K(n)'s slot released
-      if (!mbar_wait_warp(&ctl->empty[uk % kPairs], (uk / kPairs) & 1, a.status, abort_flag)) break;
-      tc_fence_after();
+      bool ok = mbar_wait_warp(&ctl->empty[uk % kPairs], (uk / kPairs) & 1, a.status, abort_flag);
       uint32_t sv[kN];
-      tmem_ld32(tmem + lane_base + s_col(n), sv);
-      tmem_ld_wait();
-      if (!mbar_wait_warp(&ctl->tab_full[n % kTabBufs], (n / kTabBufs) & 1, a.status, abort_flag))
-        break;
-      const int code = ctl->tab[n % kTabBufs][r];
+      if (ok) {
+        tc_fence_after();
+        tmem_ld32(tmem + lane_base + s_col(n), sv);
+        tmem_ld_wait();
+      }
+      ok = ok && mbar_wait_warp(&ctl->tab_full[n % kTabBufs], (n / kTabBufs) & 1, a.status,
+                                abort_flag);
+      const int code = ok ? ctl->tab[n % kTabBufs][r] : kDeadZero;
       const bool valid = code == kLive;
       float x[kGroupCols];
 #pragma unroll
       for (int h = 0; h < kGroupCols; ++h)
         x[h] = (valid && h < G) ? __uint_as_float(gg ? sv[kGroupCols + h] : sv[h]) * sl2 : -INFINITY;
+      if (named_bar_or(1, 128, !ok)) break;            // some warp failed: all leave
       // The running maxima change only when some score exceeds them by the rescale threshold,
       // which after the first tile is rare: test for that first and compute the exact
       // column maxima of the tile only when it happens.
@@ -433,32 +439,35 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
       }
       const bool need = __any_sync(0xffffffffu, alpha_c != 1.f);
       const float mu_c = m_c == -INFINITY ? 0.f : m_c;
-      // P^T buffer n % 2 was read by PV(n - 2), which must have completed
-      if (n > 1 && !mbar_wait_warp(&ctl->pv_done[n & 1], ((n - 2) >> 1) & 1, a.status, abort_flag))
-        break;
-      // P^T [32 columns][128 rows], two K-major 64-row chunks with the 128-byte swizzle; this
-      // thread writes its own group's 16 columns, the other group's stay zero
-      uint8_t* prow = p_s + (n & 1) * kPBytes + (r >> 6) * (kN * 128);
-      const int rr = r & 63;
+      // P^T buffer n % 2 was read by PV(n - 2), which must have completed.  From here on a
+      // failure skips the rest of the tile; the next tile's first barrier ends the loop.
+      ok = n <= 1 || mbar_wait_warp(&ctl->pv_done[n & 1], ((n - 2) >> 1) & 1, a.status, abort_flag);
+      if (ok) {
+        // P^T [32 columns][128 rows], two K-major 64-row chunks with the 128-byte swizzle;
+        // this thread writes its own group's 16 columns, the other group's stay zero
+        uint8_t* prow = p_s + (n & 1) * kPBytes + (r >> 6) * (kN * 128);
+        const int rr = r & 63;
 #pragma unroll
-      for (int h = 0; h < kGroupCols; ++h) {
-        const int c = gg * kGroupCols + h;
-        const float mu = __shfl_sync(0xffffffffu, mu_c, c);
-        const float ac = __shfl_sync(0xffffffffu, alpha_c, c);
-        const float pv = fast_exp2(x[h] - mu);
-        l[h] = l[h] * ac + pv;
-        *reinterpret_cast<__nv_bfloat16*>(prow + c * 128 + ((((rr >> 3) ^ (c & 7)) & 7) << 4) +
-                                          (rr & 7) * 2) = __float2bfloat16_rn(pv);
+        for (int h = 0; h < kGroupCols; ++h) {
+          const int c = gg * kGroupCols + h;
+          const float mu = __shfl_sync(0xffffffffu, mu_c, c);
+          const float ac = __shfl_sync(0xffffffffu, alpha_c, c);
+          const float pv = fast_exp2(x[h] - mu);
+          l[h] = l[h] * ac + pv;
+          *reinterpret_cast<__nv_bfloat16*>(prow + c * 128 + ((((rr >> 3) ^ (c & 7)) & 7) << 4) +
+                                            (rr & 7) * 2) = __float2bfloat16_rn(pv);
+        }
+        if (code == kDeadLoaded)
+          ok = zero_dead_v_row(ctl, ring, unit_v(n, N), r, a.status, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
       }
-      if (code == kDeadLoaded &&
-          !zero_dead_v_row(ctl, ring, unit_v(n, N), r, a.status, abort_flag))
-        n = N;                                         // aborted: leave after this arrival
-      if (n > 0 && need) {
+      if (ok && n > 0 && need) {
         // O^T is accumulated by PV(n - 1): it must have completed before the rescale
-        if (!mbar_wait_warp(&ctl->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, a.status, abort_flag))
-          break;
-        tc_fence_after();
-        rescale_o(tmem + lane_base + 32, alpha_c);
+        ok = mbar_wait_warp(&ctl->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, a.status, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          rescale_o(tmem + lane_base + 32, alpha_c);
+        }
       }
       fence_proxy_async_smem();   // P^T and zeroed V rows (generic) -> tensor-core reads
       tc_fence_before();
