@@ -78,7 +78,7 @@ struct QsaCtrl {
   uint64_t tab_full[kTabBufs];
   uint64_t p_full[2];                         // P^T of tiles n with n % 2 = index written
   uint64_t pv_done[2];                        // PV of tiles n with n % 2 = index complete
-  uint64_t q_full, o_full;
+  uint64_t q_full, q_empty, o_full, o_empty;
   uint32_t tmem_base;
   int abort_flag;
   int8_t tab[kTabBufs][kRows];
@@ -201,15 +201,27 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
 
   // one decision for the whole CTA: another CTA may set the status word meanwhile
   if (__syncthreads_or(launch_aborted(a.status))) return;
-  const int t = blockIdx.x / a.pairs, g0 = 2 * (blockIdx.x % a.pairs);
-  const bool two = g0 + 1 < a.Hkv;
+  const int jobs = a.T * a.pairs;                // (query token, KV-head pair) units of work
   const int G = a.G;
-  const int beg = __ldg(a.indptr + t);
-  const int nblk = __ldg(a.indptr + t + 1) - beg;
-  const int N = nblk > 0 ? (nblk + kBlocksPerTile - 1) / kBlocksPerTile : 0;   // tiles
-  const int S = kUnitsPerTile * N;                                              // units
-  const int lo = __ldg(a.lo + t), hi = __ldg(a.hi + t);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The CTA walks jobs blockIdx.x, + gridDim.x, ...; every counter below runs over the whole
+  // walk (units, tiles, jobs with tiles), so the rings' phases carry from job to job.
+  struct Job {
+    int t, g0, beg, nblk, N, lo, hi;
+    bool two;
+  };
+  auto job_of = [&](int jj) -> Job {
+    Job jb;
+    jb.t = jj / a.pairs;
+    jb.g0 = 2 * (jj % a.pairs);
+    jb.two = jb.g0 + 1 < a.Hkv;
+    jb.beg = __ldg(a.indptr + jb.t);
+    jb.nblk = __ldg(a.indptr + jb.t + 1) - jb.beg;
+    jb.N = jb.nblk > 0 ? (jb.nblk + kBlocksPerTile - 1) / kBlocksPerTile : 0;
+    jb.lo = __ldg(a.lo + jb.t);
+    jb.hi = __ldg(a.hi + jb.t);
+    return jb;
+  };
 
   // Q rows G..15 of each group and all of P^T start at zero: the copies never write the
   // former, and softmax writes only its own group's half of the latter.
@@ -221,11 +233,13 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
     for (int i = 0; i < kPairs; ++i) mbar_init(&ctl->empty[i], 1);
     for (int i = 0; i < kTabBufs; ++i) mbar_init(&ctl->tab_full[i], 32 * kProducers);
     mbar_init(&ctl->q_full, 1);
+    mbar_init(&ctl->q_empty, 1);
     mbar_init(&ctl->pv_done[0], 1);
     mbar_init(&ctl->pv_done[1], 1);
     mbar_init(&ctl->p_full[0], 128);
     mbar_init(&ctl->p_full[1], 128);
     mbar_init(&ctl->o_full, 1);
+    mbar_init(&ctl->o_empty, 128);
     ctl->abort_flag = 0;
     fence_mbar_init();
   }
@@ -243,132 +257,173 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
   if (warp < kProducers) {
     // ================================ producers ===========================================
     const int pw = warp;
-    if (N > 0 && pw == 0) {
-      if (lane == 0) {
-        tma_prefetch_desc(&kmap);
-        tma_prefetch_desc(&vmap);
-        mbar_arrive_expect_tx(&ctl->q_full, (two ? 8u : 4u) * static_cast<uint32_t>(G) * 128u);
-      }
-      __syncwarp();
-      if (lane < (two ? 8 : 4)) {                      // Q: d chunk lane & 3, group lane >> 2
-        const int c = lane & 3, gg = lane >> 2;
-        tma_load_3d(q_s + c * (kN * 128) + gg * (kGroupCols * 128), &qmap, &ctl->q_full, c * 64,
-                    (g0 + gg) * G, t);
-      }
+    if (pw == 0 && lane == 0) {
+      tma_prefetch_desc(&kmap);
+      tma_prefetch_desc(&vmap);
     }
     // lane l < 4 of producer warp pw (pipeline pl = pw / 2) handles block 4 pw + l of each tile
     const int pl = pw / 2;
     const int jb = kBlocksPerProducer * pw + lane;
-    auto block_of = [&](int n) -> int {
-      const int i = n * kBlocksPerTile + jb;
-      return (lane < kBlocksPerProducer && n < N && i < nblk) ? __ldg(a.indices + beg + i) : -1;
-    };
-    // block spans are fetched two tiles ahead of their publication: block ids of tile n + 2 and
-    // first/last tokens of tile n + 1 are in flight while tile n is published
-    int b_cur = block_of(0), first_cur = 0, last_cur = -1;
-    if (b_cur >= 0) {
-      first_cur = __ldg(a.bfirst + b_cur);
-      last_cur = __ldg(a.blast + b_cur);
-    }
-    int b_nx = block_of(1);
-    int first_t[2] = {a.T, a.T};   // token coordinate of this lane's block in tiles of parity 0/1
-    int issued = 0;
-    for (int s = 0; s < S; ++s) {
-      // unit s: K(n) or V(n) in the consumption order
-      const bool is_k = s == 0 || (s & 1 && s != S - 1);
-      const int n = s == 0 ? 0 : (is_k ? (s + 1) >> 1 : (s == S - 1 ? N - 1 : (s - 2) >> 1));
-      const int ps = s % kPairs;
-      if (is_k) {                                      // publish tile n's rows
-        const int f = b_cur >= 0 ? first_cur : a.T;
-        if (n & 1) first_t[1] = f; else first_t[0] = f;
-        if (lane < kBlocksPerProducer) {
-          int8_t* tab = ctl->tab[n % kTabBufs] + jb * 8;
+    int U = 0, gt = 0, jq = 0;                  // units, tiles, jobs with tiles so far
+    int issued = 0, q_issued = 0;               // copies issued (units, Q loads)
+    int first_t0 = a.T, first_t1 = a.T;  // token coordinate of this lane's block in tiles of parity 0/1
+    bool ok = true;
+    for (int jj = blockIdx.x; ok && jj < jobs; jj += gridDim.x) {
+      const Job J = job_of(jj);
+      if (J.N == 0) continue;
+      const int S = kUnitsPerTile * J.N;
+      if (pw == 0) {
+        // Q of this job, once the previous job's last QK has read the buffer
+        ok = jq == 0 || mbar_wait_warp(&ctl->q_empty, (jq - 1) & 1, a.status, abort_flag);
+        if (!ok) break;
+        if (lane == 0)
+          mbar_arrive_expect_tx(&ctl->q_full, (J.two ? 8u : 4u) * static_cast<uint32_t>(G) * 128u);
+        __syncwarp();
+        if (lane < (J.two ? 8 : 4)) {                  // Q: d chunk lane & 3, group lane >> 2
+          const int c = lane & 3, gg = lane >> 2;
+          tma_load_3d(q_s + c * (kN * 128) + gg * (kGroupCols * 128), &qmap, &ctl->q_full,
+                      c * 64, (J.g0 + gg) * G, J.t);
+        }
+        ++q_issued;
+      }
+      auto block_of = [&](int n) -> int {
+        const int i = n * kBlocksPerTile + jb;
+        return (lane < kBlocksPerProducer && n < J.N && i < J.nblk) ? __ldg(a.indices + J.beg + i)
+                                                                   : -1;
+      };
+      // block spans are fetched two tiles ahead of their publication: block ids of tile
+      // n + 2 and first/last tokens of tile n + 1 are in flight while tile n is published
+      int b_cur = block_of(0), first_cur = 0, last_cur = -1;
+      if (b_cur >= 0) {
+        first_cur = __ldg(a.bfirst + b_cur);
+        last_cur = __ldg(a.blast + b_cur);
+      }
+      int b_nx = block_of(1);
+      for (int s = 0; s < S; ++s) {
+        // unit s: K(n) or V(n) in the consumption order
+        const bool is_k = s == 0 || (s & 1 && s != S - 1);
+        const int n = s == 0 ? 0 : (is_k ? (s + 1) >> 1 : (s == S - 1 ? J.N - 1 : (s - 2) >> 1));
+        const int u = U + s, ps = u % kPairs, g = gt + n;
+        if (is_k) {                                    // publish tile n's rows
+          const int f = b_cur >= 0 ? first_cur : a.T;
+          if (g & 1) first_t1 = f; else first_t0 = f;
+          if (lane < kBlocksPerProducer) {
+            int8_t* tab = ctl->tab[g % kTabBufs] + jb * 8;
 #pragma unroll
-          for (int o = 0; o < 4; ++o) {
-            const int tok = first_cur + o;
+            for (int o = 0; o < 4; ++o) {
+              const int tok = first_cur + o;
 #pragma unroll
-            for (int gg = 0; gg < 2; ++gg) {
-              int8_t code;
-              if (b_cur < 0 || tok >= a.T || (gg == 1 && !two)) code = kDeadZero;
-              else if (tok <= last_cur && tok >= lo && tok <= hi) code = kLive;
-              else code = kDeadLoaded;
-              tab[o * 2 + gg] = code;                  // row = token offset * 2 + head
+              for (int gg = 0; gg < 2; ++gg) {
+                int8_t code;
+                if (b_cur < 0 || tok >= a.T || (gg == 1 && !J.two)) code = kDeadZero;
+                else if (tok <= last_cur && tok >= J.lo && tok <= J.hi) code = kLive;
+                else code = kDeadLoaded;
+                tab[o * 2 + gg] = code;                // row = token offset * 2 + head
+              }
             }
           }
+          mbar_arrive(&ctl->tab_full[g % kTabBufs]);
+          // advance the prefetch: spans of tile n + 1 (ids fetched a tile ago), ids of n + 2
+          b_cur = b_nx;
+          if (b_cur >= 0) {
+            first_cur = __ldg(a.bfirst + b_cur);
+            last_cur = __ldg(a.blast + b_cur);
+          }
+          b_nx = block_of(n + 2);
         }
-        mbar_arrive(&ctl->tab_full[n % kTabBufs]);
-        // advance the prefetch: spans of tile n + 1 (ids fetched a tile ago), ids of n + 2
-        b_cur = b_nx;
-        if (b_cur >= 0) {
-          first_cur = __ldg(a.bfirst + b_cur);
-          last_cur = __ldg(a.blast + b_cur);
+        if (u >= kPairs &&
+            !mbar_wait_warp(&ctl->empty[ps], ((u / kPairs) - 1) & 1, a.status, abort_flag)) {
+          ok = false;
+          break;
         }
-        b_nx = block_of(n + 2);
+        if (lane == 0) mbar_arrive_expect_tx(&ctl->full[pl][ps], kBlocksPerProducer * kBlockBytes);
+        __syncwarp();
+        if (lane < kBlocksPerProducer)
+          tma_load_4d(ring + ps * kPairBytes + jb * kBlockBytes, is_k ? &kmap : &vmap,
+                      &ctl->full[pl][ps], 0, J.g0, (g & 1) ? first_t1 : first_t0, 0);
+        issued = u + 1;
       }
-      if (s >= kPairs &&
-          !mbar_wait_warp(&ctl->empty[ps], ((s / kPairs) - 1) & 1, a.status, abort_flag))
-        break;
-      if (lane == 0) mbar_arrive_expect_tx(&ctl->full[pl][ps], kBlocksPerProducer * kBlockBytes);
-      __syncwarp();
-      if (lane < kBlocksPerProducer)
-        tma_load_4d(ring + ps * kPairBytes + jb * kBlockBytes, is_k ? &kmap : &vmap,
-                    &ctl->full[pl][ps], 0, g0, (n & 1) ? first_t[1] : first_t[0], 0);
-      issued = s + 1;
+      if (!ok) break;
+      U += S;
+      gt += J.N;
+      ++jq;
     }
     if (*abort_flag && lane == 0) {                    // copies still in flight after an abort
-      for (int s = issued > kPairs ? issued - kPairs : 0; s < issued; ++s)
-        drain_wait(&ctl->full[pl][s % kPairs], (s / kPairs) & 1);
-      if (N > 0 && pw == 0) drain_wait(&ctl->q_full, 0);
+      for (int u = issued > kPairs ? issued - kPairs : 0; u < issued; ++u)
+        drain_wait(&ctl->full[pl][u % kPairs], (u / kPairs) & 1);
+      if (pw == 0 && q_issued > 0) drain_wait(&ctl->q_full, (q_issued - 1) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ================================ MMA issuer ==========================================
-    if (lane == 0 && N > 0) {
+    if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(128, kN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(128, kN, true, false);
       const uint32_t ring_addr = smem_u32(ring), q_addr = smem_u32(q_s), p_addr = smem_u32(p_s);
-      // S^T of tile n + 1 is computed while softmax works on tile n (two S^T buffers), so
-      // softmax runs tile after tile without waiting for an MMA round trip.
-      auto issue_qk = [&](int n) -> bool {
-        const int u = unit_k(n), sk = u % kPairs;
-        if (!mbar_wait(&ctl->full[0][sk], (u / kPairs) & 1, a.status, abort_flag) ||
-            !mbar_wait(&ctl->full[1][sk], (u / kPairs) & 1, a.status, abort_flag))
-          return false;
-        tc_fence_after();
+      int U = 0, gt = 0, jq = 0;
+      bool ok = true;
+      for (int jj = blockIdx.x; ok && jj < jobs; jj += gridDim.x) {
+        const int t = jj / a.pairs;
+        const int nblk = __ldg(a.indptr + t + 1) - __ldg(a.indptr + t);
+        const int N = nblk > 0 ? (nblk + kBlocksPerTile - 1) / kBlocksPerTile : 0;
+        if (N == 0) continue;
+        // S^T of tile n + 1 is computed while softmax works on tile n (two S^T buffers,
+        // indexed by the tile count of the whole walk), so softmax runs tile after tile
+        // without waiting for an MMA round trip.
+        auto issue_qk = [&](int n) -> bool {
+          const int u = U + unit_k(n), sk = u % kPairs;
+          if (!mbar_wait(&ctl->full[0][sk], (u / kPairs) & 1, a.status, abort_flag) ||
+              !mbar_wait(&ctl->full[1][sk], (u / kPairs) & 1, a.status, abort_flag))
+            return false;
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {                 // chunk k / 4, 16 columns (k % 4)
-          const uint32_t ka = ring_addr + sk * kPairBytes + (k >> 2) * 1024 + (k & 3) * 32;
-          const uint32_t qa = q_addr + (k >> 2) * (kN * 128) + (k & 3) * 32;
-          mma_ss(tmem + s_col(n), sdesc_sw128(ka, 16, kBlockBytes), sdesc_sw128(qa, 16, 1024),
-                 idesc_qk, k > 0);
-        }
-        mma_commit(&ctl->empty[sk]);                   // K(n) read, S^T(n) ready
-        return true;
-      };
-      bool ok = mbar_wait(&ctl->q_full, 0, a.status, abort_flag) && issue_qk(0);
-      for (int n = 0; ok && n < N; ++n) {
-        // S^T(n + 1) may reuse buffer (n + 1) % 2: softmax(n - 1) finished with it before
-        // PV(n - 1) was issued
-        if (n + 1 < N && !issue_qk(n + 1)) break;
-        // O^T[d half h] += V^T P^T over both V units (blocks 0-7, 8-15)
-        const int u = unit_v(n, N), sv = u % kPairs;
-        if (!mbar_wait(&ctl->p_full[n & 1], (n >> 1) & 1, a.status, abort_flag) ||
-            !mbar_wait(&ctl->full[0][sv], (u / kPairs) & 1, a.status, abort_flag) ||
-            !mbar_wait(&ctl->full[1][sv], (u / kPairs) & 1, a.status, abort_flag))
-          break;
-        tc_fence_after();
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {             // 16 key rows = 2 blocks per step
-            const uint32_t va = ring_addr + sv * kPairBytes + h * 2048 + ks * 2 * kBlockBytes;
-            const uint32_t pa = p_addr + (n & 1) * kPBytes + (ks >> 2) * (kN * 128) + (ks & 3) * 32;
-            mma_ss(tmem + 32 + 32 * h, sdesc_sw128(va, 1024, kBlockBytes),
-                   sdesc_sw128(pa, 16, 1024), idesc_pv, (n > 0 || ks > 0));
+          for (int k = 0; k < 16; ++k) {               // chunk k / 4, 16 columns (k % 4)
+            const uint32_t ka = ring_addr + sk * kPairBytes + (k >> 2) * 1024 + (k & 3) * 32;
+            const uint32_t qa = q_addr + (k >> 2) * (kN * 128) + (k & 3) * 32;
+            mma_ss(tmem + s_col(gt + n), sdesc_sw128(ka, 16, kBlockBytes),
+                   sdesc_sw128(qa, 16, 1024), idesc_qk, k > 0);
           }
+          mma_commit(&ctl->empty[sk]);                 // K(n) read, S^T(n) ready
+          if (n == N - 1) mma_commit(&ctl->q_empty);   // the job's Q is no longer read
+          return true;
+        };
+        ok = mbar_wait(&ctl->q_full, jq & 1, a.status, abort_flag) && issue_qk(0);
+        for (int n = 0; ok && n < N; ++n) {
+          const int g = gt + n;
+          // S^T(n + 1) may reuse buffer (g + 1) % 2: softmax(g - 1) finished with it before
+          // PV(g - 1) was issued
+          if (n + 1 < N && !issue_qk(n + 1)) {
+            ok = false;
+            break;
+          }
+          // O^T[d half h] += V^T P^T over both V units (blocks 0-7, 8-15); the first PV of a
+          // job overwrites O^T, once the previous job's epilogue has read it
+          const int u = U + unit_v(n, N), sv = u % kPairs;
+          if (!mbar_wait(&ctl->p_full[g & 1], (g >> 1) & 1, a.status, abort_flag) ||
+              !mbar_wait(&ctl->full[0][sv], (u / kPairs) & 1, a.status, abort_flag) ||
+              !mbar_wait(&ctl->full[1][sv], (u / kPairs) & 1, a.status, abort_flag) ||
+              (n == 0 && jq > 0 &&
+               !mbar_wait(&ctl->o_empty, (jq - 1) & 1, a.status, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {           // 16 key rows = 2 blocks per step
+              const uint32_t va = ring_addr + sv * kPairBytes + h * 2048 + ks * 2 * kBlockBytes;
+              const uint32_t pa = p_addr + (g & 1) * kPBytes + (ks >> 2) * (kN * 128) + (ks & 3) * 32;
+              mma_ss(tmem + 32 + 32 * h, sdesc_sw128(va, 1024, kBlockBytes),
+                     sdesc_sw128(pa, 16, 1024), idesc_pv, (n > 0 || ks > 0));
+            }
+          }
+          mma_commit(&ctl->empty[sv]);
+          mma_commit(&ctl->pv_done[g & 1]);
+          if (n == N - 1) mma_commit(&ctl->o_full);
         }
-        mma_commit(&ctl->empty[sv]);
-        mma_commit(&ctl->pv_done[n & 1]);
-        if (n == N - 1) mma_commit(&ctl->o_full);
+        U += kUnitsPerTile * N;
+        gt += N;
+        ++jq;
       }
     }
   } else if (warp >= 4) {
@@ -379,111 +434,133 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const float sl2 = a.scale_log2;
     const int ord_ninf = f2ord(-INFINITY);
-    // Column bookkeeping is spread over the lanes: lane c of every warp keeps the running
-    // maximum of S^T column c (query head c % 16 of KV head g0 + c / 16); each warp holds
-    // an identical copy.  Rows read their 16 columns' values by shuffles, so the per-tile
-    // code stays short.
-    float m_c = -INFINITY;
-    float l[kGroupCols];
+    int gt = 0, jq = 0;
+    bool alive = true;
+    for (int jj = blockIdx.x; alive && jj < jobs; jj += gridDim.x) {
+      const int t = jj / a.pairs, g0 = 2 * (jj % a.pairs);
+      const bool two = g0 + 1 < a.Hkv;
+      const int nblk = __ldg(a.indptr + t + 1) - __ldg(a.indptr + t);
+      const int N = nblk > 0 ? (nblk + kBlocksPerTile - 1) / kBlocksPerTile : 0;
+      // Column bookkeeping is spread over the lanes: lane c of every warp keeps the running
+      // maximum of S^T column c (query head c % 16 of KV head g0 + c / 16); each warp holds
+      // an identical copy.  Rows read their 16 columns' values by shuffles, so the per-tile
+      // code stays short.
+      float m_c = -INFINITY;
+      float l[kGroupCols];
 #pragma unroll
-    for (int h = 0; h < kGroupCols; ++h) l[h] = 0.f;
-    // The four softmax warps meet at named barriers every tile, so they must take the same
-    // path through the loop: a failed wait does not leave the loop at once but is carried
-    // in `ok` to the tile's first barrier, whose reduction tells every warp to leave together.
-    for (int n = 0; n < N; ++n) {
-      const int uk = unit_k(n);                        // S^T(n) ready = K(n)'s slot released
-      bool ok = mbar_wait_warp(&ctl->empty[uk % kPairs], (uk / kPairs) & 1, a.status, abort_flag);
-      uint32_t sv[kN];
-      if (ok) {
-        tc_fence_after();
-        tmem_ld32(tmem + lane_base + s_col(n), sv);
-        tmem_ld_wait();
-      }
-      ok = ok && mbar_wait_warp(&ctl->tab_full[n % kTabBufs], (n / kTabBufs) & 1, a.status,
-                                abort_flag);
-      const int code = ok ? ctl->tab[n % kTabBufs][r] : kDeadZero;
-      const bool valid = code == kLive;
-      float x[kGroupCols];
-#pragma unroll
-      for (int h = 0; h < kGroupCols; ++h)
-        x[h] = (valid && h < G) ? __uint_as_float(gg ? sv[kGroupCols + h] : sv[h]) * sl2 : -INFINITY;
-      if (named_bar_or(1, 128, !ok)) break;            // some warp failed: all leave
-      // The running maxima change only when some score exceeds them by the rescale threshold,
-      // which after the first tile is rare: test for that first and compute the exact
-      // column maxima of the tile only when it happens.
-      bool exceed = false;
-#pragma unroll
-      for (int h = 0; h < kGroupCols; ++h)
-        exceed |= x[h] > __shfl_sync(0xffffffffu, m_c, gg * kGroupCols + h) + kRescaleThreshold;
-      float alpha_c = 1.f;
-      if (named_bar_or(1, 128, exceed)) {
-        float* red = reinterpret_cast<float*>(ctl->red[wq]);
-#pragma unroll
-        for (int h = 0; h < kGroupCols; ++h) {
-          const int v = f2ord(x[h]);
-          const int m0 = __reduce_max_sync(0xffffffffu, gg == 0 ? v : ord_ninf);
-          const int m1 = __reduce_max_sync(0xffffffffu, gg == 1 ? v : ord_ninf);
-          if (lane == 0) {
-            red[h] = ord2f(m0);
-            red[kGroupCols + h] = ord2f(m1);
-          }
-        }
-        named_bar(1, 128);
-        const float* rd = reinterpret_cast<const float*>(ctl->red);
-        const float M =
-            fmaxf(fmaxf(rd[lane], rd[kN + lane]), fmaxf(rd[2 * kN + lane], rd[3 * kN + lane]));
-        if (M > m_c + kRescaleThreshold || (m_c == -INFINITY && M > -INFINITY)) {
-          alpha_c = m_c == -INFINITY ? 0.f : fast_exp2(m_c - M);
-          m_c = M;
-        }
-      }
-      const bool need = __any_sync(0xffffffffu, alpha_c != 1.f);
-      const float mu_c = m_c == -INFINITY ? 0.f : m_c;
-      // P^T buffer n % 2 was read by PV(n - 2), which must have completed.  From here on a
-      // failure skips the rest of the tile; the next tile's first barrier ends the loop.
-      ok = n <= 1 || mbar_wait_warp(&ctl->pv_done[n & 1], ((n - 2) >> 1) & 1, a.status, abort_flag);
-      if (ok) {
-        // P^T [32 columns][128 rows], two K-major 64-row chunks with the 128-byte swizzle;
-        // this thread writes its own group's 16 columns, the other group's stay zero
-        uint8_t* prow = p_s + (n & 1) * kPBytes + (r >> 6) * (kN * 128);
-        const int rr = r & 63;
-#pragma unroll
-        for (int h = 0; h < kGroupCols; ++h) {
-          const int c = gg * kGroupCols + h;
-          const float mu = __shfl_sync(0xffffffffu, mu_c, c);
-          const float ac = __shfl_sync(0xffffffffu, alpha_c, c);
-          const float pv = fast_exp2(x[h] - mu);
-          l[h] = l[h] * ac + pv;
-          *reinterpret_cast<__nv_bfloat16*>(prow + c * 128 + ((((rr >> 3) ^ (c & 7)) & 7) << 4) +
-                                            (rr & 7) * 2) = __float2bfloat16_rn(pv);
-        }
-        if (code == kDeadLoaded)
-          ok = zero_dead_v_row(ctl, ring, unit_v(n, N), r, a.status, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-      }
-      if (ok && n > 0 && need) {
-        // O^T is accumulated by PV(n - 1): it must have completed before the rescale
-        ok = mbar_wait_warp(&ctl->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, a.status, abort_flag);
+      for (int h = 0; h < kGroupCols; ++h) l[h] = 0.f;
+      // The four softmax warps meet at named barriers every tile, so they must take the same
+      // path through the loop: a failed wait does not leave the loop at once but is carried
+      // in `ok` to the tile's first barrier, whose reduction tells every warp to leave
+      // together.
+      for (int n = 0; n < N; ++n) {
+        const int g = gt + n;
+        const int uk = 2 * gt + unit_k(n);             // S^T(n) ready = K(n)'s slot released
+        bool ok = mbar_wait_warp(&ctl->empty[uk % kPairs], (uk / kPairs) & 1, a.status, abort_flag);
+        uint32_t sv[kN];
         if (ok) {
           tc_fence_after();
-          rescale_o(tmem + lane_base + 32, alpha_c);
+          tmem_ld32(tmem + lane_base + s_col(g), sv);
+          tmem_ld_wait();
         }
+        ok = ok && mbar_wait_warp(&ctl->tab_full[g % kTabBufs], (g / kTabBufs) & 1, a.status,
+                                  abort_flag);
+        const int code = ok ? ctl->tab[g % kTabBufs][r] : kDeadZero;
+        const bool valid = code == kLive;
+        float x[kGroupCols];
+#pragma unroll
+        for (int h = 0; h < kGroupCols; ++h)
+          x[h] = (valid && h < G) ? __uint_as_float(gg ? sv[kGroupCols + h] : sv[h]) * sl2 : -INFINITY;
+        if (named_bar_or(1, 128, !ok)) {               // some warp failed: all leave
+          alive = false;
+          break;
+        }
+        // The running maxima change only when some score exceeds them by the rescale
+        // threshold, which after the first tile is rare: test for that first and compute the
+        // exact column maxima of the tile only when it happens.
+        bool exceed = false;
+#pragma unroll
+        for (int h = 0; h < kGroupCols; ++h)
+          exceed |= x[h] > __shfl_sync(0xffffffffu, m_c, gg * kGroupCols + h) + kRescaleThreshold;
+        float alpha_c = 1.f;
+        if (named_bar_or(1, 128, exceed)) {
+          float* red = reinterpret_cast<float*>(ctl->red[wq]);
+#pragma unroll
+          for (int h = 0; h < kGroupCols; ++h) {
+            const int v = f2ord(x[h]);
+            const int m0 = __reduce_max_sync(0xffffffffu, gg == 0 ? v : ord_ninf);
+            const int m1 = __reduce_max_sync(0xffffffffu, gg == 1 ? v : ord_ninf);
+            if (lane == 0) {
+              red[h] = ord2f(m0);
+              red[kGroupCols + h] = ord2f(m1);
+            }
+          }
+          named_bar(1, 128);
+          const float* rd = reinterpret_cast<const float*>(ctl->red);
+          const float M =
+              fmaxf(fmaxf(rd[lane], rd[kN + lane]), fmaxf(rd[2 * kN + lane], rd[3 * kN + lane]));
+          if (M > m_c + kRescaleThreshold || (m_c == -INFINITY && M > -INFINITY)) {
+            alpha_c = m_c == -INFINITY ? 0.f : fast_exp2(m_c - M);
+            m_c = M;
+          }
+        }
+        const bool need = __any_sync(0xffffffffu, alpha_c != 1.f);
+        const float mu_c = m_c == -INFINITY ? 0.f : m_c;
+        // P^T buffer g % 2 was read by PV(g - 2), which must have completed.  From here on
+        // a failure skips the rest of the tile; the next tile's first barrier ends the loop.
+        ok = g <= 1 || mbar_wait_warp(&ctl->pv_done[g & 1], ((g - 2) >> 1) & 1, a.status, abort_flag);
+        if (ok) {
+          // P^T [32 columns][128 rows], two K-major 64-row chunks with the 128-byte swizzle;
+          // this thread writes its own group's 16 columns, the other group's stay zero
+          uint8_t* prow = p_s + (g & 1) * kPBytes + (r >> 6) * (kN * 128);
+          const int rr = r & 63;
+#pragma unroll
+          for (int h = 0; h < kGroupCols; ++h) {
+            const int c = gg * kGroupCols + h;
+            const float mu = __shfl_sync(0xffffffffu, mu_c, c);
+            const float ac = __shfl_sync(0xffffffffu, alpha_c, c);
+            const float pv = fast_exp2(x[h] - mu);
+            l[h] = l[h] * ac + pv;
+            *reinterpret_cast<__nv_bfloat16*>(prow + c * 128 + ((((rr >> 3) ^ (c & 7)) & 7) << 4) +
+                                              (rr & 7) * 2) = __float2bfloat16_rn(pv);
+          }
+          if (code == kDeadLoaded)
+            ok = zero_dead_v_row(ctl, ring, 2 * gt + unit_v(n, N), r, a.status, abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok && n > 0 && need) {
+          // O^T is accumulated by PV(g - 1): it must have completed before the rescale
+          ok = mbar_wait_warp(&ctl->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, a.status, abort_flag);
+          if (ok) {
+            tc_fence_after();
+            rescale_o(tmem + lane_base + 32, alpha_c);
+          }
+        }
+        fence_proxy_async_smem();   // P^T and zeroed V rows (generic) -> tensor-core reads
+        tc_fence_before();
+        mbar_arrive(&ctl->p_full[g & 1]);
       }
-      fence_proxy_async_smem();   // P^T and zeroed V rows (generic) -> tensor-core reads
-      tc_fence_before();
-      mbar_arrive(&ctl->p_full[n & 1]);
-    }
-    // ---- epilogue: column sums, normalise, write out / out_fp32 / lse ---------------------
+      if (!alive) break;
+      // ---- epilogue: column sums, normalise, write out / out_fp32 / lse -------------------
+      named_bar(1, 128);            // every warp has read the previous job's sums
 #pragma unroll
-    for (int h = 0; h < kGroupCols; ++h) {
-      float v = l[h];
+      for (int h = 0; h < kGroupCols; ++h) {
+        float v = l[h];
 #pragma unroll
-      for (int o = 2; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);   // same group
-      if (lane < 2) ctl->lred[wq][lane * kGroupCols + h] = v;
+        for (int o = 2; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);   // same group
+        if (lane < 2) ctl->lred[wq][lane * kGroupCols + h] = v;
+      }
+      named_bar(1, 128);
+      const bool have_o = N > 0 && mbar_wait_warp(&ctl->o_full, jq & 1, a.status, abort_flag);
+      write_output(a, ctl, tmem + lane_base + 32, have_o, t, g0, two, r, lane, m_c);
+      if (N > 0) {
+        // O^T has been read into registers: the next job's first PV may overwrite it
+        tc_fence_before();
+        mbar_arrive(&ctl->o_empty);
+        gt += N;
+        ++jq;
+      }
     }
-    named_bar(1, 128);
-    const bool have_o = N > 0 && mbar_wait_warp(&ctl->o_full, 0, a.status, abort_flag);
-    write_output(a, ctl, tmem + lane_base + 32, have_o, t, g0, two, r, lane, m_c);
   }
   tc_fence_before();
   __syncthreads();
@@ -538,7 +615,11 @@ int launch_qsa(const paged_attn_params* p, const paged_attn_meta* m, const void*
   a.scale_log2 = p->sm_scale * 1.4426950408889634f;
   void* tok;
   timer_begin(st, &tok);
-  qsa_kernel<<<static_cast<unsigned>(units), kThreads, kSmemBytes, st>>>(qmap, kmap, vmap, a);
+  // persistent: one CTA per SM walks the (token, KV-head pair) jobs
+  const int sms = current_sm_count();
+  if (sms <= 0) return PAGED_ATTN_ERR_CUDA;
+  const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
+  qsa_kernel<<<grid, kThreads, kSmemBytes, st>>>(qmap, kmap, vmap, a);
   timer_end(st, tok);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? PAGED_ATTN_OK : PAGED_ATTN_ERR_CUDA;
