@@ -148,44 +148,47 @@ __device__ __noinline__ void rescale_o(uint32_t taddr, float alpha_c) {
 }
 
 // Normalise and store this thread's d rows (r, r + 128) of every live column; lane c holds
-// the running maximum of column c.
-__device__ __noinline__ void write_output(const QsaLaunch& a, const QsaCtrl* ctl, uint32_t taddr,
-                                          bool have_o, int t, int g0, bool two, int r, int lane,
-                                          float m_c) {
+// the running maximum of column c.  Both O^T halves come in with two 32-column TMEM loads
+// and one wait; the scalars of the launch are passed by value so that they stay in
+// registers (a reference to the kernel parameter would place it in local memory).
+__device__ __forceinline__ void write_output(__nv_bfloat16* __restrict__ out,
+                                             float* __restrict__ out32, float* __restrict__ lse,
+                                             int Hq, int G, int T, const QsaCtrl* ctl,
+                                             uint32_t taddr, bool have_o, int t, int g0,
+                                             bool two, int r, int lane, float m_c) {
   const float L_c = ctl->lred[0][lane] + ctl->lred[1][lane] + ctl->lred[2][lane] +
                     ctl->lred[3][lane];
   const float inv_c = L_c > 0.f ? 1.f / L_c : 0.f;
-  if (have_o) tc_fence_after();
-  const long long row0 = static_cast<long long>(t) * a.Hq * kD + r;
-#pragma unroll 1
-  for (int c0 = 0; c0 < kN; c0 += 4) {
-    uint32_t o0[4] = {0u, 0u, 0u, 0u}, o1[4] = {0u, 0u, 0u, 0u};
-    if (have_o) {
-      tmem_ld4(taddr + c0, o0);
-      tmem_ld4(taddr + 32 + c0, o1);
-      tmem_ld_wait();
-    }
+  uint32_t o0[kN], o1[kN];
+  if (have_o) {
+    tc_fence_after();
+    tmem_ld32(taddr, o0);
+    tmem_ld32(taddr + 32, o1);
+    tmem_ld_wait();
+  } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int c = c0 + e;
-      const float inv = __shfl_sync(0xffffffffu, inv_c, c);
-      const int gq = c / kGroupCols, h = c % kGroupCols;
-      if (h >= a.G || (gq == 1 && !two)) continue;
-      const float v0 = __uint_as_float(o0[e]) * inv;
-      const float v1 = __uint_as_float(o1[e]) * inv;
-      const long long o = row0 + static_cast<long long>((g0 + gq) * a.G + h) * kD;
-      a.out[o] = __float2bfloat16_rn(v0);
-      a.out[o + 128] = __float2bfloat16_rn(v1);
-      if (a.out32) {
-        a.out32[o] = v0;
-        a.out32[o + 128] = v1;
-      }
+    for (int c = 0; c < kN; ++c) o0[c] = o1[c] = 0u;
+  }
+  const long long row0 = static_cast<long long>(t) * Hq * kD + r;
+#pragma unroll
+  for (int c = 0; c < kN; ++c) {
+    const float inv = __shfl_sync(0xffffffffu, inv_c, c);
+    const int gq = c / kGroupCols, h = c % kGroupCols;
+    if (h >= G || (gq == 1 && !two)) continue;
+    const float v0 = __uint_as_float(o0[c]) * inv;
+    const float v1 = __uint_as_float(o1[c]) * inv;
+    const long long o = row0 + static_cast<long long>((g0 + gq) * G + h) * kD;
+    out[o] = __float2bfloat16_rn(v0);
+    out[o + 128] = __float2bfloat16_rn(v1);
+    if (out32) {
+      out32[o] = v0;
+      out32[o + 128] = v1;
     }
   }
   // lse of column c from lane c of the first warp
   const int gq = lane / kGroupCols, h = lane % kGroupCols;
-  if (r == lane && a.lse && h < a.G && (gq == 0 || two))
-    a.lse[static_cast<long long>((g0 + gq) * a.G + h) * a.T + t] =
+  if (r == lane && lse && h < G && (gq == 0 || two))
+    lse[static_cast<long long>((g0 + gq) * G + h) * T + t] =
         L_c > 0.f ? (m_c + fast_log2(L_c)) * kLn2 : -INFINITY;
 }
 
@@ -552,7 +555,8 @@ qsa_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUt
       }
       named_bar(1, 128);
       const bool have_o = N > 0 && mbar_wait_warp(&ctl->o_full, jq & 1, a.status, abort_flag);
-      write_output(a, ctl, tmem + lane_base + 32, have_o, t, g0, two, r, lane, m_c);
+      write_output(a.out, a.out32, a.lse, a.Hq, G, a.T, ctl, tmem + lane_base + 32, have_o, t,
+                   g0, two, r, lane, m_c);
       if (N > 0) {
         // O^T has been read into registers: the next job's first PV may overwrite it
         tc_fence_before();
