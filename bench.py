@@ -246,6 +246,17 @@ def sage_pairs(p):
 # one workload on the GPU
 # ----------------------------------------------------------------------------------------
 
+def main_kernel(p):
+    """Name of the kernel that does the attention arithmetic of workload p."""
+    if p["form"] == "decode":
+        return "decode_split_kernel"
+    if p["form"] in ("qsa", "qsa_indexed"):
+        return "qsa_kernel"
+    if p["form"] == "prefill" and p["q"].shape[-1] == 256:
+        return "attn256_kernel"
+    return "attn_tc_kernel"
+
+
 def make_workload(name):
     if name == "decode_b64":
         return W.decode_b64()
@@ -825,9 +836,7 @@ def main():
                  "qsa_indexed": qsa_indexed_pairs, "sage": sage_pairs}[p["form"]](p)
         units *= 4 * (p["q"] if "q" in p else p["q_int8"]).shape[-1]
         unit, scale = "TFLOP/s", 1e12
-        kernel = "qsa_kernel" if p["form"] in ("qsa", "qsa_indexed") else "attn_tc_kernel"
-        if p["form"] == "prefill" and p["q"].shape[-1] == 256:
-            kernel = "attn256_kernel"
+        kernel = main_kernel(p)
         bound, peak = "tensor", pk["bf16_tflops"]
     value = job_rate(units, world, ms_step, scale)
     achieved = units / (kernel_ms * 1e-3) / scale
@@ -887,7 +896,9 @@ def main():
                     extra[name] = {"gbs_step": nb / (reg / steps * 1e-3) / 1e9,
                                    "gbs_kernel": nb / (kms * 1e-3) / 1e9,
                                    "frac_hbm_peak": nb / (kms * 1e-3) / 1e9 / pk["hbm_gbs"],
-                                   "ms_step": reg / steps, "ms_kernel": kms, "kv_bytes": nb}
+                                   "ms_step": reg / steps, "ms_kernel": kms, "kv_bytes": nb,
+                                   "kernel": main_kernel(q),
+                                   "traffic": recorded_traffic(main_kernel(q), name)}
                     del rr
                     torch.cuda.empty_cache()
                     if not args.skip_cpu:
@@ -903,7 +914,9 @@ def main():
                                "frac_bf16_sustained": tk / pk.get("bf16_tflops_sustained",
                                                                   pk["bf16_tflops"]),
                                "ms_step": reg / steps, "ms_kernel": kms,
-                               "visible_pairs": n, "flops": flops}
+                               "visible_pairs": n, "flops": flops,
+                               "kernel": main_kernel(q),
+                               "traffic": recorded_traffic(main_kernel(q), name)}
                 if q["form"] in ("qsa", "qsa_indexed"):
                     if l2_gbs is None:
                         l2_gbs = l2_read_gbs(dev)
