@@ -740,10 +740,13 @@ int paged_prefill_run(const paged_prefill_params* p, const void* q, const void* 
                    at<int>(ws, s.offs), st);
   const float scale = p->sm_scale > 0.f ? p->sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
   AttnLaunch a{};
-  const int R = page_piece_rows(ps, D == 256 ? 64 : kKvTile);   // keys per KV tile: 64 / 128
+  // keys per page piece of a copy: 128-key tiles; the D = 256 kernel copies V 32 keys at a time
+  const int RK = page_piece_rows(ps, kKvTile);
+  const int RV = page_piece_rows(ps, D == 256 ? 32 : kKvTile);
   const long long pool_rows = static_cast<long long>(p->num_pages) * Hkv * ps;
   if (!encode_q_map(&a.qmap, q, p->total_q, Hq, D, G, sub_tile_tokens(G)) ||
-      !encode_rows_map(&a.kmap, kc, pool_rows, D, R) || !encode_rows_map(&a.vmap, vc, pool_rows, D, R))
+      !encode_rows_map(&a.kmap, kc, pool_rows, D, RK) ||
+      !encode_rows_map(&a.vmap, vc, pool_rows, D, RV))
     return PAGED_ATTN_ERR_CUDA;
   a.tiles = sorted;
   a.n_tiles = n_tiles;

@@ -4,18 +4,21 @@
 // Persistent: one CTA per SM walks the prefill planner's tile list (largest first) with a
 // stride of the grid size.  A work tile is one Q sub-tile of 128 rows, a row being a
 // (token, head-in-group) pair, so the G query heads that share a KV head share every K/V
-// tile.  K and V are walked in 64-key tiles over the keys the tile's rows can see.
+// tile.  K and V are walked in 128-key tiles over the keys the tile's rows can see, so that
+// the score MMA runs at N = 128 (an M = 128 MMA costs the same for any N up to 128).
 // Roles (224 threads):
 //   warps 0-3  softmax + epilogue (thread t <-> TMEM lane t <-> row t)
-//   warp  4    TMA producer of Q (once per work tile) and K (2-stage ring)
+//   warp  4    TMA producer of Q (once per work tile) and K
 //   warp  5    TMEM owner and MMA issuer (one thread)
-//   warp  6    TMA producer of V (2-stage ring)
-// Tensor memory (512 columns allocated): S_0 [0,64) S_1 [64,128) O [128,384).  The scores of
-// KV tile i (counted over the whole launch) land in S_(i%2); P is written over the first 32
-// columns of that buffer as packed bf16 and read from TMEM by the PV MMA.  The MMA issuer
-// queues QK(i+2) behind PV(i), so the softmax of tile i+1 runs while PV(i) and QK(i+2) do.
-// Per 64-key tile the MMAs take 2 x 128 x 64 x 256 multiply-adds and the softmax 64 exp2 per
-// row, so one softmax warpgroup keeps up with the tensor core.
+//   warp  6    TMA producer of V
+// Tensor memory (512 columns): S_0 [0,128) S_1 [128,256) O [256,512).  The scores of KV tile
+// i (counted over the whole launch) land in S_(i%2); P is written over the first 64 columns
+// of that buffer as packed bf16 and read from TMEM by the PV MMA.  The MMA issuer queues
+// QK(i+2) behind PV(i), so the softmax of tile i+1 runs while PV(i) and QK(i+2) do.
+// A whole 128-key K or V tile (64 KB) does not fit twice beside Q, so both stream through
+// rings of 16 KB chunks: K in 64-column chunks (128 keys x 64 dims: the score MMA's k-steps
+// over those dims need nothing else), V in 32-key chunks (32 keys x 256 dims: two k-steps of
+// the PV MMA).  Each chunk is released as soon as its MMAs have read it.
 // The online softmax runs in the log2 domain; the running maximum only moves (and O is
 // rescaled in TMEM) when a tile's maximum exceeds it by more than 8.
 #include <cstdint>
@@ -28,45 +31,50 @@ namespace pa {
 namespace {
 
 constexpr int kD = 256;
-constexpr int kKeys = 64;                      // keys per KV tile
+constexpr int kKeys = 128;                     // keys per KV tile
 constexpr int kChunks = kD / 64;               // 64-column (128-byte) chunks of a row
 constexpr int kRows = 128;                     // rows of a Q sub-tile
 constexpr int kQChunk = kRows * 128;           // 128 rows x 64 columns of bf16
 constexpr int kQBytes = kChunks * kQChunk;     // 64 KB
-constexpr int kKvChunk = kKeys * 128;          // 64 keys x 64 columns
-constexpr int kKvBytes = kChunks * kKvChunk;   // 32 KB per K (or V) tile
-constexpr int kKStages = 2;
-constexpr int kVStages = 2;
+// K ring slot: 128 keys x 64 columns (one 128-byte-swizzled block, 16 KB)
+constexpr int kKSlotBytes = kKeys * 128;
+// V ring slot: 32 keys x 256 columns as four 32 x 64 blocks (4 KB each), 16 KB
+constexpr int kVKeys = 32;
+constexpr int kVBlock = kVKeys * 128;
+constexpr int kVSlotBytes = kChunks * kVBlock;
+constexpr int kVChunks = kKeys / kVKeys;       // V chunks per KV tile
+constexpr int kKSlots = 5;
+constexpr int kVSlots = 5;
 constexpr int kProdK = 4, kMmaWarp = 5, kProdV = 6;
 constexpr int kThreads = 7 * 32;
-constexpr int kTmemS = 0;                      // S_0, S_1: 64 columns each
-constexpr int kTmemO = 128;                    // O: 256 columns
+constexpr int kTmemS = 0;                      // S_0, S_1: 128 columns each
+constexpr int kTmemO = 256;                    // O: 256 columns
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct Ctrl {
   uint64_t q_full, q_empty;
-  uint64_t k_full[kKStages], k_empty[kKStages];
-  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t k_full[kKSlots], k_empty[kKSlots];
+  uint64_t v_full[kVSlots], v_empty[kVSlots];
   uint64_t s_full[2], p_full[2];
-  uint64_t pv_done, o_final, o_empty;
+  uint64_t o_final, o_empty;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-constexpr int kSmemBytes =
-    kQBytes + (kKStages + kVStages) * kKvBytes + static_cast<int>(sizeof(Ctrl)) + 1024;
+constexpr int kSmemBytes = kQBytes + kKSlots * kKSlotBytes + kVSlots * kVSlotBytes +
+                           static_cast<int>(sizeof(Ctrl)) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // One work tile as every role sees it.
 struct Tile {
   int b, g, tok0, ntok, q_row0, L, nq;
-  int kt0, N;          // 64-key tiles kt0 .. kt0 + N - 1
+  int kt0, N;          // 128-key tiles kt0 .. kt0 + N - 1
 };
 
 // The keys the tile's rows can see are [lo, hi): hi = min(L, p(last row) + 1) under the
 // causal mask (L otherwise) and lo = max(0, p(first row) - window_left) with a window, where
-// p(token i) = L - nq + i.  They are walked in 64-key tiles.
+// p(token i) = L - nq + i.  They are walked in 128-key tiles.
 // L and nq are request b's KV length and query count.
 __device__ __forceinline__ Tile tile_from_parts(const AttnLaunch& a, const TileRec& r, int L,
                                                 int nq) {
@@ -110,8 +118,8 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   extern __shared__ uint8_t smem_raw[];
   uint8_t* q_s = smem_align<1024>(smem_raw);
   uint8_t* k_s = q_s + kQBytes;
-  uint8_t* v_s = k_s + kKStages * kKvBytes;
-  Ctrl* ctl = reinterpret_cast<Ctrl*>(v_s + kVStages * kKvBytes);
+  uint8_t* v_s = k_s + kKSlots * kKSlotBytes;
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(v_s + kVSlots * kVSlotBytes);
 
   const int n_live = a.n_tiles ? *a.n_tiles : a.capacity;
   if (static_cast<int>(blockIdx.x) >= n_live) return;
@@ -121,19 +129,18 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   if (threadIdx.x == 0) {
     mbar_init(&ctl->q_full, 1);
     mbar_init(&ctl->q_empty, 1);
-    for (int s = 0; s < kKStages; ++s) {
+    for (int s = 0; s < kKSlots; ++s) {
       mbar_init(&ctl->k_full[s], 1);
       mbar_init(&ctl->k_empty[s], 1);
     }
-    for (int s = 0; s < kVStages; ++s) {
+    for (int s = 0; s < kVSlots; ++s) {
       mbar_init(&ctl->v_full[s], 1);
       mbar_init(&ctl->v_empty[s], 1);
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&ctl->s_full[w], 1);
-      mbar_init(&ctl->p_full[w], kRows);
+      mbar_init(&ctl->p_full[w], 4);           // one arrival per softmax warp
     }
-    mbar_init(&ctl->pv_done, 1);
     mbar_init(&ctl->o_final, 1);
     mbar_init(&ctl->o_empty, kRows);
     // a launch that an earlier CTA already broke does nothing
@@ -154,8 +161,11 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // nothing to do; fall through to the teardown
   } else if (warp == kProdK || warp == kProdV) {
     // =============================== producers =========================================
-    // warp 4 copies Q (lane 0) and K, warp 6 copies V; lane p copies page piece p of a tile
-    // (R keys of one page, one TMA box per 64-column chunk)
+    // warp 4 copies Q (lane 0) and K, warp 6 copies V.  Lane p owns page piece p of a KV tile
+    // (R keys of one page; its page id is loaded once per tile, while the tile before is
+    // copied).  A K chunk is
+    // one 64-column block of the tile: every piece.  A V chunk is 32 keys of the tile in all
+    // four 64-column blocks: the pieces that fall in it.
     const bool is_k = warp == kProdK;
     if (lane == 0) {
       if (is_k) {
@@ -166,22 +176,28 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       }
     }
     const int ps = a.page_size;
-    const int R = page_piece_rows(ps, kKeys);
-    const int pieces = kKeys / R;
-    const int stages = is_k ? kKStages : kVStages;
+    const int R = is_k ? page_piece_rows(ps, kKeys) : page_piece_rows(ps, kVKeys);
+    const int pieces = kKeys / R;                // per KV tile (at most 16)
+    const int my_chunk = (lane * R) / kVKeys;    // V: the chunk this lane's piece falls in
+    const int slots = is_k ? kKSlots : kVSlots;
     uint8_t* ring = is_k ? k_s : v_s;
+    const int slot_bytes = is_k ? kKSlotBytes : kVSlotBytes;
     uint64_t* full = is_k ? ctl->k_full : ctl->v_full;
     uint64_t* empty = is_k ? ctl->k_empty : ctl->v_empty;
     const CUtensorMap* map = is_k ? &kmap : &vmap;
     const int head_off = is_k ? a.k_head_off : a.v_head_off;
-    int kv_it = 0, qcount = 0, issued = 0;
+    // chunks per KV tile: the four column blocks of K, or the four 32-key parts of V
+    constexpr int kPerTile = kChunks;
+    static_assert(kVChunks == kChunks, "four K chunks and four V chunks per KV tile");
+    int ch = 0, qcount = 0;                      // chunks issued (over the launch), Q loads
     bool ok = true;
     for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
       const Tile t = make_tile(a, a.tiles[idx]);
       if (t.N == 0) continue;
       const int* pt = a.pt_indptr ? a.pt + __ldg(a.pt_indptr + t.b)
                                   : a.pt + static_cast<long long>(t.b) * a.pt_stride;
-      auto key_of = [&](int n) {                 // first key of this lane's piece, or -1
+      // first key of this lane's piece of KV tile n, or -1
+      auto key_of = [&](int n) {
         const int key = (t.kt0 + n) * kKeys + lane * R;
         return (lane < pieces && key < t.L) ? key : -1;
       };
@@ -201,39 +217,49 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
         ++qcount;
       }
-      for (int n = 0; n < t.N; ++n) {
-        const int it = kv_it + n, slot = it % stages;
-        if (it >= stages &&
-            !mbar_wait_warp<true>(&empty[slot], ((it / stages) - 1) & 1, a.status, abort_flag)) {
-          ok = false;
-          break;
-        }
+      for (int n = 0; ok && n < t.N; ++n) {
+        // the next KV tile's page id, loaded now: it is first used a whole tile later
+        const int key_nx = n + 1 < t.N ? key_of(n + 1) : -1;
+        const int page_nx = key_nx >= 0 ? __ldg(pt + key_nx / ps) : 0;
         bool live = key >= 0;
         if (live && (page < 0 || page >= a.num_pages)) {
           report_error(a.status, kErrMetadata);
           live = false;
         }
-        const uint32_t nlive = __popc(__ballot_sync(0xffffffffu, live));
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], nlive * R * 128u * kChunks);
-        __syncwarp();
-        if (live) {
-          uint8_t* dst = ring + slot * kKvBytes + static_cast<uint32_t>(lane * R) * 128u;
-          const int row = page * a.page_rows + t.g * ps + key % ps + head_off;
+        const int row = page * a.page_rows + t.g * ps + (key >= 0 ? key % ps : 0) + head_off;
+        for (int j = 0; j < kPerTile; ++j) {
+          const int slot = ch % slots;
+          if (ch >= slots &&
+              !mbar_wait_warp<true>(&empty[slot], ((ch / slots) - 1) & 1, a.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const bool mine = live && (is_k || my_chunk == j);
+          const uint32_t nlive = __popc(__ballot_sync(0xffffffffu, mine));
+          if (lane == 0)
+            mbar_arrive_expect_tx(&full[slot], nlive * R * 128u * (is_k ? 1u : kChunks));
+          __syncwarp();
+          if (mine) {
+            uint8_t* base = ring + slot * slot_bytes;
+            if (is_k) {
+              tma_load_2d(base + static_cast<uint32_t>(lane * R) * 128u, map, &full[slot], j * 64,
+                          row);
+            } else {
+              uint8_t* dst = base + static_cast<uint32_t>(lane * R - j * kVKeys) * 128u;
 #pragma unroll
-          for (int c = 0; c < kChunks; ++c)
-            tma_load_2d(dst + c * kKvChunk, map, &full[slot], c * 64, row);
+              for (int c = 0; c < kChunks; ++c)
+                tma_load_2d(dst + c * kVBlock, map, &full[slot], c * 64, row);
+            }
+          }
+          ++ch;
         }
-        issued = it + 1;
-        if (n + 1 < t.N) {                       // the next tile's page ids
-          key = key_of(n + 1);
-          page = key >= 0 ? __ldg(pt + key / ps) : 0;
-        }
+        key = key_nx;
+        page = page_nx;
       }
-      kv_it += t.N;
     }
     if (!ok && lane == 0) {                      // let copies in flight land before exiting
-      for (int it = issued > stages ? issued - stages : 0; it < issued; ++it)
-        drain_wait(&full[it % stages], (it / stages) & 1);
+      for (int c = ch > slots ? ch - slots : 0; c < ch; ++c)
+        drain_wait(&full[c % slots], (c / slots) & 1);
       if (is_k && qcount > 0) drain_wait(&ctl->q_full, (qcount - 1) & 1);
     }
   } else if (warp == kMmaWarp) {
@@ -245,26 +271,44 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       // address field, which never carries out of it inside shared memory.
       const uint64_t q_desc0 = sdesc_sw128(smem_u32(q_s), 16, 1024);
       const uint64_t k_desc0 = sdesc_sw128(smem_u32(k_s), 16, 1024);
-      const uint64_t v_desc0 = sdesc_sw128(smem_u32(v_s), kKvChunk, 1024);
-      auto issue_qk = [&](int it) {              // S_(it%2) = Q K(it)^T, 16 k-steps of 16
-        const uint64_t kd = k_desc0 + static_cast<uint64_t>(((it % kKStages) * kKvBytes) >> 4);
+      const uint64_t v_desc0 = sdesc_sw128(smem_u32(v_s), kVBlock, 1024);
+      auto wait = [&](uint64_t* bar, int parity) {
+        return mbar_wait_fast(bar, parity, a.status, abort_flag);
+      };
+      int kc = 0, vc = 0;                        // K and V chunks consumed over the launch
+      // S_(it%2) = Q K(it)^T: per 64-column K chunk, the 4 k-steps of 16 columns it holds
+      auto issue_qk = [&](int it) -> bool {
+        for (int c = 0; c < kChunks; ++c, ++kc) {
+          const int slot = kc % kKSlots;
+          if (!wait(&ctl->k_full[slot], (kc / kKSlots) & 1)) return false;
+          tc_fence_after();
+          const uint64_t kd = k_desc0 + static_cast<uint64_t>((slot * kKSlotBytes) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-          const uint32_t qoff = ((ks >> 2) * kQChunk + (ks & 3) * 32) >> 4;
-          const uint32_t koff = ((ks >> 2) * kKvChunk + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + kTmemS + (it & 1) * kKeys, q_desc0 + qoff, kd + koff, idesc_qk, ks > 0);
+          for (int k4 = 0; k4 < 4; ++k4)
+            mma_ss(tmem + kTmemS + (it & 1) * kKeys,
+                   q_desc0 + static_cast<uint64_t>((c * kQChunk + k4 * 32) >> 4),
+                   kd + static_cast<uint64_t>((k4 * 32) >> 4), idesc_qk, c > 0 || k4 > 0);
+          mma_commit(&ctl->k_empty[slot]);
         }
         mma_commit(&ctl->s_full[it & 1]);
+        return true;
       };
-      auto issue_pv = [&](int it, bool acc) {    // O += P(it) V(it), 4 k-steps of 16 keys
-        const uint64_t vd = v_desc0 + static_cast<uint64_t>(((it % kVStages) * kKvBytes) >> 4);
+      // O += P(it) V(it): per 32-key V chunk, its 2 k-steps of 16 keys
+      auto issue_pv = [&](int it, bool acc) -> bool {
+        for (int j = 0; j < kVChunks; ++j, ++vc) {
+          const int slot = vc % kVSlots;
+          if (!wait(&ctl->v_full[slot], (vc / kVSlots) & 1)) return false;
+          tc_fence_after();
+          const uint64_t vd = v_desc0 + static_cast<uint64_t>((slot * kVSlotBytes) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < kKeys / 16; ++ks)
-          mma_ts(tmem + kTmemO, tmem + kTmemS + (it & 1) * kKeys + ks * 8,
-                 vd + ((ks * 16 * 128) >> 4), idesc_pv, acc || ks > 0);
-      };
-      auto wait = [&](uint64_t* bar, int parity) {
-        return mbar_wait<true>(bar, parity, a.status, abort_flag);
+          for (int k2 = 0; k2 < 2; ++k2) {
+            const int ks = 2 * j + k2;
+            mma_ts(tmem + kTmemO, tmem + kTmemS + (it & 1) * kKeys + ks * 8,
+                   vd + static_cast<uint64_t>((k2 * 16 * 128) >> 4), idesc_pv, acc || ks > 0);
+          }
+          mma_commit(&ctl->v_empty[slot]);     // the last one also tells the softmax PV is done
+        }
+        return true;
       };
       int kv_it = 0, qcount = 0, ep = 0;
       bool ok = true;
@@ -279,39 +323,28 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
         ++qcount;
         for (int n = 0; ok && n < 2 && n < N; ++n) {   // the first two score tiles
-          const int it = it0 + n;
-          if (!wait(&ctl->k_full[it % kKStages], (it / kKStages) & 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_qk(it);
-          mma_commit(&ctl->k_empty[it % kKStages]);
-          if (n == N - 1) mma_commit(&ctl->q_empty);
+          ok = issue_qk(it0 + n);
+          if (ok && n == N - 1) mma_commit(&ctl->q_empty);
         }
         for (int n = 0; ok && n < N; ++n) {
-          const int it = it0 + n, vs = it % kVStages;
+          const int it = it0 + n;
           // O is free once the previous work tile's epilogue has read it
-          if (!wait(&ctl->v_full[vs], (it / kVStages) & 1) ||
-              !wait(&ctl->p_full[it & 1], (it >> 1) & 1) ||
+          if (!wait(&ctl->p_full[it & 1], (it >> 1) & 1) ||
               (n == 0 && ep > 0 && !wait(&ctl->o_empty, (ep - 1) & 1))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_pv(it, n > 0);
-          mma_commit(&ctl->pv_done);
-          mma_commit(&ctl->v_empty[vs]);
+          if (!issue_pv(it, n > 0)) {
+            ok = false;
+            break;
+          }
           if (n == N - 1) mma_commit(&ctl->o_final);
           if (n + 2 < N) {                       // QK(it + 2) into the buffer P(it) came from
-            const int it2 = it + 2;
-            if (!wait(&ctl->k_full[it2 % kKStages], (it2 / kKStages) & 1)) {
+            if (!issue_qk(it + 2)) {
               ok = false;
               break;
             }
-            tc_fence_after();
-            issue_qk(it2);
-            mma_commit(&ctl->k_empty[it2 % kKStages]);
             if (n + 2 == N - 1) mma_commit(&ctl->q_empty);
           }
         }
@@ -329,6 +362,21 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int wl = a.window_left;
     int kv_it = 0, ep = 0;
     bool ok = true;
+    // S(it) lands in buffer it % 2, whose next scores (QK(it + 2)) wait for this softmax's P.
+    // PV(j) is complete once it has released V chunk 4 j + 3 (the commit covers every earlier
+    // MMA).  The softmax of tile it asks for PV(it - 1) after it has seen S(it); the parity
+    // wait is sound there because that slot's previous chunk belongs to PV(it - 2), complete
+    // before S(it) (QK(it) was issued after it), and its next one to PV(it) or later, which
+    // waits for this softmax's P.
+    auto s_ready = [&](int it) {
+      return mbar_wait_fast_warp(&ctl->s_full[it & 1], (it >> 1) & 1, a.status, abort_flag);
+    };
+    auto pv_done = [&](int it) {
+      const int c = kVChunks * it + kVChunks - 1;
+      return mbar_wait_warp<true>(&ctl->v_empty[c % kVSlots], (c / kVSlots) & 1, a.status,
+                                  abort_flag);
+    };
+    static_assert(kKSlots >= kChunks && kVSlots >= kVChunks, "ring slots per KV tile");
     // The next work tile's record is read after the current tile's last softmax and its KV
     // length and query count after the wait for O, so a work tile starts without a global
     // round trip.
@@ -349,15 +397,16 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       float m_run = -INFINITY, l_run = 0.f;
       for (int n = 0; n < t.N; ++n) {
         const int it = kv_it + n;
-        if (!mbar_wait_warp<true>(&ctl->s_full[it & 1], (it >> 1) & 1, a.status, abort_flag)) {
+        if (!s_ready(it)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t s_col = tmem + lane_base + kTmemS + (it & 1) * kKeys;
         uint32_t r[kKeys];
-        tmem_ld32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-        tmem_ld32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+#pragma unroll
+        for (int q = 0; q < kKeys / 32; ++q)
+          tmem_ld32(s_col + q * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[q * 32]));
         tmem_ld_wait();
         const int key0 = (t.kt0 + n) * kKeys;
         if (key0 < klo || key0 + kKeys > khi) {
@@ -398,10 +447,11 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           r[j] = pack_bf16(p0, p1);
         }
         tmem_st32(s_col, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_st32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
         l_run = l_run * alpha + ((sa0 + sa1) + (sb0 + sb1));
         if (n > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           // O holds PV of the previous KV tile, which may still run: wait for it, then scale
-          if (!mbar_wait_warp<true>(&ctl->pv_done, (it - 1) & 1, a.status, abort_flag)) {
+          if (!pv_done(it - 1)) {
             ok = false;
             break;
           }
@@ -417,27 +467,42 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           }
         }
         tmem_st_wait();
-        if (key0 + kKeys > t.L) {
+        if (key0 + kKeys > t.L && warp == 0) {
           // Rows of keys past the length hold stale or non-finite data (tail slots of the
-          // last page, or nothing copied); P is 0 there, so make V exactly 0 as well.
-          const int vs = it % kVStages;
-          if (!mbar_wait_warp<true>(&ctl->v_full[vs], (it / kVStages) & 1, a.status,
-                                    abort_flag)) {
+          // last page, or nothing copied); P is 0 there, so make V exactly 0 as well.  V chunk
+          // j of KV tile it is chunk 4 it + j of the launch; lane m clears its key row.
+          // The chunk's ring slot last held a chunk of KV tile it - 1, whose copy may not have
+          // landed yet, and a parity wait for the phase after the barrier's current one
+          // returns at once.  PV(it - 1) waited for every chunk of tile it - 1, so wait for it
+          // first.
+          if (it > 0 && !pv_done(it - 1)) {
             ok = false;
             break;
           }
-          if (m < kKeys && key0 + m >= t.L) {
-            uint8_t* vt = v_s + vs * kKvBytes + m * 128;
-            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+          for (int j = 0; j < kVChunks; ++j) {
+            if (key0 + (j + 1) * kVKeys <= t.L) continue;
+            const int vc = kVChunks * it + j;
+            const int slot = vc % kVSlots;
+            if (!mbar_wait_warp<true>(&ctl->v_full[slot], (vc / kVSlots) & 1, a.status,
+                                      abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (key0 + j * kVKeys + m >= t.L) {
+              uint8_t* vt = v_s + slot * kVSlotBytes + m * 128;
+              const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c)
+              for (int c = 0; c < kChunks; ++c)
 #pragma unroll
-              for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(vt + c * kKvChunk + i * 16) = z;
+                for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(vt + c * kVBlock + i * 16) = z;
+            }
           }
           fence_proxy_async_smem();
+          if (!ok) break;
         }
         tc_fence_before();
-        mbar_arrive(&ctl->p_full[it & 1]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->p_full[it & 1]);
       }
       if (!ok) break;
       if (has_nx) rec_nx = a.tiles[idx_nx];

@@ -61,6 +61,8 @@ CASES = [
     ([500], [1100], 12, 2, 128, "causal", 37, 1.25),          # G = 6: 126 live rows of 128
     ([40, 90], [0, 7], 24, 2, 16, "dense", -1, 1.0),          # G = 12: 120 live rows
     ([1, 2, 3], [0, 0, 0], 2, 1, 32, "causal", 0, 1.0),       # tiny, window 0
+    ([150, 70], [213, 30], 8, 2, 16, "causal", -1, 1.0),      # 8 K and 2 V page pieces
+    ([260, 45], [0, 700], 4, 2, 128, "causal", 100, 1.0),     # one page per KV tile, window
 ]
 
 
