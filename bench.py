@@ -862,8 +862,11 @@ def main():
     del r
     torch.cuda.empty_cache()
 
-    if rank == 0 and world == 1 and not args.skip_cpu and p["form"] == "decode":
-        line["cpu_baseline"] = cpu_baseline_decode(p)
+    # The oracle baselines run after every GPU timing: their BLAS threads would otherwise
+    # compete with the launching thread of the latency-bound workloads.
+    cpu_todo = []
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        cpu_todo.append(None)                      # the headline workload
     l2_gbs = None
     if p["form"] in ("qsa", "qsa_indexed"):
         l2_gbs = l2_read_gbs(dev)
@@ -874,8 +877,6 @@ def main():
                                "gathered_bytes": gb,
                                "peak_source": "measured in this run (paged_attn_l2_read_probe "
                                               "over a 24 MiB L2-resident buffer)"}
-    if rank == 0 and world == 1 and not args.skip_cpu and p["form"] != "decode":
-        line["cpu_baseline"] = oracle_sample_rate(args.workload, p)
     if not args.no_extra and rank == 0:
         extra = {}
         for name in ("decode_b64_sq4", "tiny_bsr", "prefill_b16", "prefill_b16_w1023",
@@ -902,7 +903,7 @@ def main():
                     del rr
                     torch.cuda.empty_cache()
                     if not args.skip_cpu:
-                        extra[name]["cpu_baseline"] = oracle_sample_rate(name, q)
+                        cpu_todo.append(name)
                     continue
                 n = {"bsr": bsr_pairs, "prefill": prefill_pairs, "qsa": qsa_pairs,
                      "qsa_indexed": qsa_indexed_pairs, "sage": sage_pairs}[q["form"]](q)
@@ -933,8 +934,15 @@ def main():
                 extra[name] = {"unavailable": str(e)}
                 continue
             if not args.skip_cpu:
-                extra[name]["cpu_baseline"] = oracle_sample_rate(name, q)
+                cpu_todo.append(name)
         line["per_config"] = extra
+    for name in cpu_todo:
+        if name is None:
+            line["cpu_baseline"] = (cpu_baseline_decode(p) if p["form"] == "decode" else
+                                    oracle_sample_rate(args.workload, p))
+        else:
+            line["per_config"][name]["cpu_baseline"] = oracle_sample_rate(name,
+                                                                         make_workload(name))
     if rank == 0:
         print(json.dumps(line))
     if dist_on:
