@@ -4,8 +4,11 @@
 // listed per (request, KV head, query block) in BSR form) and the dense packed-Q form of
 // batch_prefill_with_paged_kv_cache (every KV tile that meets the causal / window span).
 //
-// Persistent: one CTA per SM walks the planner's tile list (sorted by cost, largest first)
-// with a stride of the grid size.  A tile holds up to two Q sub-tiles of 128 rows, a row
+// Persistent: one CTA per SM walks the planner's tile list (sorted by cost, largest first).
+// CTA c starts with tile c; after that the CTAs claim tiles from a counter in the status area
+// (so each takes the largest tile left whenever it needs one: a static stride left the
+// slowest CTA ~7% behind the mean on dense prefill).  The K producer claims two tiles ahead
+// and hands the claims to the other roles through a small ring in shared memory.  A tile holds up to two Q sub-tiles of 128 rows, a row
 // being a (token, head-in-group) pair, so the G query heads that share a KV head share
 // every K/V tile.  Roles (384 threads):
 //   warps 0-3  softmax + epilogue of sub-tile 0 (thread t <-> TMEM lane t <-> row t)
@@ -50,6 +53,7 @@ constexpr float kRescaleThreshold = 8.0f;      // log2 units
 constexpr float kLn2 = 0.6931471805599453f;
 
 constexpr int kFacts = 4;                      // column-facts ring entries
+constexpr int kTileRing = 4;                   // claimed work tiles handed to the roles
 
 // Facts of one KV tile that are the same for every row.
 struct TileFacts {
@@ -68,6 +72,8 @@ struct Ctrl {
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
   uint64_t s_full[2], p_full[2], o_final[2], o_empty[2];
+  uint64_t t_full[kTileRing], t_empty[kTileRing];
+  int tidx[kTileRing];      // tile of claim sequence s in slot s % kTileRing
   uint32_t tmem_base;
   int abort_flag;
   int skip;                 // this CTA has no work tile (or the launch was aborted)
@@ -75,6 +81,17 @@ struct Ctrl {
 
 constexpr int kSmemBytes =
     2 * kQBytes + (kKStages + kVStages) * kKvBytes + static_cast<int>(sizeof(Ctrl)) + 1024;
+
+// Tile claims: status[2] counts the tiles claimed beyond the first one of every CTA, and
+// status[3] the CTAs that have finished; the last CTA of a launch to finish sets both back to
+// zero, so every launch (and every graph replay) starts from zero.
+__device__ __forceinline__ void claims_done(uint32_t* status) {
+  __threadfence();
+  if (atomicAdd(status + 3, 1u) == gridDim.x - 1) {
+    atomicExch(status + 2, 0u);
+    atomicExch(status + 3, 0u);
+  }
+}
 
 // Geometry of the KV tile sequence of one planner tile.
 template <int CK>
@@ -175,7 +192,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   if constexpr (FACTS) {
     // one decision for the whole CTA: another CTA may set the status word meanwhile
     const int n0 = a.n_tiles ? *a.n_tiles : a.capacity;
-    if (__syncthreads_or(static_cast<int>(blockIdx.x) >= n0 || launch_aborted(a.status))) return;
+    if (__syncthreads_or(static_cast<int>(blockIdx.x) >= n0 || launch_aborted(a.status))) {
+      if (threadIdx.x == 0) claims_done(a.status);
+      return;
+    }
   }
   const int G = a.G;
   const int TM = kMTileRows / G;                         // tokens per sub-tile
@@ -205,6 +225,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       mbar_init(&ctl->o_final[w], 1);
       mbar_init(&ctl->o_empty[w], 128);
     }
+    // readers of every claim: the V producer, the MMA issuer, the facts warp (block-sparse
+    // only) and the eight softmax warps
+    for (int i = 0; i < kTileRing; ++i) {
+      mbar_init(&ctl->t_full[i], 1);
+      mbar_init(&ctl->t_empty[i], (use_facts ? 3 : 2) + 8);
+    }
     ctl->abort_flag = 0;
     fence_mbar_init();
   }
@@ -230,11 +256,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   if constexpr (!FACTS) {
     if (ctl->skip) {
       if (warp == 9) tmem_dealloc(tmem, 512);
+      if (threadIdx.x == 0) claims_done(a.status);
       return;
     }
   }
   const int n_live = a.n_tiles ? *a.n_tiles : a.capacity;
   volatile int* abort_flag = &ctl->abort_flag;
+  // The tile of claim sequence s >= 1 (sequence 0 is tile blockIdx.x, never in the ring; the
+  // ring holds sequence s as entry s - 1), read by one warp (all lanes) or by one thread
+  // (single); a failed wait reads as the end of the list.
+  auto read_claim = [&](int s, bool single) -> int {
+    const int e = s - 1, slot = e % kTileRing;
+    const bool got = single ? mbar_wait_fast(&ctl->t_full[slot], (e / kTileRing) & 1, a.status,
+                                             abort_flag)
+                            : mbar_wait_warp<true>(&ctl->t_full[slot], (e / kTileRing) & 1,
+                                                   a.status, abort_flag);
+    const int v = got ? *reinterpret_cast<volatile int*>(&ctl->tidx[slot]) : n_live;
+    if (!single) __syncwarp();
+    if (got && (single || lane == 0)) mbar_arrive(&ctl->t_empty[slot]);
+    return v;
+  };
   if (warp >= 8) {
   regs_decrease<kControlRegs>();
   if (warp == 8 || warp == 10) {
@@ -259,11 +300,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int head_off = is_k ? a.k_head_off : a.v_head_off;
     int kv_it = 0, qcount = 0;
     bool ok = true;
+    // K producer: claims sequence s into ring entry s - 1 (its slot free once entry s - 5 is
+    // read by every reader); a claim past the list is the end marker.
+    auto claim = [&](int s) -> int {
+      const int e = s - 1, slot = e % kTileRing;
+      const bool free = e < kTileRing ||
+                        mbar_wait_warp<true>(&ctl->t_empty[slot], ((e / kTileRing) - 1) & 1,
+                                             a.status, abort_flag);
+      int v = n_live;
+      if (lane == 0) {
+        if (free) v = min(n_live, static_cast<int>(gridDim.x) +
+                                      static_cast<int>(atomicAdd(a.status + 2, 1u)));
+        ctl->tidx[slot] = v;
+        mbar_arrive(&ctl->t_full[slot]);
+      }
+      return __shfl_sync(0xffffffffu, v, 0);
+    };
+    int claimed = is_k ? claim(1) : 0;          // K producer: the newest claim (sequence s + 1)
     TileRec rec_nx = a.tiles[blockIdx.x];       // record of the next work tile, loaded a tile ahead
-    for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
+    for (int idx = blockIdx.x, s = 0; ok && idx < n_live; ++s) {
       const TileInfo<CK> t = tile_from_rec<CK>(a, rec_nx);
-      if (idx + static_cast<int>(gridDim.x) < n_live) rec_nx = a.tiles[idx + gridDim.x];
-      if (t.N == 0) continue;
+      // tile s + 1: claimed by the K producer at the end of tile s - 1 (it claims s + 2 once
+      // this tile's copies are issued, keeping the claim's round trip off the tile's start)
+      const int nx = is_k ? claimed : read_claim(s + 1, false);
+      if (nx < n_live) rec_nx = a.tiles[nx];
+      idx = nx;
+      if (t.N == 0) {
+        if (is_k && claimed < n_live) claimed = claim(s + 2);
+        continue;
+      }
       // page ids of the first KV tile: loaded before the wait for the Q buffer
       const int* pt = a.pt_indptr ? a.pt + __ldg(a.pt_indptr + t.rec.b)
                                   : a.pt + static_cast<long long>(t.rec.b) * a.pt_stride;
@@ -312,6 +377,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
       }
       kv_it += t.N;
+      if (is_k && ok && claimed < n_live) claimed = claim(s + 2);
     }
   } else if (warp == 11 && use_facts) {
     // =============================== column facts ======================================
@@ -320,9 +386,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     int kv_it = 0;
     bool ok = true;
     TileRec rec_nx = a.tiles[blockIdx.x];       // record of the next work tile, loaded a tile ahead
-    for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
+    for (int idx = blockIdx.x, s = 0; ok && idx < n_live; ++s) {
       const TileInfo<CK> t = tile_from_rec<CK>(a, rec_nx);
-      if (idx + static_cast<int>(gridDim.x) < n_live) rec_nx = a.tiles[idx + gridDim.x];
+      idx = read_claim(s + 1, false);
+      if (idx < n_live) rec_nx = a.tiles[idx];
       for (int n = 0; n < t.N; ++n) {
         const int it = kv_it + n, slot = it % kFacts;
         if (it >= kFacts &&
@@ -415,9 +482,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       int ep[2] = {0, 0};                        // epilogues that read O_w so far
       bool ok = true;
       TileRec rec_nx = a.tiles[blockIdx.x];     // record of the next work tile, a tile ahead
-      for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
+      for (int idx = blockIdx.x, s = 0; ok && idx < n_live; ++s) {
         const TileInfo<CK> t = tile_from_rec<CK>(a, rec_nx);
-        if (idx + static_cast<int>(gridDim.x) < n_live) rec_nx = a.tiles[idx + gridDim.x];
+        idx = read_claim(s + 1, true);
+        if (idx < n_live) rec_nx = a.tiles[idx];
         const int N = t.N;
         if (N == 0) continue;
         const bool two = t.nsub > 1;
@@ -496,10 +564,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     TileRec rec_nx = a.tiles[blockIdx.x];
     int L_nx, nq_nx;
     request_lengths(a, rec_nx.b, L_nx, nq_nx);
-    for (int idx = blockIdx.x; ok && idx < n_live; idx += gridDim.x) {
+    int idx_nx = 0;                                // the next claim, read at the tile's end
+    for (int idx = blockIdx.x, s = 0; ok && idx < n_live; idx = idx_nx, ++s) {
       const TileInfo<CK> t = tile_from_parts<CK>(a, rec_nx, L_nx, nq_nx);
-      const int idx_nx = idx + static_cast<int>(gridDim.x);
-      const bool has_nx = idx_nx < n_live;
       const int N = t.N;
       const int ntok_w = w == 0 ? t.ntok0 : t.ntok1;
       if (w >= t.nsub) {                           // this sub-tile is empty
@@ -509,7 +576,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                     abort_flag);
           if (ok && lane == 0) mbar_arrive(&ctl->facts_empty[it % kFacts]);
         }
-        if (has_nx) {
+        idx_nx = read_claim(s + 1, false);
+        if (idx_nx < n_live) {
           rec_nx = a.tiles[idx_nx];
           request_lengths(a, rec_nx.b, L_nx, nq_nx);
         }
@@ -736,6 +804,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->p_full[w]);
       }
+      idx_nx = read_claim(s + 1, false);
+      const bool has_nx = idx_nx < n_live;
       if (has_nx) rec_nx = a.tiles[idx_nx];
       // ---- epilogue ------------------------------------------------------------------------
       bool have_o = false;
@@ -807,6 +877,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) claims_done(a.status);
   if (warp == 9) {
     __syncwarp();
     tc_fence_after();
