@@ -309,8 +309,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                              a.status, abort_flag);
       int v = n_live;
       if (lane == 0) {
-        if (free) v = min(n_live, static_cast<int>(gridDim.x) +
-                                      static_cast<int>(atomicAdd(a.status + 2, 1u)));
+        // nothing to claim when every tile is some CTA's first (small plans): no round trip
+        if (free && static_cast<int>(gridDim.x) < n_live)
+          v = min(n_live, static_cast<int>(gridDim.x) +
+                              static_cast<int>(atomicAdd(a.status + 2, 1u)));
         ctl->tidx[slot] = v;
         mbar_arrive(&ctl->t_full[slot]);
       }
