@@ -82,17 +82,6 @@ struct Ctrl {
 constexpr int kSmemBytes =
     2 * kQBytes + (kKStages + kVStages) * kKvBytes + static_cast<int>(sizeof(Ctrl)) + 1024;
 
-// Tile claims: status[2] counts the tiles claimed beyond the first one of every CTA, and
-// status[3] the CTAs that have finished; the last CTA of a launch to finish sets both back to
-// zero, so every launch (and every graph replay) starts from zero.
-__device__ __forceinline__ void claims_done(uint32_t* status) {
-  __threadfence();
-  if (atomicAdd(status + 3, 1u) == gridDim.x - 1) {
-    atomicExch(status + 2, 0u);
-    atomicExch(status + 3, 0u);
-  }
-}
-
 // Geometry of the KV tile sequence of one planner tile.
 template <int CK>
 struct KvWalk {

@@ -88,6 +88,20 @@ __host__ __device__ inline int page_piece_rows(int page_size, int span) {
   return page_size < span ? page_size : span;
 }
 
+#ifdef __CUDACC__
+// Work-tile claims of the persistent tensor-core kernels: status[2] counts the tiles claimed
+// beyond the first one of every CTA, status[3] the CTAs that have finished; the last CTA of a
+// launch to finish sets both back to zero, so every launch (and every graph replay) starts
+// from zero.  Called once per CTA, by one thread, on every exit path.
+__device__ __forceinline__ void claims_done(uint32_t* status) {
+  __threadfence();
+  if (atomicAdd(status + 3, 1u) == gridDim.x - 1) {
+    atomicExch(status + 2, 0u);
+    atomicExch(status + 3, 0u);
+  }
+}
+#endif
+
 // Tokens per Q sub-tile: floor(128 / G); a CTA holds two sub-tiles.
 inline int sub_tile_tokens(int G) { return kMTileRows / G; }
 inline int cta_tile_tokens(int G) { return 2 * sub_tile_tokens(G); }
