@@ -150,7 +150,9 @@ __device__ __noinline__ void rescale_o(uint32_t taddr, float alpha_c) {
 // Normalise and store this thread's d rows (r, r + 128) of every live column; lane c holds
 // the running maximum of column c.  Both O^T halves come in with two 32-column TMEM loads
 // and one wait; the scalars of the launch are passed by value so that they stay in
-// registers (a reference to the kernel parameter would place it in local memory).
+// registers (a reference to the kernel parameter would place it in local memory).  Lanes
+// 2i and 2i + 1 trade one value per column pair, so that each stores two adjacent d of one
+// column (a bf16x2 and a float2 store instead of two of each width).
 __device__ __forceinline__ void write_output(__nv_bfloat16* __restrict__ out,
                                              float* __restrict__ out32, float* __restrict__ lse,
                                              int Hq, int G, int T, const QsaCtrl* ctl,
@@ -169,20 +171,29 @@ __device__ __forceinline__ void write_output(__nv_bfloat16* __restrict__ out,
 #pragma unroll
     for (int c = 0; c < kN; ++c) o0[c] = o1[c] = 0u;
   }
-  const long long row0 = static_cast<long long>(t) * Hq * kD + r;
+  const bool odd = lane & 1;
+  const long long row0 = static_cast<long long>(t) * Hq * kD + (r & ~1);   // d of the pair
 #pragma unroll
-  for (int c = 0; c < kN; ++c) {
-    const float inv = __shfl_sync(0xffffffffu, inv_c, c);
-    const int gq = c / kGroupCols, h = c % kGroupCols;
+  for (int c = 0; c < kN; c += 2) {
+    // this lane's d row in both columns, each scaled by its column's 1 / l
+    const float inv_a = __shfl_sync(0xffffffffu, inv_c, c);
+    const float inv_b = __shfl_sync(0xffffffffu, inv_c, c + 1);
+    const float a0 = __uint_as_float(o0[c]) * inv_a, a1 = __uint_as_float(o1[c]) * inv_a;
+    const float b0 = __uint_as_float(o0[c + 1]) * inv_b, b1 = __uint_as_float(o1[c + 1]) * inv_b;
+    // the even lane keeps column c, the odd lane column c + 1; each sends the other one
+    const float x0 = __shfl_xor_sync(0xffffffffu, odd ? a0 : b0, 1);
+    const float x1 = __shfl_xor_sync(0xffffffffu, odd ? a1 : b1, 1);
+    const int cc = c + (odd ? 1 : 0);
+    const int gq = cc / kGroupCols, h = cc % kGroupCols;
     if (h >= G || (gq == 1 && !two)) continue;
-    const float v0 = __uint_as_float(o0[c]) * inv;
-    const float v1 = __uint_as_float(o1[c]) * inv;
+    const float lo0 = odd ? x0 : a0, hi0 = odd ? b0 : x0;     // d, d + 1 (rows r & ~1, | 1)
+    const float lo1 = odd ? x1 : a1, hi1 = odd ? b1 : x1;     // d + 128, d + 129
     const long long o = row0 + static_cast<long long>((g0 + gq) * G + h) * kD;
-    out[o] = __float2bfloat16_rn(v0);
-    out[o + 128] = __float2bfloat16_rn(v1);
+    *reinterpret_cast<__nv_bfloat162*>(out + o) = __floats2bfloat162_rn(lo0, hi0);
+    *reinterpret_cast<__nv_bfloat162*>(out + o + 128) = __floats2bfloat162_rn(lo1, hi1);
     if (out32) {
-      out32[o] = v0;
-      out32[o + 128] = v1;
+      *reinterpret_cast<float2*>(out32 + o) = make_float2(lo0, hi0);
+      *reinterpret_cast<float2*>(out32 + o + 128) = make_float2(lo1, hi1);
     }
   }
   // lse of column c from lane c of the first warp
@@ -585,7 +596,8 @@ int launch_qsa(const paged_attn_params* p, const paged_attn_meta* m, const void*
   if (!out || !m->lo_dev || !m->hi_dev || !m->block_first_dev || !m->block_last_dev)
     return PAGED_ATTN_ERR_INVALID_ARGUMENT;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-       reinterpret_cast<uintptr_t>(v)) & 15u)
+       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out) |
+       reinterpret_cast<uintptr_t>(out_fp32)) & 15u)
     return PAGED_ATTN_ERR_INVALID_ARGUMENT;
   const int pairs = (p->num_kv_heads + 1) / 2;
   const long long units = static_cast<long long>(p->q_len) * pairs;
