@@ -7,19 +7,21 @@
 // Persistent: one CTA per SM walks the planner's tile list (sorted by cost, largest first).
 // CTA c starts with tile c; after that the CTAs claim tiles from a counter in the status area
 // (so each takes the largest tile left whenever it needs one: a static stride left the
-// slowest CTA ~7% behind the mean on dense prefill).  The K producer claims two tiles ahead
-// and hands the claims to the other roles through a small ring in shared memory.  A tile holds up to two Q sub-tiles of 128 rows, a row
-// being a (token, head-in-group) pair, so the G query heads that share a KV head share
-// every K/V tile.  Roles (384 threads):
+// slowest CTA ~7% behind the mean on dense prefill).  The claims reach the other roles
+// through a small ring in shared memory; the K producer makes them (two tiles ahead) in
+// block-sparse launches, warp 11 (otherwise idle) in dense ones.
+// A tile holds up to two Q sub-tiles of 128 rows, a row being a (token, head-in-group) pair,
+// so the G query heads that share a KV head share every K/V tile.  Roles (384 threads):
 //   warps 0-3  softmax + epilogue of sub-tile 0 (thread t <-> TMEM lane t <-> row t)
 //   warps 4-7  softmax + epilogue of sub-tile 1
 //   warp  8    TMA producer of Q (once per tile) and K (2-stage ring)
 //   warp  9    TMEM owner and MMA issuer (one thread): S_w = Q_w K^T and O_w += P_w V
 //   warp 10    TMA producer of V (3-stage ring: a V stage is free only after PV of both
 //              sub-tiles, later than a K stage after QK, so V gets the deeper ring)
-//   warp 11    column facts of each KV tile (first key of each sub-chunk, live-key mask, key
-//              range), a few tiles ahead into a small ring, so that the softmax reads them
-//              from shared memory instead of issuing block-id and valid-bit loads
+//   warp 11    block-sparse: column facts of each KV tile (first key of each sub-chunk,
+//              live-key mask, key range), a few tiles ahead into a small ring, so that the
+//              softmax reads them from shared memory instead of issuing block-id and
+//              valid-bit loads; dense: work-tile claims
 // K and V of a 128-key tile are gathered one TMA box per page piece (a page, or the part of
 // a page inside a selected block) and 64-column half.
 // Tensor memory (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512); P_w is
@@ -182,7 +184,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // one decision for the whole CTA: another CTA may set the status word meanwhile
     const int n0 = a.n_tiles ? *a.n_tiles : a.capacity;
     if (__syncthreads_or(static_cast<int>(blockIdx.x) >= n0 || launch_aborted(a.status))) {
-      if (threadIdx.x == 0) claims_done(a.status);
+      // (no claims, hence no count, when every tile is some CTA's first)
+      if (threadIdx.x == 0 && static_cast<int>(gridDim.x) < n0) claims_done(a.status);
       return;
     }
   }
@@ -214,11 +217,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       mbar_init(&ctl->o_final[w], 1);
       mbar_init(&ctl->o_empty[w], 128);
     }
-    // readers of every claim: the V producer, the MMA issuer, the facts warp (block-sparse
-    // only) and the eight softmax warps
+    // readers of every claim: the V producer, the MMA issuer, the eight softmax warps, and
+    // the facts warp (block-sparse) or the K producer (dense, where warp 11 claims)
     for (int i = 0; i < kTileRing; ++i) {
       mbar_init(&ctl->t_full[i], 1);
-      mbar_init(&ctl->t_empty[i], (use_facts ? 3 : 2) + 8);
+      mbar_init(&ctl->t_empty[i], 3 + 8);
     }
     ctl->abort_flag = 0;
     fence_mbar_init();
@@ -245,7 +248,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   if constexpr (!FACTS) {
     if (ctl->skip) {
       if (warp == 9) tmem_dealloc(tmem, 512);
-      if (threadIdx.x == 0) claims_done(a.status);
+      if (threadIdx.x == 0 && static_cast<int>(gridDim.x) < (a.n_tiles ? *a.n_tiles : a.capacity))
+        claims_done(a.status);
       return;
     }
   }
@@ -264,6 +268,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     if (!single) __syncwarp();
     if (got && (single || lane == 0)) mbar_arrive(&ctl->t_empty[slot]);
     return v;
+  };
+  // The claimer (the K producer of block-sparse launches, warp 11 of dense ones) claims
+  // sequence s into ring entry s - 1, its slot free once entry s - 5 is read by every
+  // reader; a claim past the list is the end marker.
+  auto claim = [&](int s) -> int {
+    const int e = s - 1, slot = e % kTileRing;
+    const bool free = e < kTileRing ||
+                      mbar_wait_warp<true>(&ctl->t_empty[slot], ((e / kTileRing) - 1) & 1,
+                                           a.status, abort_flag);
+    int v = n_live;
+    if (lane == 0) {
+      // nothing to claim when every tile is some CTA's first (small plans): no round trip
+      if (free && static_cast<int>(gridDim.x) < n_live)
+        v = min(n_live, static_cast<int>(gridDim.x) +
+                            static_cast<int>(atomicAdd(a.status + 2, 1u)));
+      ctl->tidx[slot] = v;
+      mbar_arrive(&ctl->t_full[slot]);
+    }
+    return __shfl_sync(0xffffffffu, v, 0);
   };
   if (warp >= 8) {
   regs_decrease<kControlRegs>();
@@ -289,35 +312,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     const int head_off = is_k ? a.k_head_off : a.v_head_off;
     int kv_it = 0, qcount = 0;
     bool ok = true;
-    // K producer: claims sequence s into ring entry s - 1 (its slot free once entry s - 5 is
-    // read by every reader); a claim past the list is the end marker.
-    auto claim = [&](int s) -> int {
-      const int e = s - 1, slot = e % kTileRing;
-      const bool free = e < kTileRing ||
-                        mbar_wait_warp<true>(&ctl->t_empty[slot], ((e / kTileRing) - 1) & 1,
-                                             a.status, abort_flag);
-      int v = n_live;
-      if (lane == 0) {
-        // nothing to claim when every tile is some CTA's first (small plans): no round trip
-        if (free && static_cast<int>(gridDim.x) < n_live)
-          v = min(n_live, static_cast<int>(gridDim.x) +
-                              static_cast<int>(atomicAdd(a.status + 2, 1u)));
-        ctl->tidx[slot] = v;
-        mbar_arrive(&ctl->t_full[slot]);
-      }
-      return __shfl_sync(0xffffffffu, v, 0);
-    };
-    int claimed = is_k ? claim(1) : 0;          // K producer: the newest claim (sequence s + 1)
+    const bool claimer = is_k && use_facts;
+    int claimed = claimer ? claim(1) : 0;       // the newest claim (sequence s + 1)
     TileRec rec_nx = a.tiles[blockIdx.x];       // record of the next work tile, loaded a tile ahead
     for (int idx = blockIdx.x, s = 0; ok && idx < n_live; ++s) {
       const TileInfo<CK> t = tile_from_rec<CK>(a, rec_nx);
       // tile s + 1: claimed by the K producer at the end of tile s - 1 (it claims s + 2 once
       // this tile's copies are issued, keeping the claim's round trip off the tile's start)
-      const int nx = is_k ? claimed : read_claim(s + 1, false);
+      const int nx = claimer ? claimed : read_claim(s + 1, false);
       if (nx < n_live) rec_nx = a.tiles[nx];
       idx = nx;
       if (t.N == 0) {
-        if (is_k && claimed < n_live) claimed = claim(s + 2);
+        if (claimer && claimed < n_live) claimed = claim(s + 2);
         continue;
       }
       // page ids of the first KV tile: loaded before the wait for the Q buffer
@@ -368,7 +374,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         }
       }
       kv_it += t.N;
-      if (is_k && ok && claimed < n_live) claimed = claim(s + 2);
+      if (claimer && ok && claimed < n_live) claimed = claim(s + 2);
     }
   } else if (warp == 11 && use_facts) {
     // =============================== column facts ======================================
@@ -438,6 +444,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
         if (lane == 0) mbar_arrive(&ctl->facts_full[slot]);
       }
       kv_it += t.N;
+    }
+  } else if (warp == 11) {
+    // =============================== work-tile claims (dense) ==========================
+    // up to four claims ahead of the slowest reader, off every other role's path
+    for (int s = 1; claim(s) < n_live; ++s) {
     }
   } else if (warp == 9) {
     // =============================== MMA issuer ========================================
@@ -868,7 +879,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
   }
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0) claims_done(a.status);
+  if (threadIdx.x == 0 && static_cast<int>(gridDim.x) < n_live) claims_done(a.status);
   if (warp == 9) {
     __syncwarp();
     tc_fence_after();
