@@ -56,7 +56,7 @@ struct Ctrl {
   uint64_t q_full, q_empty;
   uint64_t k_full[kKSlots], k_empty[kKSlots];
   uint64_t v_full[kVSlots], v_empty[kVSlots];
-  uint64_t s_full[2], p_full[2];
+  uint64_t p_full[2];
   uint64_t o_final, o_empty;
   uint32_t tmem_base;
   int abort_flag;
@@ -137,10 +137,7 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       mbar_init(&ctl->v_full[s], 1);
       mbar_init(&ctl->v_empty[s], 1);
     }
-    for (int w = 0; w < 2; ++w) {
-      mbar_init(&ctl->s_full[w], 1);
-      mbar_init(&ctl->p_full[w], 4);           // one arrival per softmax warp
-    }
+    for (int w = 0; w < 2; ++w) mbar_init(&ctl->p_full[w], 4);   // one arrival per softmax warp
     mbar_init(&ctl->o_final, 1);
     mbar_init(&ctl->o_empty, kRows);
     // a launch that an earlier CTA already broke does nothing
@@ -288,9 +285,8 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
             mma_ss(tmem + kTmemS + (it & 1) * kKeys,
                    q_desc0 + static_cast<uint64_t>((c * kQChunk + k4 * 32) >> 4),
                    kd + static_cast<uint64_t>((k4 * 32) >> 4), idesc_qk, c > 0 || k4 > 0);
-          mma_commit(&ctl->k_empty[slot]);
+          mma_commit(&ctl->k_empty[slot]);     // the last one also tells the softmax S is ready
         }
-        mma_commit(&ctl->s_full[it & 1]);
         return true;
       };
       // O += P(it) V(it): per 32-key V chunk, its 2 k-steps of 16 keys
@@ -368,8 +364,15 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // wait is sound there because that slot's previous chunk belongs to PV(it - 2), complete
     // before S(it) (QK(it) was issued after it), and its next one to PV(it) or later, which
     // waits for this softmax's P.
+    // S(it) is complete once QK(it) has released K chunk 4 it + 3.  That barrier's previous
+    // commit came from QK(it - 1), complete before this softmax saw S(it - 1), and its next
+    // from QK(it + 2), which is issued after PV(it) and so after this softmax's P: the parity
+    // wait cannot alias (it could with four K slots, where the next commit is QK(it + 1)'s).
+    static_assert(kKSlots >= kChunks + 1, "S readiness rides on the K-slot release");
     auto s_ready = [&](int it) {
-      return mbar_wait_fast_warp(&ctl->s_full[it & 1], (it >> 1) & 1, a.status, abort_flag);
+      const int c = kChunks * it + kChunks - 1;
+      return mbar_wait_fast_warp(&ctl->k_empty[c % kKSlots], (c / kKSlots) & 1, a.status,
+                                 abort_flag);
     };
     auto pv_done = [&](int it) {
       const int c = kVChunks * it + kVChunks - 1;
