@@ -158,11 +158,12 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     // nothing to do; fall through to the teardown
   } else if (warp == kProdK || warp == kProdV) {
     // =============================== producers =========================================
-    // warp 4 copies Q (lane 0) and K, warp 6 copies V.  Lane p owns page piece p of a KV tile
-    // (R keys of one page; its page id is loaded once per tile, while the tile before is
-    // copied).  A K chunk is
-    // one 64-column block of the tile: every piece.  A V chunk is 32 keys of the tile in all
-    // four 64-column blocks: the pieces that fall in it.
+    // warp 4 copies Q (lane 0) and K, warp 6 copies V.  A piece is R keys of one page inside
+    // a KV tile; its page id is loaded once per tile, while the tile before is copied.  A K
+    // chunk is one 64-column block of the tile: every piece, lane p copying piece p.  A V
+    // chunk is 32 keys of the tile in all four 64-column blocks: the pieces that fall in it,
+    // lane 4 p + c copying column block c of piece p, so that the four copies of a piece
+    // leave from four lanes at once.
     const bool is_k = warp == kProdK;
     if (lane == 0) {
       if (is_k) {
@@ -174,8 +175,10 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     }
     const int ps = a.page_size;
     const int R = is_k ? page_piece_rows(ps, kKeys) : page_piece_rows(ps, kVKeys);
-    const int pieces = kKeys / R;                // per KV tile (at most 16)
-    const int my_chunk = (lane * R) / kVKeys;    // V: the chunk this lane's piece falls in
+    const int pieces = kKeys / R;                // per KV tile: K at most 16, V at most 8
+    const int piece = is_k ? lane : lane >> 2;   // V: R >= 16 (page sizes 16 to 128)
+    const int vblk = lane & 3;                   // V: the 64-column block this lane copies
+    const int my_chunk = (piece * R) / kVKeys;   // V: the chunk this lane's piece falls in
     const int slots = is_k ? kKSlots : kVSlots;
     uint8_t* ring = is_k ? k_s : v_s;
     const int slot_bytes = is_k ? kKSlotBytes : kVSlotBytes;
@@ -195,8 +198,8 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
                                   : a.pt + static_cast<long long>(t.b) * a.pt_stride;
       // first key of this lane's piece of KV tile n, or -1
       auto key_of = [&](int n) {
-        const int key = (t.kt0 + n) * kKeys + lane * R;
-        return (lane < pieces && key < t.L) ? key : -1;
+        const int key = (t.kt0 + n) * kKeys + piece * R;
+        return (piece < pieces && key < t.L) ? key : -1;
       };
       int key = key_of(0);
       int page = key >= 0 ? __ldg(pt + key / ps) : 0;
@@ -234,7 +237,7 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           const bool mine = live && (is_k || my_chunk == j);
           const uint32_t nlive = __popc(__ballot_sync(0xffffffffu, mine));
           if (lane == 0)
-            mbar_arrive_expect_tx(&full[slot], nlive * R * 128u * (is_k ? 1u : kChunks));
+            mbar_arrive_expect_tx(&full[slot], nlive * R * 128u);   // one R-row box per lane
           __syncwarp();
           if (mine) {
             uint8_t* base = ring + slot * slot_bytes;
@@ -242,10 +245,8 @@ attn256_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
               tma_load_2d(base + static_cast<uint32_t>(lane * R) * 128u, map, &full[slot], j * 64,
                           row);
             } else {
-              uint8_t* dst = base + static_cast<uint32_t>(lane * R - j * kVKeys) * 128u;
-#pragma unroll
-              for (int c = 0; c < kChunks; ++c)
-                tma_load_2d(dst + c * kVBlock, map, &full[slot], c * 64, row);
+              uint8_t* dst = base + static_cast<uint32_t>(piece * R - j * kVKeys) * 128u;
+              tma_load_2d(dst + vblk * kVBlock, map, &full[slot], vblk * 64, row);
             }
           }
           ++ch;
