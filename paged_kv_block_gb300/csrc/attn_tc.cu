@@ -149,17 +149,17 @@ __device__ __forceinline__ TileInfo<CK> tile_from_rec(const AttnLaunch& a, const
   return tile_from_parts<CK>(a, rec, L, nq);
 }
 
-// Page piece `lane` of KV tile n: keys [key, key + R) of one page (R = page_piece_rows).
+// Page piece p of KV tile n: keys [key, key + R) of one page (R = page_piece_rows).
 // Returns the piece's first key, or -1 (no piece, empty slot, past the length); the page-table
 // load it issues is first used by the caller after its next barrier wait, so the loads of
-// the whole tile (one per lane) overlap that wait.
+// the whole tile (one per piece) overlap that wait.
 template <int CK>
-__device__ __forceinline__ int piece_key(const AttnLaunch& a, const TileInfo<CK>& t, int n, int lane) {
+__device__ __forceinline__ int piece_key(const AttnLaunch& a, const TileInfo<CK>& t, int n, int p) {
   const int ps = a.page_size;
   const int R = page_piece_rows(ps, CK);
-  if (lane >= kKvTile / R) return -1;
-  const int k0 = t.walk.key0(n, (lane * R) / CK);
-  const int key = k0 + (lane * R) % CK;
+  if (p >= kKvTile / R) return -1;
+  const int k0 = t.walk.key0(n, (p * R) / CK);
+  const int key = k0 + (p * R) % CK;
   const int max_page_idx = (t.L + ps - 1) / ps;
   return (k0 >= 0 && key < t.L && key / ps < max_page_idx) ? key : -1;
 }
@@ -304,6 +304,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
     }
     const int ps = a.page_size;
     const int R = page_piece_rows(ps, CK);
+    // lane 2 p + h copies the 64-column half h of page piece p (R >= 8, so at most 16 pieces),
+    // so that a piece's two copies leave from two lanes at once
+    const int piece = lane >> 1, half = lane & 1;
     const int stages = is_k ? kKStages : kVStages;
     uint8_t* ring = is_k ? k_s : v_s;
     uint64_t* full = is_k ? ctl->k_full : ctl->v_full;
@@ -329,7 +332,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
       // page ids of the first KV tile: loaded before the wait for the Q buffer
       const int* pt = a.pt_indptr ? a.pt + __ldg(a.pt_indptr + t.rec.b)
                                   : a.pt + static_cast<long long>(t.rec.b) * a.pt_stride;
-      int key = piece_key<CK>(a, t, 0, lane);
+      int key = piece_key<CK>(a, t, 0, piece);
       int page = key >= 0 ? __ldg(pt + key / ps) : 0;
       if (is_k) {
         if (qcount > 0 &&
@@ -360,16 +363,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__
           live = false;
         }
         const uint32_t nlive = __popc(__ballot_sync(0xffffffffu, live));
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], nlive * R * 128u * 2u);
+        if (lane == 0) mbar_arrive_expect_tx(&full[slot], nlive * R * 128u);   // a box per lane
         __syncwarp();
         if (live) {
-          uint8_t* dst = ring + slot * kKvBytes + static_cast<uint32_t>(lane * R) * 128u;
+          uint8_t* dst = ring + slot * kKvBytes + static_cast<uint32_t>(piece * R) * 128u +
+                         half * kKvHalf;
           const int row = page * a.page_rows + t.rec.g * ps + key % ps + head_off;
-          tma_load_2d(dst, map, &full[slot], 0, row);
-          tma_load_2d(dst + kKvHalf, map, &full[slot], 64, row);
+          tma_load_2d(dst, map, &full[slot], half * 64, row);
         }
         if (n + 1 < t.N) {                       // next tile's page ids, used after the wait
-          key = piece_key<CK>(a, t, n + 1, lane);
+          key = piece_key<CK>(a, t, n + 1, piece);
           page = key >= 0 ? __ldg(pt + key / ps) : 0;
         }
       }
