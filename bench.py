@@ -242,9 +242,93 @@ def sage_pairs(p):
     return total
 
 
+# Block-granular counts: the (row, head, key) triples of every selected block (or, for dense
+# prefill, of every 128-key tile a work tile visits) taken whole, before the length, validity,
+# causal and window masks cut it.  A secondary figure beside the visible-pair count: the
+# tensor cores do at least this much work, and visible / block-granular is the share of it that
+# counts toward the headline TFLOPS.
+
+def bsr_block_pairs(p):
+    q = p["q"]
+    B, Sq, Hq, _ = q.shape
+    Hkv = (p["k_cache"] if "k_cache" in p else p["kv_cache"][:, 0]).shape[1]
+    qbs, kvbs = p["q_block_size"], p["kv_block_size"]
+    nqb = -(-Sq // qbs)
+    bptr = p["block_indptr"].numpy().astype(np.int64).reshape(B, Hkv, nqb + 1)
+    rows = np.minimum(qbs, Sq - qbs * np.arange(nqb))
+    nblk = bptr[:, :, 1:] - bptr[:, :, :-1]
+    return int((nblk * rows[None, None, :]).sum()) * kvbs * (Hq // Hkv)
+
+
+def prefill_tile_pairs(p):
+    """Work tiles of 2 x (128 // G) tokens (one sub-tile of 128 // G for D = 256) against the
+    128-key KV tiles that meet their causal / window span, 128 keys each."""
+    qo = p["qo_indptr"].numpy().astype(np.int64)
+    lens = p["seq_lens_kv"].numpy().astype(np.int64)
+    Hq, D = p["q"].shape[1], p["q"].shape[2]
+    G = Hq // p["k_cache"].shape[1]
+    T = (128 // G) * (1 if D == 256 else 2)
+    causal, w = p["mask_type"] == "causal", p["window_left"]
+    total = 0
+    for b in range(lens.size):
+        nq, L = int(qo[b + 1] - qo[b]), int(lens[b])
+        for tok0 in range(0, nq, T):
+            ntok = min(T, nq - tok0)
+            p0 = L - nq + tok0
+            hi = min(L, p0 + ntok) if causal else L
+            lo = max(0, p0 - w) if (causal and w >= 0) else 0
+            if hi > lo:
+                total += (-(-hi // 128) - lo // 128) * 128 * ntok
+    return total * Hq
+
+
+def _qsa_block_pairs(t, g, p):
+    lo, hi = p["lo"].numpy()[t].astype(np.int64), p["hi"].numpy()[t].astype(np.int64)
+    first = p["block_first"].numpy()[g].astype(np.int64)
+    last = p["block_last"].numpy()[g].astype(np.int64)
+    meets = np.maximum(first, lo) <= np.minimum(last, hi)
+    return int((last - first + 1)[meets].sum()) * p["q"].shape[1]
+
+
+def qsa_block_pairs(p):
+    t, g = np.nonzero(p["sel_blocks"].numpy())
+    return _qsa_block_pairs(t, g, p)
+
+
+def qsa_indexed_block_pairs(p):
+    idx = p["sel_indices"].numpy()
+    t, c = np.nonzero((idx >= 0) & (idx < p["block_first"].numel()))
+    return _qsa_block_pairs(t, idx[t, c].astype(np.int64), p)
+
+
+def sage_block_pairs(p):
+    B, H, Sq, _ = p["q_int8"].shape
+    nqb = -(-Sq // 64)
+    rows = np.minimum(64, Sq - 64 * np.arange(nqb))
+    if p["q2k_block_nums"] is not None:
+        n = p["q2k_block_nums"].numpy().astype(np.int64).reshape(B, H, nqb)
+    else:
+        n = np.full((B, H, nqb), p["block_sparse_num"], np.int64)
+    return int((n * rows[None, None, :]).sum()) * 64
+
+
+BLOCK_COUNTERS = {"bsr": bsr_block_pairs, "prefill": prefill_tile_pairs,
+                  "qsa": qsa_block_pairs, "qsa_indexed": qsa_indexed_block_pairs,
+                  "sage": sage_block_pairs}
+
+
 # ----------------------------------------------------------------------------------------
 # one workload on the GPU
 # ----------------------------------------------------------------------------------------
+
+def block_granular(p, kernel_ms):
+    """The labelled secondary figure: block-granular triples and the kernel's rate over them."""
+    nb = BLOCK_COUNTERS[p["form"]](p)
+    D = (p["q"] if "q" in p else p["q_int8"]).shape[-1]
+    return {"pairs": nb, "tflops_kernel": 4 * D * nb / (kernel_ms * 1e-3) / 1e12,
+            "what": "selected blocks (dense prefill: the 128-key tiles each work tile visits) "
+                    "taken whole, before length, validity, causal and window masks"}
+
 
 def main_kernel(p):
     """Name of the kernel that does the attention arithmetic of workload p."""
@@ -859,6 +943,8 @@ def main():
                     "ms_per_step": e2e_ms},
             "gpu_launches": launches,
             "clocks": clocks}
+    if p["form"] != "decode":
+        line["block_granular"] = block_granular(p, kernel_ms)
     del r
     torch.cuda.empty_cache()
 
@@ -917,6 +1003,7 @@ def main():
                                "ms_step": reg / steps, "ms_kernel": kms,
                                "visible_pairs": n, "flops": flops,
                                "kernel": main_kernel(q),
+                               "block_granular": block_granular(q, kms),
                                "traffic": recorded_traffic(main_kernel(q), name)}
                 if q["form"] in ("qsa", "qsa_indexed"):
                     if l2_gbs is None:

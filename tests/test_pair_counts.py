@@ -250,3 +250,93 @@ def test_planted_counter_mistakes_are_caught():
     want_w = brute(dict(pf, window_left=w))
     assert A.prefill_visible_pairs(2, qo, pf["seq_lens_kv"], "causal", w) == want_w
     assert A.prefill_visible_pairs(2, qo, pf["seq_lens_kv"], "causal", w - 1) != want_w
+
+
+# ----------------------------------------------------------------------------------------
+# block-granular counts (the benchmark's secondary figure)
+# ----------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", BSR_CASES)
+def test_bsr_block_pairs(case):
+    """Every listed block taken whole for every row of its q-block: a loop over (row, head)
+    of the row's block count times the block size; never below the visible count."""
+    case = dict(case)
+    p = W.make_bsr_problem(case.pop("seed"), **case)
+    B, Sq, Hq, _ = p["q"].shape
+    Hkv = (p["k_cache"] if "k_cache" in p else p["kv_cache"][:, 0]).shape[1]
+    G, qbs, kvbs = Hq // Hkv, p["q_block_size"], p["kv_block_size"]
+    bp = p["block_indptr"].numpy()
+    want = sum(int(bp[b, h // G, i // qbs + 1] - bp[b, h // G, i // qbs]) * kvbs
+               for b in range(B) for i in range(Sq) for h in range(Hq))
+    assert bench.bsr_block_pairs(p) == want
+    assert want >= _bsr_brute_count(p)
+
+
+def test_bsr_block_pairs_equal_visible_without_masks():
+    """Every block, dense mask, no valid bits, lengths whole blocks: nothing is cut."""
+    p = W.make_bsr_problem(63, B=2, Sq=6, Hq=4, Hkv=2, D=8, seq_lens=[16, 8], page_size=4,
+                           qbs=3, kvbs=4, policy="all", mask_type="dense")
+    assert p["kv_valid_bits"] is None
+    assert bench.bsr_block_pairs(p) == bench.bsr_pairs(p) == _bsr_brute_count(p)
+
+
+@pytest.mark.parametrize("mask,window,D", [("causal", -1, 128), ("causal", 37, 128),
+                                           ("dense", -1, 128), ("causal", 100, 256)])
+def test_prefill_tile_pairs_follow_the_planner(mask, window, D):
+    """The dense prefill count is the oracle planner's tile list (work tiles of 2 x 128 / G
+    tokens, one sub-tile for D = 256) times 128 keys per KV tile and the tile's rows."""
+    from oracle import planner
+    p = W.make_prefill_problem(64, q_lens=[130, 7, 300], prefix_lens=[0, 260, 45], Hq=8,
+                               Hkv=2, D=D, page_size=32, mask_type=mask, window_left=window)
+    G = 4
+    T = (128 // G) * (1 if D == 256 else 2)
+    recs = np.asarray(planner.plan_prefill_tiles(2, p["qo_indptr"], p["seq_lens_kv"], T,
+                                                 mask, window))
+    want = int(((recs[:, 5] - recs[:, 4]) * 128 * recs[:, 3]).sum()) * G
+    assert bench.prefill_tile_pairs(p) == want
+    assert want >= bench.prefill_pairs(p)
+
+
+def test_qsa_block_pairs():
+    """Selected blocks that meet [lo, hi], whole: a loop over (token, block); the indexed form
+    of the same selection gives the same count."""
+    p = W.make_qsa_problem(65, [16, 24], Hq=4, Hkv=2, D=8, block_size=4, n_near=2, n_random=2)
+    sel = p["sel_blocks"].numpy()
+    lo, hi = p["lo"].numpy(), p["hi"].numpy()
+    first, last = p["block_first"].numpy(), p["block_last"].numpy()
+    want = 0
+    for t in range(sel.shape[0]):
+        for g in range(sel.shape[1]):
+            if sel[t, g] and max(first[g], lo[t]) <= min(last[g], hi[t]):
+                want += int(last[g] - first[g] + 1)
+    want *= 4
+    assert bench.qsa_block_pairs(p) == want
+    assert want >= bench.qsa_pairs(p)
+    pi = W.make_qsa_indexed_problem(66, [16, 12, 8], Hq=2, Hkv=1, D=8, block_size=4, n_near=2,
+                                    n_random=2, extra_cols=3, junk=0.5)
+    idx = pi["sel_indices"].numpy()
+    NB = pi["block_first"].numel()
+    as_bitmap = np.zeros((idx.shape[0], NB), np.uint8)
+    for t, c in zip(*np.nonzero((idx >= 0) & (idx < NB))):
+        as_bitmap[t, idx[t, c]] = 1
+    pb = dict(pi, sel_blocks=torch.from_numpy(as_bitmap))
+    assert bench.qsa_indexed_block_pairs(pi) == bench.qsa_block_pairs(pb)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(B=1, H=2, Sq=70, Sk=150, capacity=2, sizes="bhnb", empty_rows=0.3),
+    dict(B=1, H=1, Sq=33, Sk=190, uniform=2, sizes="none"),
+])
+def test_sage_block_pairs(kw):
+    """Each listed 64-key block taken whole for every query of its 64-query block."""
+    p = W.make_sage_problem(67, D=8, **kw)
+    B, H, Sq, _ = p["q_int8"].shape
+    nums = p["q2k_block_nums"]
+    want = 0
+    for b in range(B):
+        for h in range(H):
+            for i in range(Sq):
+                n = int(nums[b, h, i // 64]) if nums is not None else p["block_sparse_num"]
+                want += 64 * n
+    assert bench.sage_block_pairs(p) == want
+    assert want >= bench.sage_pairs(p)
