@@ -67,3 +67,23 @@ def test_reference_arm_does_no_work_off_rank_zero(capsys):
     args = argparse.Namespace(workload=bench.HEADLINE, steps=1, warmup=1)
     assert bench.reference_arm(args, rank=1, world=2) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_the_contract_line(capsys):
+    """Rank 0 of the reference arm times the float64 oracle on a bounded sample of the headline
+    workload and prints one JSON line with the arm's metric, unit and direction, its own CPU
+    baseline and an end-to-end figure with no host-device copies."""
+    import json
+    args = argparse.Namespace(workload=bench.HEADLINE, steps=1, warmup=0)
+    assert bench.reference_arm(args, rank=0, world=1) == 0
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["unit"] == "GB/s" and d["higher_is_better"] is True and d["steps"] == 1
+    assert d["value"] > 0 and d["dtype"] == "f64"
+    assert d["config"]["workload"] == bench.HEADLINE
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
