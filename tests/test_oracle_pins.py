@@ -658,3 +658,66 @@ def test_planted_gqa_mapping_is_caught():
     swapped["q"] = p["q"][:, :, [0, 2, 1, 3]]
     o2, _ = _run_bsa(swapped)
     assert np.abs(o2[:, :, [0, 2, 1, 3]] - ob).max() > 1e-3
+
+
+def test_planted_exclusive_hi_is_caught():
+    """Reading the bitmap form's hi as an exclusive bound (keys lo .. hi - 1) must disagree
+    with the brute force, which keeps hi itself ([QSA] lo/hi are inclusive)."""
+    p = W.make_qsa_problem(46, [20, 12], Hq=4, Hkv=2, D=8, block_size=4, n_near=2, n_random=2)
+    ob, sb = BF.qsa_bruteforce(p)
+    o, s = _run_qsa(p)
+    _close(o, ob)
+    excl = dict(p, hi=p["hi"] - 1)                # the oracle fed the misreading
+    o2, s2 = _run_qsa(excl)
+    fin = np.isfinite(sb) & np.isfinite(np.asarray(s2))
+    assert np.abs(np.asarray(s2)[fin] - np.asarray(sb)[fin]).max() > 1e-3
+
+
+def test_planted_msb_first_valid_bits_are_caught():
+    """Reading kv_valid_bits most significant bit first must disagree with the brute force,
+    which takes bit j & 31 of word j >> 5, least significant first."""
+    p = W.make_bsr_problem(47, B=1, Sq=8, Hq=2, Hkv=1, D=8, seq_lens=[40], page_size=8, qbs=4,
+                           kvbs=8, policy="all", valid_drop=0.3, mask_type="causal")
+    ob, _ = BF.bsa_bruteforce(p)
+    o, _ = _run_bsa(p)
+    _close(o, ob)
+    w = p["kv_valid_bits"].numpy().view(np.uint32)
+    rev = np.zeros_like(w)
+    for k in range(32):                            # bit k moves to bit 31 - k
+        rev |= ((w >> np.uint32(k)) & np.uint32(1)) << np.uint32(31 - k)
+    o2, _ = _run_bsa(dict(p, kv_valid_bits=torch.from_numpy(rev.view(np.int32))))
+    assert np.abs(o2 - ob).max() > 1e-3
+
+
+def test_planted_query_scale_group_is_caught():
+    """Using one query scale per 64 queries (column i // 64) instead of per 32 (column
+    i // 32) must disagree with the brute force."""
+    p = W.make_sage_problem(48, D=8, B=1, H=1, Sq=96, Sk=128, uniform=2, sizes="none")
+    ref = BF.sage_bruteforce(p)
+    _close(_run_sage(p), ref, 1e-12)
+    qs = p["q_scale"].clone()
+    ncol = qs.shape[-1]
+    qs_wrong = qs[..., [min(c // 2, ncol - 1) for c in range(ncol)]]
+    assert not torch.equal(qs_wrong, qs)
+    assert np.abs(_run_sage(dict(p, q_scale=qs_wrong)) - ref).max() > 1e-3
+
+
+def test_planted_merge_weights_are_caught():
+    """Merging split-KV partials with weights exp(LSE_s) left unnormalised (or with equal
+    weights) must disagree with the unsplit softmax that the merge pin compares against."""
+    rng = np.random.default_rng(49)
+    q = rng.standard_normal((1, 2, 16))
+    K = rng.standard_normal((60, 16))
+    V = rng.standard_normal((60, 16))
+    vis = np.ones((1, 60), bool)
+    o_full, _ = A.masked_softmax_attention(q, K, V, vis, 0.25)
+    parts = [A.masked_softmax_attention(q, K[a:b], V[a:b], vis[:, a:b], 0.25)
+             for a, b in ((0, 17), (17, 60))]
+    o_parts = np.stack([x[0] for x in parts])
+    lse = np.stack([x[1] for x in parts])
+    unnormalised = (np.exp(lse)[..., None] * o_parts).sum(0)
+    equal = o_parts.mean(0)
+    assert np.abs(unnormalised - o_full).max() > 1e-3
+    assert np.abs(equal - o_full).max() > 1e-3
+    o, _ = A.merge_partials([x[0] for x in parts], [x[1] for x in parts])
+    _close(o, o_full)
