@@ -721,3 +721,22 @@ def test_planted_merge_weights_are_caught():
     assert np.abs(equal - o_full).max() > 1e-3
     o, _ = A.merge_partials([x[0] for x in parts], [x[1] for x in parts])
     _close(o, o_full)
+
+
+def test_planted_window_of_w_keys_is_caught():
+    """A window of w keys (p - w < j) instead of w + 1 (p - w <= j, the query's own position
+    counted inside it) must disagree with the brute force, for prefill and for decode."""
+    p = W.make_prefill_problem(50, q_lens=[5, 3], prefix_lens=[6, 2], Hq=2, Hkv=1, D=8,
+                               page_size=4, mask_type="causal", window_left=3)
+    ob, _ = BF.prefill_bruteforce(p)
+    o, _ = _run_prefill(p)
+    _close(o, ob)
+    o2, _ = _run_prefill(dict(p, window_left=2))
+    assert np.abs(o2 - ob).max() > 1e-3
+    d = W.make_decode_problem(51, [9, 14], Hq=2, Hkv=1, D=8, page_size=4, q_lens=[1, 3],
+                              mask_type="causal", window_left=4)
+    db, _ = BF.decode_bruteforce(d)
+    o, _ = _run_decode(d)
+    _close(o, db)
+    o2, _ = _run_decode(dict(d, window_left=3))
+    assert np.abs(o2 - db).max() > 1e-3
