@@ -121,3 +121,38 @@ def test_sparse_run_argument_checks(lib):
     assert run(q=None) == pkb.ERR_INVALID_ARGUMENT
     assert run(ws=None) == pkb.ERR_WORKSPACE
     assert run(ws_bytes=16) == pkb.ERR_WORKSPACE
+    # block-sparse: the output must start on a 16-byte boundary as well
+    m.kv_indptr_dev = m.block_indptr_dev = m.seq_lens_kv_dev = A16
+    assert run(out=MIS8) == pkb.ERR_INVALID_ARGUMENT
+    assert run(k=MIS8) == pkb.ERR_INVALID_ARGUMENT
+
+
+@pytest.mark.parametrize("form", [1, 2])
+def test_bitmap_run_argument_checks(lib, form):
+    """The bitmap and indexed forms refuse a missing V, missing bounds, unaligned tensors
+    (out_fp32 included) and an unsupported head size or group before any work."""
+    def params(**kw):
+        p = pkb.AttnParams(form=form, batch=1, q_len=64, num_qo_heads=24, num_kv_heads=2,
+                           head_dim=256, num_blocks=16, block_size=4, max_blocks_per_query=16,
+                           sm_scale=0.0, index_width=8)
+        for k, v in kw.items():
+            setattr(p, k, v)
+        return p
+
+    m = pkb.AttnMeta(lo_dev=A16, hi_dev=A16, block_first_dev=A16, block_last_dev=A16,
+                     sel_blocks_dev=A16, sel_indices_dev=A16, blk_base_dev=A16, tok_base_dev=A16)
+
+    def run(p, q=A16, k=A16, v=A16, out=A16, out32=None, meta=m):
+        n = pkb.paged_attn_workspace_size(p)
+        return lib.paged_attn_run(C.byref(p), C.byref(meta), q, k, v, out, out32, None, A16,
+                                  max(n, 16), None)
+
+    p = params()
+    assert run(p, v=None) == pkb.ERR_INVALID_ARGUMENT
+    for bad in (dict(q=MIS8), dict(k=MIS8), dict(v=MIS8), dict(out=MIS8), dict(out32=MIS8)):
+        assert run(p, **bad) == pkb.ERR_INVALID_ARGUMENT, bad
+    no_hi = pkb.AttnMeta(lo_dev=A16, block_first_dev=A16, block_last_dev=A16,
+                         sel_blocks_dev=A16, sel_indices_dev=A16)
+    assert run(p, meta=no_hi) == pkb.ERR_INVALID_ARGUMENT
+    assert run(params(head_dim=128)) == pkb.ERR_INVALID_ARGUMENT        # D = 256 only
+    assert run(params(num_qo_heads=40, num_kv_heads=2)) == pkb.ERR_UNSUPPORTED   # G = 20 > 16
